@@ -1,0 +1,209 @@
+"""Seeded synthetic inputs for the Gated DeltaNet speculative verify/commit path.
+
+This module only draws random tensors with the shapes and value distributions of
+the workloads and rounds them to their storage types.  It holds none of the
+method's arithmetic, so both the CUDA path and the float64 oracle can be fed from
+it without sharing any computation.
+
+Value recipe (every workload):
+  * q, k  ~ N(0, 1) per element, L2-normalised per (token, head) in float32, then
+            rounded to bfloat16 (round to nearest even) unless the workload keeps
+            float32.  The rounded values are the inputs; nothing renormalises them.
+  * v     ~ N(0, 1), rounded the same way.
+  * alpha = exp(-softplus(x)) = 1 / (1 + exp(x)),  x ~ N(0, 1), float32.
+  * beta  = sigmoid(y) = 1 / (1 + exp(-y)),        y ~ N(0, 1), float32.
+  * S0    = 0.1 * N(0, 1) per element, float32 (the standard deviation is 0.1).
+  * slot ids: the first B entries of a random permutation of the pool slots
+    (distinct and non-contiguous).
+  * accepted length a_r: uniform on {0..T_r} or Binomial(T, 0.75), per workload.
+
+The state tile of one (request, head) is stored key-index-major: element (i, j)
+with i the key index (0..dk-1) and j the value index (0..dv-1), value index
+contiguous.
+"""
+from __future__ import annotations
+
+import dataclasses
+from typing import List, Optional, Sequence
+
+import numpy as np
+
+__all__ = [
+    "Problem",
+    "WORKLOADS",
+    "round_to_bf16",
+    "bf16_bits",
+    "make_problem",
+    "make_custom",
+    "make_layers",
+    "POOL_SENTINEL_BITS",
+]
+
+# Bit pattern (a quiet NaN with a payload) written into pool slots that no
+# request names, so a stray write by any implementation shows up bitwise.
+POOL_SENTINEL_BITS = 0x7FC0BEEF
+
+
+def round_to_bf16(x: np.ndarray) -> np.ndarray:
+    """Round float32 values to the nearest bfloat16 (ties to even); float32 out."""
+    x = np.ascontiguousarray(x, dtype=np.float32)
+    b = x.view(np.uint32).astype(np.uint64)
+    b = (b + 0x7FFF + ((b >> 16) & 1)) >> 16
+    return (b.astype(np.uint32) << np.uint32(16)).view(np.float32)
+
+
+def bf16_bits(x: np.ndarray) -> np.ndarray:
+    """uint16 bfloat16 encodings of float32 values that are already bf16-exact."""
+    u = np.ascontiguousarray(x, dtype=np.float32).view(np.uint32)
+    if np.any(u & 0xFFFF):
+        raise ValueError("bf16_bits: values are not bfloat16-representable")
+    return (u >> 16).astype(np.uint16)
+
+
+@dataclasses.dataclass
+class Problem:
+    """One layer-call's inputs, host side (numpy)."""
+
+    name: str
+    batch: int
+    heads: int
+    dk: int
+    dv: int
+    max_T: int
+    ragged: bool
+    qkv_dtype: str  # "bf16" or "fp32": how q, k, v are stored for the kernels
+    cu_seqlens: np.ndarray  # int32 [B+1], token rows of request r are [cu[r], cu[r+1])
+    q: np.ndarray  # float32 [N_tok][H][dk]
+    k: np.ndarray  # float32 [N_tok][H][dk]
+    v: np.ndarray  # float32 [N_tok][H][dv]
+    alpha: np.ndarray  # float32 [N_tok][H]
+    beta: np.ndarray  # float32 [N_tok][H]
+    pool_slots: int
+    slot_ids: np.ndarray  # int32 [B]
+    accepted: np.ndarray  # int32 [B]
+    s0: np.ndarray  # float32 [B][H][dk][dv], the state held in slot slot_ids[r]
+
+    @property
+    def n_tok(self) -> int:
+        return int(self.cu_seqlens[-1])
+
+    @property
+    def lengths(self) -> np.ndarray:
+        return np.diff(self.cu_seqlens).astype(np.int32)
+
+    @property
+    def units(self) -> int:
+        return self.batch * self.heads
+
+
+def _draw_tokens(rng: np.random.Generator, n_tok: int, heads: int, dk: int, dv: int,
+                 qkv_dtype: str):
+    def unit_rows(d):
+        x = rng.standard_normal((n_tok, heads, d), dtype=np.float32)
+        nrm = np.sqrt(np.sum(x * x, axis=-1, keepdims=True, dtype=np.float32))
+        return (x / np.maximum(nrm, np.float32(1e-30))).astype(np.float32)
+
+    q = unit_rows(dk)
+    k = unit_rows(dk)
+    v = rng.standard_normal((n_tok, heads, dv), dtype=np.float32)
+    if qkv_dtype == "bf16":
+        q, k, v = round_to_bf16(q), round_to_bf16(k), round_to_bf16(v)
+    elif qkv_dtype != "fp32":
+        raise ValueError(qkv_dtype)
+    x = rng.standard_normal((n_tok, heads), dtype=np.float32).astype(np.float64)
+    y = rng.standard_normal((n_tok, heads), dtype=np.float32).astype(np.float64)
+    alpha = (1.0 / (1.0 + np.exp(x))).astype(np.float32)
+    beta = (1.0 / (1.0 + np.exp(-y))).astype(np.float32)
+    return q, k, v, alpha, beta
+
+
+def _draw_accepted(rng: np.random.Generator, lengths: np.ndarray, dist: str) -> np.ndarray:
+    if dist == "uniform":
+        return np.array([rng.integers(0, int(L) + 1) for L in lengths], dtype=np.int32)
+    if dist == "binom":
+        a = rng.binomial(int(lengths.max()), 0.75, size=len(lengths))
+        return np.minimum(a, lengths).astype(np.int32)
+    if dist == "full":
+        return lengths.astype(np.int32).copy()
+    if dist == "zero":
+        return np.zeros(len(lengths), dtype=np.int32)
+    raise ValueError(dist)
+
+
+def make_custom(*, batch: int, heads: int, dk: int, dv: int,
+                T: Optional[int] = None, lengths: Optional[Sequence[int]] = None,
+                qkv_dtype: str = "bf16", pool_slots: Optional[int] = None,
+                accept: str = "uniform", seed: int = 0, layer: int = 0,
+                slot_ids: Optional[np.ndarray] = None,
+                accepted: Optional[np.ndarray] = None,
+                name: str = "custom") -> Problem:
+    """Draw one problem.  Give either a uniform draft length T or per-request lengths.
+
+    Slot ids and accepted lengths come from a stream that does not depend on
+    `layer`, so the layers of one multi-layer step share them (one request keeps
+    its slot index and its accepted length in every layer).
+    """
+    if (T is None) == (lengths is None):
+        raise ValueError("give exactly one of T or lengths")
+    ragged = lengths is not None
+    lens = np.full(batch, T, dtype=np.int32) if T is not None else np.asarray(lengths, np.int32)
+    if lens.shape != (batch,) or np.any(lens < 0):
+        raise ValueError("bad lengths")
+    cu = np.zeros(batch + 1, dtype=np.int32)
+    cu[1:] = np.cumsum(lens)
+    pool_slots = batch if pool_slots is None else pool_slots
+    meta = np.random.default_rng(np.random.SeedSequence([seed, 0]))
+    data = np.random.default_rng(np.random.SeedSequence([seed, 1 + layer]))
+    if slot_ids is None:
+        slot_ids = meta.permutation(pool_slots)[:batch].astype(np.int32)
+    if accepted is None:
+        accepted = _draw_accepted(meta, lens, accept)
+    q, k, v, alpha, beta = _draw_tokens(data, int(cu[-1]), heads, dk, dv, qkv_dtype)
+    s0 = (np.float32(0.1) * data.standard_normal((batch, heads, dk, dv), dtype=np.float32))
+    return Problem(name=name, batch=batch, heads=heads, dk=dk, dv=dv,
+                   max_T=int(lens.max()) if batch else 0, ragged=ragged,
+                   qkv_dtype=qkv_dtype, cu_seqlens=cu, q=q, k=k, v=v, alpha=alpha,
+                   beta=beta, pool_slots=pool_slots,
+                   slot_ids=np.asarray(slot_ids, np.int32),
+                   accepted=np.asarray(accepted, np.int32), s0=s0.astype(np.float32))
+
+
+# The five workloads: (name, recipe).  Seeds are 1000 + workload index.
+WORKLOADS = {
+    # batch 1, 2 heads, dk = dv = 32, 4 draft tokens, everything float32.
+    "tiny_b1_h2_d32_t4": dict(batch=1, heads=2, dk=32, dv=32, T=4, qkv_dtype="fp32",
+                              pool_slots=1, accept="uniform", seed=1000),
+    # batch 8, 16 heads, dk = dv = 128, 8 draft tokens, 64-slot pool.
+    "b8_h16_d128_t8": dict(batch=8, heads=16, dk=128, dv=128, T=8, qkv_dtype="bf16",
+                           pool_slots=64, accept="uniform", seed=1001),
+    # batch 32, 32 heads, 16 draft tokens, 256-slot pool, ~12 accepted tokens.
+    "b32_h32_d128_t16": dict(batch=32, heads=32, dk=128, dv=128, T=16, qkv_dtype="bf16",
+                             pool_slots=256, accept="binom", seed=1002),
+    # batch 64, 32 heads, 16 draft tokens, 24 layers, 512 slots per layer.
+    "b64_h32_d128_t16_x24": dict(batch=64, heads=32, dk=128, dv=128, T=16, qkv_dtype="bf16",
+                                 pool_slots=512, accept="binom", seed=1003, layers=24),
+    # batch 128 ragged (draft length uniform in 1..16), 32 heads, 1024-slot pool.
+    "b128_h32_d128_ragged16": dict(batch=128, heads=32, dk=128, dv=128, lengths="u1_16",
+                                   qkv_dtype="bf16", pool_slots=1024, accept="uniform",
+                                   seed=1004),
+}
+
+
+def _recipe_kwargs(name: str) -> dict:
+    spec = dict(WORKLOADS[name])
+    spec.pop("layers", None)
+    if spec.get("lengths") == "u1_16":
+        rng = np.random.default_rng(np.random.SeedSequence([spec["seed"], 999]))
+        spec["lengths"] = rng.integers(1, 17, size=spec["batch"]).astype(np.int32)
+    return spec
+
+
+def make_problem(name: str, layer: int = 0) -> Problem:
+    """The named workload (one layer of it for the multi-layer one)."""
+    return make_custom(name=name, layer=layer, **_recipe_kwargs(name))
+
+
+def make_layers(name: str) -> List[Problem]:
+    """Every layer of a workload (one element for single-layer workloads)."""
+    n = WORKLOADS[name].get("layers", 1)
+    return [make_problem(name, layer=l) for l in range(n)]
