@@ -1,0 +1,444 @@
+#!/usr/bin/env python
+"""Benchmark of the Gated DeltaNet speculative verify/commit path on one GB300.
+
+Metric: microseconds per layer-call (verify + commit of one layer) and the
+achieved HBM GB/s of that layer-call, from the algorithmic bytes the method
+must move (each checkpoint read, the tokens' q/k/v/gates, the outputs, the
+committed states).
+
+Workload (default): batch 64, 32 heads, dk = dv = 128, 16 draft tokens per
+request, 24 independent layers called back to back, each request's state in a
+24 x 512-slot fp32 pool (24 GiB), accepted lengths ~ Binomial(16, 0.75).  One
+step = for every layer: gdn_verify then gdn_commit.  Every step touches about
+11 GB, far more than the 129 MB L2, so no flush is needed between steps.
+
+  python bench.py [--steps K] [--warmup W] [--gpus N] [--impl ours|reference]
+
+--impl reference times the float64 CPU oracle on a bounded sample of the same
+workload (the slow reference this path is checked against).  Under torchrun
+(N > 1) every rank runs its own replica of the workload (weak scaling; no data
+is exchanged); the step time is the maximum over ranks.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import re
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from speculative_decode_gated_gb300 import inputs  # noqa: E402
+
+WORKLOAD = "b64_h32_d128_t16_x24"
+METRIC = "us per layer-call (verify+commit) and achieved HBM GB/s vs ~8 TB/s, 1xGB300"
+UNIT = "us/layer-call"
+NOMINAL_HBM_GBS = 8000.0
+MODE_NAME = {"v": "verify", "c": "commit", "f": "fused"}
+
+
+# ----------------------------------------------------------------- accounting
+
+def alg_bytes(prob, mode: str) -> int:
+    """Minimum bytes the method moves for one call, per unit (request, head):
+    verify  = state read + T (q, k, v, alpha, beta) + T o
+    commit  = [a > 0] (state read + state write) + a (k, v, alpha, beta)
+    fused   = state read + [a > 0] state write + T (q, k, v, alpha, beta, o)
+    plus per-request metadata (slot id, accepted length, sequence offsets)."""
+    esz = 2 if prob.qkv_dtype == "bf16" else 4
+    tile = prob.dk * prob.dv * 4
+    q_k = prob.dk * esz
+    v_ = prob.dv * esz
+    o_ = prob.dv * 4
+    lens = prob.lengths.astype(np.int64)
+    acc = prob.accepted.astype(np.int64)
+    H = prob.heads
+    meta = prob.batch * (4 + (4 if mode != "verify" else 0) + (4 if prob.ragged else 0))
+    if mode == "verify":
+        per_r = tile + lens * (2 * q_k + v_ + 8 + o_)
+    elif mode == "commit":
+        per_r = (acc > 0) * (2 * tile) + acc * (q_k + v_ + 8)
+    else:
+        per_r = tile + (acc > 0) * tile + lens * (2 * q_k + v_ + 8 + o_)
+    return int(H * per_r.sum() + meta)
+
+
+# ----------------------------------------------------------------- clocks
+
+class ClockSampler:
+    """nvidia-smi clock / throttle-reason samples while the timed region runs."""
+
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.file = None
+
+    def start(self):
+        try:
+            self.file = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.QUERY}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=self.file, stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.file.flush()
+        self.file.seek(0)
+        rows = [l.strip().split(", ") for l in self.file.read().splitlines() if l.strip()]
+        os.unlink(self.file.name)
+        sm, smax, power, reasons = [], [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for row in rows:
+            if len(row) < 9:
+                continue
+            try:
+                sm.append(float(row[1]))
+                smax.append(float(row[2]))
+                power.append(float(row[3]))
+            except ValueError:
+                continue
+            for name, flag in zip(names, row[5:9]):
+                if flag.strip().lower() in ("active", "1"):
+                    reasons.add(name)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax),
+                "power_w_max": max(power) if power else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ----------------------------------------------------------------- helpers
+
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    return 6800.0, "fallback"
+
+
+def profile_traffic(kernel_tag: str, workload: str):
+    """DRAM bytes per launch from the committed ncu summary of this kernel, if the
+    kernel source has not changed since the capture (else None)."""
+    path = os.path.join(ROOT, "profiles", f"{kernel_tag}_{workload}.md")
+    if not os.path.exists(path):
+        return None
+    text = open(path).read()
+    m_b = re.search(r"traffic_bytes_per_launch:\s*([0-9.]+)", text)
+    m_h = re.search(r"source_sha256:\s*([0-9a-f]{64})", text)
+    m_f = re.search(r"source_file:\s*(\S+)", text)
+    if not (m_b and m_h and m_f):
+        return None
+    src = os.path.join(ROOT, m_f.group(1))
+    if not os.path.exists(src):
+        return None
+    if hashlib.sha256(open(src, "rb").read()).hexdigest() != m_h.group(1):
+        return None
+    return float(m_b.group(1))
+
+
+def cpu_oracle_time(prob, n_units: int, threads: int):
+    """Seconds the float64 oracle takes for verify + commit of n_units sampled
+    units of one layer, and the per-layer-call extrapolation in microseconds."""
+    import dataclasses
+
+    import oracle
+
+    # float64 copies up front, so the timed region holds the recurrence only
+    p64 = dataclasses.replace(prob, **{f: np.asarray(getattr(prob, f), np.float64)
+                                       for f in ("q", "k", "v", "alpha", "beta", "s0")})
+    rng = np.random.default_rng(7)
+    units = np.sort(rng.choice(prob.units, size=min(n_units, prob.units), replace=False))
+    oracle.load()
+    t0 = time.perf_counter()
+    oracle.run_units(p64, units, want_o=True, want_state=False, threads=threads)
+    oracle.run_units(p64, units, want_o=False, want_state=True, threads=threads)
+    dt = time.perf_counter() - t0
+    return dt, dt / len(units) * prob.units * 1e6, len(units)
+
+
+# ----------------------------------------------------------------- arms
+
+def run_reference(args, rank):
+    if rank != 0:
+        return
+    prob = inputs.make_problem(args.workload, layer=0)
+    threads = os.cpu_count() or 1
+    for _ in range(args.warmup):
+        cpu_oracle_time(prob, args.ref_units, threads)
+    times = []
+    for _ in range(args.steps):
+        _, us, n = cpu_oracle_time(prob, args.ref_units, threads)
+        times.append(us)
+    value = statistics.median(times)
+    sample = (f"{args.ref_units} of {prob.units} units of layer 0 per step "
+              f"(verify pass + commit pass), scaled to a full layer-call")
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT,
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": value / 1e3, "higher_is_better": False, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": args.workload, "order": "verify then commit per layer"},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": threads, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def run_ours(args, rank, world, local_rank):
+    import torch
+    import torch.distributed as dist
+
+    from speculative_decode_gated_gb300 import binding, staging
+
+    dev = torch.device("cuda", local_rank)
+    torch.cuda.set_device(dev)
+    binding.lib()  # fails loudly if the CUDA library is missing
+    name = args.workload
+    layers = inputs.make_layers(name)
+    L = len(layers)
+    p0 = layers[0]
+    pool = staging.new_pool(p0.pool_slots, p0.heads, p0.dk, p0.dv, dev, fill="zero",
+                            layers=L if L > 1 else None)
+    dps = [staging.DeviceProblem(pr, dev, pool=(pool[l] if L > 1 else pool), algo=args.algo)
+           for l, pr in enumerate(layers)]
+    fused = args.mode == "fused"
+    kinds = ["f"] if fused else ["v", "c"]
+    bytes_of = {m: [alg_bytes(pr, MODE_NAME[m]) for pr in layers] for m in ("v", "c", "f")}
+    bytes_call = sum(sum(bytes_of[m]) for m in kinds) / L
+    stream = torch.cuda.current_stream(dev)
+
+    if args.order == "engine" and not fused:
+        order = [(d, "v") for d in dps] + [(d, "c") for d in dps]
+    else:
+        order = [(d, m) for d in dps for m in kinds]
+    calls = [(m, d.launcher(MODE_NAME[m], stream)) for d, m in order]
+
+    def step(events=None):
+        if events is None:
+            for _, call in calls:
+                call()
+            return
+        for m, call in calls:
+            a, b = events[m][events["i"][m]]
+            a.record(stream)
+            call()
+            b.record(stream)
+            events["i"][m] += 1
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    for d in dps:
+        if binding.gdn_read_device_error(d.c) != 0:
+            raise RuntimeError("device-side argument error during warm-up")
+
+    def barrier():
+        if world > 1:
+            dist.barrier()
+
+    n_per_step = {m: sum(1 for _, mm in order if mm == m) for m in kinds}
+    events = {m: [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                  for _ in range(n_per_step[m] * args.steps)] for m in kinds}
+    events["i"] = {m: 0 for m in kinds}
+    clocks = ClockSampler(local_rank)
+    clocks.start()
+    time.sleep(0.3)
+    barrier()
+    torch.cuda.synchronize()
+    t_start = torch.cuda.Event(enable_timing=True)
+    t_end = torch.cuda.Event(enable_timing=True)
+    t_start.record(stream)
+    for _ in range(args.steps):
+        step(events)
+    t_end.record(stream)
+    torch.cuda.synchronize()
+    barrier()
+    clk = clocks.stop()
+    ms_total = t_start.elapsed_time(t_end)
+    if world > 1:
+        t = torch.tensor([ms_total], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms_total = float(t.item())
+    ms_step = ms_total / args.steps
+    us_call = ms_step * 1e3 / L
+
+    avg_ms = {m: statistics.fmean(a.elapsed_time(b) for a, b in events[m]) for m in kinds}
+    dominant = max(kinds, key=lambda m: avg_ms[m] * n_per_step[m])
+    per_launch_bytes = {m: sum(bytes_of[m]) / L for m in kinds}
+    peak, peak_kind = measured_peaks()
+    achieved = per_launch_bytes[dominant] / (avg_ms[dominant] * 1e-3) / 1e9
+    algo_used = binding.gdn_select_algo(dps[0].c)
+    ktag = (("gdn_chunk" if algo_used == binding.GDN_ALGO_CHUNK else "gdn_recurrent")
+            + "_" + MODE_NAME[dominant])
+    traffic = profile_traffic(ktag, name)
+
+    e2e = run_e2e(args, dps, stream, dev, fused) if not args.no_e2e else None
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        threads = os.cpu_count() or 1
+        dt, us, n = cpu_oracle_time(p0, args.cpu_units, threads)
+        cpu = {"value": us, "unit": UNIT, "cores": threads, "kind": "oracle",
+               "sample": f"{n} of {p0.units} units of layer 0, verify pass + commit pass, "
+                         f"{dt:.1f} s wall, scaled to a full layer-call"}
+
+    if rank == 0:
+        gbs = bytes_call / (us_call * 1e-6) / 1e9
+        line = {
+            "metric": METRIC, "value": us_call, "unit": UNIT, "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step,
+            "higher_is_better": False, "scaling": "weak", "vs_baseline": None,
+            "dtype": "f32", "data": "synthetic",
+            "config": {
+                "workload": name,
+                "description": (f"batch {p0.batch}, heads {p0.heads}, dk {p0.dk}, dv {p0.dv}, "
+                                f"draft {p0.max_T}, {L} layer(s), pool {p0.pool_slots} slots/layer, "
+                                f"q/k/v {p0.qkv_dtype}, gates/state/o fp32"),
+                "order": ("fused per layer" if fused else
+                          "verify then commit per layer" if args.order == "interleaved" else
+                          "all verifies then all commits"),
+                "l2": "inputs larger than L2 (each step touches ~%.1f GB)" % (bytes_call * L / 1e9),
+                "algo": {1: "recurrent", 2: "chunk"}.get(algo_used, str(algo_used)),
+            },
+            "achieved_gbs": gbs,
+            "frac_of_8tbs": gbs / NOMINAL_HBM_GBS,
+            "frac_of_measured_hbm": gbs / peak,
+            "alg_bytes_per_layer_call": bytes_call,
+            "kernel_us": {MODE_NAME[m]: avg_ms[m] * 1e3 for m in kinds},
+            "roofline": {"bound": "hbm", "kernel": ktag, "achieved": achieved, "peak": peak,
+                         "peak_source": peak_kind, "unit": "GB/s", "frac": achieved / peak,
+                         "traffic": traffic, "alg_bytes_per_launch": per_launch_bytes[dominant]},
+            "gpu_launches": args.steps * len(calls),
+            "clocks": clk,
+            "e2e": e2e,
+            "cpu_baseline": cpu,
+        }
+        print(json.dumps(line), flush=True)
+
+
+def run_e2e(args, dps, stream, dev, fused):
+    """Same metric end to end: every step copies each layer's q/k/v/gates/accepted
+    from pinned host memory and reads every layer's o back, overlapped on copy
+    streams with the kernels of other layers."""
+    import torch
+
+    host_in = [[t.cpu().pin_memory() for t in (d.q, d.k, d.v, d.alpha, d.beta, d.accepted)]
+               for d in dps]
+    host_o = [torch.empty(d.o.shape, dtype=d.o.dtype).pin_memory() for d in dps]
+    h2d = torch.cuda.Stream(dev)
+    d2h = torch.cuda.Stream(dev)
+    L = len(dps)
+    ev_in = [torch.cuda.Event() for _ in range(L)]
+    ev_used = [torch.cuda.Event() for _ in range(L)]
+    ev_o = [torch.cuda.Event() for _ in range(L)]
+    ev_read = [torch.cuda.Event() for _ in range(L)]
+    bi = sum(sum(t.numel() * t.element_size() for t in hs) for hs in host_in)
+    bo = sum(t.numel() * t.element_size() for t in host_o)
+    kinds = ["fused"] if fused else ["verify", "commit"]
+    calls = [{m: d.launcher(m, stream) for m in kinds} for d in dps]
+
+    def one_step():
+        for l, d in enumerate(dps):
+            with torch.cuda.stream(h2d):
+                h2d.wait_event(ev_used[l])
+                for dst, src in zip((d.q, d.k, d.v, d.alpha, d.beta, d.accepted), host_in[l]):
+                    dst.copy_(src, non_blocking=True)
+                ev_in[l].record(h2d)
+            stream.wait_event(ev_in[l])
+            stream.wait_event(ev_read[l])
+            if fused:
+                calls[l]["fused"]()
+                ev_o[l].record(stream)
+            else:
+                calls[l]["verify"]()
+                ev_o[l].record(stream)
+                calls[l]["commit"]()
+            ev_used[l].record(stream)
+            with torch.cuda.stream(d2h):
+                d2h.wait_event(ev_o[l])
+                host_o[l].copy_(d.o, non_blocking=True)
+                ev_read[l].record(d2h)
+
+    for _ in range(max(args.warmup, 1)):
+        one_step()
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    for _ in range(args.e2e_steps):
+        one_step()
+    torch.cuda.synchronize()
+    dt = time.perf_counter() - t0
+    return {"value": dt / args.e2e_steps * 1e6 / L, "unit": UNIT,
+            "h2d_bytes_per_step": bi, "d2h_bytes_per_step": bo, "steps": args.e2e_steps}
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__,
+                                 formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=300)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default=WORKLOAD, choices=sorted(inputs.WORKLOADS))
+    ap.add_argument("--mode", choices=["separate", "fused"], default=None,
+                    help="separate verify + commit (default) or the fused call")
+    ap.add_argument("--order", choices=["interleaved", "engine"], default="interleaved")
+    ap.add_argument("--algo", type=int, default=0, help="0 auto, 1 recurrent, 2 chunk")
+    ap.add_argument("--cpu-units", type=int, default=256)
+    ap.add_argument("--ref-units", type=int, default=64)
+    ap.add_argument("--e2e-steps", type=int, default=20)
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.mode is None:
+        args.mode = "fused" if "ragged" in args.workload else "separate"
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    if args.impl == "reference":
+        run_reference(args, rank)
+        return
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+
+        torch.cuda.set_device(local_rank)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local_rank))
+    try:
+        run_ours(args, rank, world, local_rank)
+    finally:
+        if world > 1:
+            import torch.distributed as dist
+
+            dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,158 @@
+/*
+ * gdn.h - C ABI of the Gated DeltaNet speculative verify/commit library (libgdn.so).
+ *
+ * The operation.  Gated DeltaNet (GDN) layers keep a fixed-size recurrent state
+ * per request and head, read and rewritten for every token; ReplaySSM keeps a
+ * checkpoint of that state, computes the draft tokens' outputs from the
+ * checkpoint and the buffered inputs, and on rejection keeps only the accepted
+ * prefix (OCRia write-up "OCRia 推理栈：单卡 B200 提速近 10 倍", section "Make
+ * speculative verification cheaper"; the same in "How OCRia achieved a 10x
+ * inference speedup on B200 GPUs", section "Wie es funktioniert").  The state
+ * update is the gated delta rule, with S the dv x dk state of one unit
+ * (request r, head h):
+ *
+ *     S_t = alpha_t S_{t-1} (I - beta_t k_t k_t^T) + beta_t v_t k_t^T
+ *     o_t = S_t q_t
+ *
+ * Layout (all row-major, all device memory, all caller-owned):
+ *   state tile  float32 [dk][dv], tile[i][j] = S[j][i] (key index i is the row,
+ *               value index j contiguous); 64 KiB at dk = dv = 128.
+ *   pool        float32 [pool_slots][heads][dk][dv]; request r's checkpoint is
+ *               pool[slot_ids[r]][h].
+ *   q, k        [N_tok][heads][dk], v [N_tok][heads][dv], bfloat16 or float32
+ *               (qkv_dtype); token rows of request r are [cu[r], cu[r+1]) with
+ *               cu = cu_seqlens, or [r*max_T, (r+1)*max_T) when cu_seqlens is NULL.
+ *   alpha, beta float32 [N_tok][heads] (alpha is the decay gate, beta the write
+ *               strength; both given directly, no log-space or activation applied).
+ *   o           float32 [N_tok][heads][dv].
+ *   accepted    int32 [batch], a_r in [0, T_r].
+ *
+ * Calls.  All compute calls are asynchronous on `stream`; they validate their
+ * arguments on the host first and return an error without launching anything
+ * if a check fails.  They allocate no memory and keep no state between calls.
+ *   gdn_verify               o_t for every draft token; never writes the pool.
+ *   gdn_commit               pool[slot_r][h] <- state after a_r tokens, for
+ *                            every r with a_r > 0; slots with a_r = 0 and slots
+ *                            no request names are left bit-identical.
+ *   gdn_verify_commit_fused  both in one pass: reads each checkpoint once,
+ *                            writes o for every token and the state once.
+ *
+ * Device-side argument errors (a slot id outside [0, pool_slots), a_r outside
+ * [0, T_r], a ragged length outside [0, max_T]) cannot be seen on the host
+ * without a synchronisation; the kernel ORs a GDN_DEVERR_* bit into *dev_err
+ * (when dev_err is not NULL) and skips that unit, writing nothing for it.  It
+ * never traps.  Duplicate slot ids among the requests of one call are a
+ * precondition violation: commit results are then undefined.
+ */
+#ifndef GDN_H
+#define GDN_H
+
+#include <stdint.h>
+
+#include <cuda_runtime_api.h>
+
+#if defined(__GNUC__)
+#define GDN_API __attribute__((visibility("default")))
+#else
+#define GDN_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum gdn_status {
+    GDN_OK = 0,
+    GDN_ERR_NULL_PTR = 1,     /* a required pointer is NULL */
+    GDN_ERR_BAD_DIM = 2,      /* batch/heads/max_T/pool_slots/n_tok out of range */
+    GDN_ERR_BAD_DTYPE = 3,    /* qkv_dtype is not a gdn_dtype */
+    GDN_ERR_UNSUPPORTED = 4,  /* dk/dv (or a forced algo) not supported */
+    GDN_ERR_DEVICE_ARG = 5,   /* reported by gdn_read_device_error only */
+    GDN_ERR_CUDA = 6,         /* a CUDA call failed; see gdn_last_error_string */
+    GDN_ERR_ALIGN = 7,        /* a pointer is not aligned (16 bytes for q/k/v/pool/o) */
+    GDN_ERR_ALIAS = 8         /* o overlaps an input, or the pool overlaps q/k/v/o */
+} gdn_status;
+
+typedef enum gdn_dtype {
+    GDN_FP32 = 0,
+    GDN_BF16 = 1
+} gdn_dtype;
+
+/* Which kernel runs.  AUTO: the chunked tensor-core kernel where it applies
+ * (bf16 q/k/v, dk = dv = 128, max_T <= 16), else the recurrent kernel. */
+typedef enum gdn_algo {
+    GDN_ALGO_AUTO = 0,
+    GDN_ALGO_RECURRENT = 1,   /* per-token update on CUDA cores, any supported shape */
+    GDN_ALGO_CHUNK = 2        /* WY/chunk form, bf16 mma.sync for the state products */
+} gdn_algo;
+
+/* Bits ORed into *dev_err by the kernels. */
+#define GDN_DEVERR_SLOT     1   /* slot_ids[r] outside [0, pool_slots) */
+#define GDN_DEVERR_ACCEPTED 2   /* accepted[r] outside [0, T_r]        */
+#define GDN_DEVERR_SEQLEN   4   /* cu[r+1] - cu[r] outside [0, max_T], or rows outside [0, n_tok) */
+
+/* Limits checked on the host. */
+#define GDN_MAX_T 1024          /* draft tokens per request */
+
+typedef struct gdn_problem {
+    int32_t batch;               /* B >= 0 requests (B = 0: calls return GDN_OK, no launch) */
+    int32_t heads;               /* H >= 1 */
+    int32_t dk;                  /* key dim: 32, 64 or 128 */
+    int32_t dv;                  /* value dim: a multiple of 32, <= 128 or 256 */
+    int32_t max_T;               /* uniform draft length (cu_seqlens NULL) or the ragged maximum, 0..GDN_MAX_T */
+    int32_t qkv_dtype;           /* gdn_dtype of q, k, v */
+    int32_t algo;                /* gdn_algo */
+    int32_t reserved;            /* must be 0 */
+    const int32_t *cu_seqlens;   /* device [batch+1] token-row offsets, or NULL (uniform) */
+    const void *q;               /* device [N_tok][heads][dk], 16-byte aligned */
+    const void *k;               /* device [N_tok][heads][dk], 16-byte aligned */
+    const void *v;               /* device [N_tok][heads][dv], 16-byte aligned */
+    const float *alpha;          /* device [N_tok][heads] */
+    const float *beta;           /* device [N_tok][heads] */
+    float *pool;                 /* device [pool_slots][heads][dk][dv], 16-byte aligned */
+    int64_t pool_slots;          /* >= batch */
+    const int32_t *slot_ids;     /* device [batch], distinct, in [0, pool_slots) */
+    int32_t *dev_err;            /* device int32 error word (GDN_DEVERR_* bits), or NULL */
+    int64_t n_tok;               /* rows of q/k/v/alpha/beta/o.  Ignored for uniform input
+                                    (batch*max_T); REQUIRED for ragged input: the kernels
+                                    flag GDN_DEVERR_SEQLEN for a request whose rows
+                                    [cu[r], cu[r+1]) do not lie in [0, n_tok) */
+} gdn_problem;
+
+/* o_t for every draft token of every unit.  o: device float32 [N_tok][heads][dv],
+ * 16-byte aligned, must not overlap any input.  Reads the pool, never writes it. */
+GDN_API gdn_status gdn_verify(const gdn_problem *p, float *o, cudaStream_t stream);
+
+/* For every request r with accepted[r] > 0: pool[slot_ids[r]][h] <- state after
+ * accepted[r] tokens, replayed from the checkpoint in that same slot (in place).
+ * Requests with accepted[r] = 0 write nothing.  accepted: device int32 [batch]. */
+GDN_API gdn_status gdn_commit(const gdn_problem *p, const int32_t *accepted, cudaStream_t stream);
+
+/* gdn_verify and then gdn_commit with the same inputs, in one pass: each
+ * checkpoint is read once, o is written for every token, the state once. */
+GDN_API gdn_status gdn_verify_commit_fused(const gdn_problem *p, const int32_t *accepted,
+                                           float *o, cudaStream_t stream);
+
+/* Waits for `stream`, copies *p->dev_err to *host_code (0 when dev_err is NULL).
+ * Returns GDN_ERR_DEVICE_ARG when the word is non-zero, GDN_OK when it is zero. */
+GDN_API gdn_status gdn_read_device_error(const gdn_problem *p, cudaStream_t stream,
+                                         int32_t *host_code);
+
+/* The algo that AUTO resolves to for this problem (host only, no CUDA call),
+ * or -1 when the shape fails validation. */
+GDN_API int32_t gdn_select_algo(const gdn_problem *p);
+
+/* Static, never NULL. */
+GDN_API const char *gdn_status_string(gdn_status s);
+
+/* Text of the last CUDA error seen by this thread ("" if none). */
+GDN_API const char *gdn_last_error_string(void);
+
+/* Library version, e.g. "0.1.0". */
+GDN_API const char *gdn_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* GDN_H */

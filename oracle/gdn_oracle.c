@@ -61,7 +61,9 @@ int gdn_oracle_run_units(int64_t heads, int64_t dk, int64_t dv, int64_t max_T,
         if (s_acc && a_r == 0)
             state_to_tile(S, s_acc + n * dk * dv, dk, dv);
 
-        for (int64_t t = 0; t < T_r; ++t) {
+        /* Without outputs only the accepted prefix needs replaying. */
+        const int64_t T_run = (o == NULL && s_acc) ? a_r : T_r;
+        for (int64_t t = 0; t < T_run; ++t) {
             const int64_t x = (row0 + t) * heads + h;  /* token row, head */
             const double a_t = alpha[x];
             const double b_t = beta[x];

@@ -1,0 +1,204 @@
+"""Python binding of libgdn.so: argument marshalling only.
+
+Every function here has the name of the C entry point it calls (include/gdn.h)
+and only turns torch tensors into device pointers and sizes; all computation
+runs in the CUDA kernels.  If the library has not been built this module raises
+on first use: there is no fallback path.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Optional
+
+import torch
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "_lib", "libgdn.so")
+
+GDN_OK = 0
+GDN_ERR_DEVICE_ARG = 5
+GDN_FP32, GDN_BF16 = 0, 1
+GDN_ALGO_AUTO, GDN_ALGO_RECURRENT, GDN_ALGO_CHUNK = 0, 1, 2
+GDN_DEVERR_SLOT, GDN_DEVERR_ACCEPTED, GDN_DEVERR_SEQLEN = 1, 2, 4
+GDN_MAX_T = 1024
+
+# Every symbol include/gdn.h declares.
+EXPORTED = (
+    "gdn_verify", "gdn_commit", "gdn_verify_commit_fused", "gdn_read_device_error",
+    "gdn_select_algo", "gdn_status_string", "gdn_last_error_string", "gdn_version",
+)
+
+
+class GdnError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        msg = f"{where}: {gdn_status_string(status)} (status {status})"
+        if status == 6:
+            msg += f": {gdn_last_error_string()}"
+        super().__init__(msg)
+
+
+class gdn_problem(ctypes.Structure):
+    """Mirror of the C struct gdn_problem (include/gdn.h), field for field."""
+
+    _fields_ = [
+        ("batch", ctypes.c_int32), ("heads", ctypes.c_int32), ("dk", ctypes.c_int32),
+        ("dv", ctypes.c_int32), ("max_T", ctypes.c_int32), ("qkv_dtype", ctypes.c_int32),
+        ("algo", ctypes.c_int32), ("reserved", ctypes.c_int32),
+        ("cu_seqlens", ctypes.c_void_p), ("q", ctypes.c_void_p), ("k", ctypes.c_void_p),
+        ("v", ctypes.c_void_p), ("alpha", ctypes.c_void_p), ("beta", ctypes.c_void_p),
+        ("pool", ctypes.c_void_p), ("pool_slots", ctypes.c_int64),
+        ("slot_ids", ctypes.c_void_p), ("dev_err", ctypes.c_void_p), ("n_tok", ctypes.c_int64),
+    ]
+
+
+_lib_handle: Optional[ctypes.CDLL] = None
+
+
+def lib() -> ctypes.CDLL:
+    """The loaded CUDA library; raises if it was never built."""
+    global _lib_handle
+    if _lib_handle is None:
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(
+                f"{LIB_PATH} is missing: build it with speculative_decode_gated_gb300.build() "
+                "(there is no CPU or PyTorch fallback)")
+        h = ctypes.CDLL(LIB_PATH)
+        P, S = ctypes.POINTER(gdn_problem), ctypes.c_void_p
+        h.gdn_verify.argtypes = [P, S, S]
+        h.gdn_commit.argtypes = [P, S, S]
+        h.gdn_verify_commit_fused.argtypes = [P, S, S, S]
+        h.gdn_read_device_error.argtypes = [P, S, ctypes.POINTER(ctypes.c_int32)]
+        h.gdn_select_algo.argtypes = [P]
+        h.gdn_status_string.argtypes = [ctypes.c_int]
+        for name in ("gdn_verify", "gdn_commit", "gdn_verify_commit_fused",
+                     "gdn_read_device_error", "gdn_select_algo"):
+            getattr(h, name).restype = ctypes.c_int
+        for name in ("gdn_status_string", "gdn_last_error_string", "gdn_version"):
+            getattr(h, name).restype = ctypes.c_char_p
+        _lib_handle = h
+    return _lib_handle
+
+
+class Problem:
+    """A gdn_problem plus references to the tensors it points into."""
+
+    def __init__(self, c: gdn_problem, refs: tuple):
+        self.c = c
+        self.refs = refs
+
+    @property
+    def ref(self):
+        return ctypes.byref(self.c)
+
+
+def _ptr(t: Optional[torch.Tensor]) -> Optional[int]:
+    return None if t is None else t.data_ptr()
+
+
+def _check(t: Optional[torch.Tensor], name: str, dtypes, device) -> None:
+    if t is None:
+        return
+    if t.dtype not in dtypes:
+        raise TypeError(f"{name}: dtype {t.dtype}, expected one of {dtypes}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if device is not None and t.device != device:
+        raise ValueError(f"{name} is on {t.device}, expected {device}")
+
+
+def make_problem(*, q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, alpha: torch.Tensor,
+                 beta: torch.Tensor, pool: torch.Tensor, slot_ids: torch.Tensor,
+                 max_T: int, cu_seqlens: Optional[torch.Tensor] = None,
+                 dev_err: Optional[torch.Tensor] = None, algo: int = GDN_ALGO_AUTO) -> Problem:
+    """Builds the C problem from device tensors (shapes as in include/gdn.h).
+
+    q, k: [N_tok, H, dk]; v: [N_tok, H, dv] (bf16 or fp32, same dtype);
+    alpha, beta: [N_tok, H] fp32; pool: [slots, H, dk, dv] fp32; slot_ids: [B] int32;
+    cu_seqlens: [B+1] int32 or None (uniform length max_T); dev_err: [1] int32 or None.
+    """
+    dev = pool.device
+    if q.dtype not in (torch.bfloat16, torch.float32) or k.dtype != q.dtype or v.dtype != q.dtype:
+        raise TypeError("q, k, v must all be bf16 or all fp32")
+    for t, n in ((q, "q"), (k, "k"), (v, "v")):
+        _check(t, n, (q.dtype,), dev)
+    _check(alpha, "alpha", (torch.float32,), dev)
+    _check(beta, "beta", (torch.float32,), dev)
+    _check(pool, "pool", (torch.float32,), dev)
+    _check(slot_ids, "slot_ids", (torch.int32,), dev)
+    _check(cu_seqlens, "cu_seqlens", (torch.int32,), dev)
+    _check(dev_err, "dev_err", (torch.int32,), dev)
+    if pool.dim() != 4:
+        raise ValueError("pool must be [slots, heads, dk, dv]")
+    slots, H, dk, dv = pool.shape
+    c = gdn_problem()
+    c.batch = slot_ids.numel()
+    c.heads, c.dk, c.dv = H, dk, dv
+    c.max_T = int(max_T)
+    c.qkv_dtype = GDN_BF16 if q.dtype == torch.bfloat16 else GDN_FP32
+    c.algo = int(algo)
+    c.reserved = 0
+    c.cu_seqlens = _ptr(cu_seqlens)
+    c.q, c.k, c.v = _ptr(q), _ptr(k), _ptr(v)
+    c.alpha, c.beta = _ptr(alpha), _ptr(beta)
+    c.pool = _ptr(pool)
+    c.pool_slots = slots
+    c.slot_ids = _ptr(slot_ids)
+    c.dev_err = _ptr(dev_err)
+    c.n_tok = q.shape[0]
+    return Problem(c, (q, k, v, alpha, beta, pool, slot_ids, cu_seqlens, dev_err))
+
+
+def _stream(stream) -> int:
+    if stream is None:
+        return torch.cuda.current_stream().cuda_stream
+    return stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
+
+
+def _raise(status: int, where: str) -> None:
+    if status != GDN_OK:
+        raise GdnError(status, where)
+
+
+def gdn_verify(prob: Problem, o: torch.Tensor, stream=None) -> None:
+    _check(o, "o", (torch.float32,), None)
+    _raise(lib().gdn_verify(prob.ref, _ptr(o), _stream(stream)), "gdn_verify")
+
+
+def gdn_commit(prob: Problem, accepted: torch.Tensor, stream=None) -> None:
+    _check(accepted, "accepted", (torch.int32,), None)
+    _raise(lib().gdn_commit(prob.ref, _ptr(accepted), _stream(stream)), "gdn_commit")
+
+
+def gdn_verify_commit_fused(prob: Problem, accepted: torch.Tensor, o: torch.Tensor,
+                            stream=None) -> None:
+    _check(accepted, "accepted", (torch.int32,), None)
+    _check(o, "o", (torch.float32,), None)
+    _raise(lib().gdn_verify_commit_fused(prob.ref, _ptr(accepted), _ptr(o), _stream(stream)),
+           "gdn_verify_commit_fused")
+
+
+def gdn_read_device_error(prob: Problem, stream=None) -> int:
+    """Synchronises the stream and returns the device error word (0 = none)."""
+    code = ctypes.c_int32(0)
+    st = lib().gdn_read_device_error(prob.ref, _stream(stream), ctypes.byref(code))
+    if st not in (GDN_OK, GDN_ERR_DEVICE_ARG):
+        _raise(st, "gdn_read_device_error")
+    return int(code.value)
+
+
+def gdn_select_algo(prob: Problem) -> int:
+    return int(lib().gdn_select_algo(prob.ref))
+
+
+def gdn_status_string(status: int) -> str:
+    return lib().gdn_status_string(int(status)).decode()
+
+
+def gdn_last_error_string() -> str:
+    return lib().gdn_last_error_string().decode()
+
+
+def gdn_version() -> str:
+    return lib().gdn_version().decode()

@@ -1,0 +1,211 @@
+// C ABI of libgdn.so: host-side validation, kernel selection and launch.
+// Every check runs before any CUDA call, so a rejected call launches nothing
+// (and the checks work on a machine without a GPU).
+#include <cstdint>
+#include <cstdio>
+
+#include "gdn.h"
+#include "gdn_device.cuh"
+#include "gdn_launch.h"
+
+namespace {
+
+thread_local char g_last_error[256] = "";
+
+void set_cuda_error(cudaError_t e, const char *where) {
+    std::snprintf(g_last_error, sizeof(g_last_error), "%s: %s (%d)", where,
+                  cudaGetErrorString(e), (int)e);
+}
+
+bool aligned16(const void *ptr) { return (reinterpret_cast<uintptr_t>(ptr) & 15u) == 0; }
+bool aligned4(const void *ptr) { return (reinterpret_cast<uintptr_t>(ptr) & 3u) == 0; }
+
+struct Range {
+    uintptr_t lo, hi;  // [lo, hi)
+};
+
+Range range(const void *ptr, int64_t bytes) {
+    const uintptr_t lo = reinterpret_cast<uintptr_t>(ptr);
+    return Range{lo, lo + (uintptr_t)(bytes > 0 ? bytes : 0)};
+}
+
+bool overlap(Range a, Range b) {
+    if (a.lo == a.hi || b.lo == b.hi) return false;
+    return a.lo < b.hi && b.lo < a.hi;
+}
+
+bool dims_supported(int dk, int dv) {
+    const bool dk_ok = dk == 32 || dk == 64 || dk == 128;
+    const bool dv_ok = dv >= 32 && dv <= 256 && dv % 32 == 0 && (dv <= 128 || dv % 128 == 0);
+    return dk_ok && dv_ok;
+}
+
+bool shape_ok(const gdn_problem *p) {
+    return p->batch >= 0 && p->heads >= 1 && p->max_T >= 0 && p->max_T <= GDN_MAX_T &&
+           (int64_t)p->batch * p->heads <= 0x7fffffffLL;
+}
+
+// Which kernel AUTO picks.  The chunked tensor-core kernel covers bf16 q/k/v at
+// dk = dv = 128 with up to 16 tokens per request; the recurrent kernel the rest.
+int resolve_algo(const gdn_problem *p) {
+    const bool chunk_ok = gdn::chunk_supported(p->qkv_dtype == GDN_BF16, p->dk, p->dv, p->max_T);
+    if (p->algo == GDN_ALGO_RECURRENT) return GDN_ALGO_RECURRENT;
+    if (p->algo == GDN_ALGO_CHUNK) return chunk_ok ? GDN_ALGO_CHUNK : -1;
+    return (chunk_ok && gdn::chunk_preferred(p->max_T)) ? GDN_ALGO_CHUNK : GDN_ALGO_RECURRENT;
+}
+
+// Host validation shared by all entry points.  On success *algo is the kernel
+// to run and *empty tells whether there is nothing to launch.
+gdn_status validate(const gdn_problem *p, bool with_o, const float *o, bool with_acc,
+                    const int32_t *accepted, int *algo, bool *empty) {
+    if (!p) return GDN_ERR_NULL_PTR;
+    if (p->reserved != 0 || !shape_ok(p)) return GDN_ERR_BAD_DIM;
+    if (p->qkv_dtype != GDN_FP32 && p->qkv_dtype != GDN_BF16) return GDN_ERR_BAD_DTYPE;
+    if (!dims_supported(p->dk, p->dv)) return GDN_ERR_UNSUPPORTED;
+    if (p->algo < GDN_ALGO_AUTO || p->algo > GDN_ALGO_CHUNK) return GDN_ERR_UNSUPPORTED;
+    *algo = resolve_algo(p);
+    if (*algo < 0) return GDN_ERR_UNSUPPORTED;
+    *empty = p->batch == 0;
+    if (*empty) return GDN_OK;
+    if (p->pool_slots < p->batch) return GDN_ERR_BAD_DIM;
+    if (p->cu_seqlens && p->n_tok < 0) return GDN_ERR_BAD_DIM;
+    if (!p->pool || !p->slot_ids) return GDN_ERR_NULL_PTR;
+    if (p->max_T > 0 && (!p->q || !p->k || !p->v || !p->alpha || !p->beta))
+        return GDN_ERR_NULL_PTR;
+    if (with_o && !o) return GDN_ERR_NULL_PTR;
+    if (with_acc && !accepted) return GDN_ERR_NULL_PTR;
+    if (!aligned16(p->q) || !aligned16(p->k) || !aligned16(p->v) || !aligned16(p->pool) ||
+        !aligned16(o) || !aligned4(p->alpha) || !aligned4(p->beta) || !aligned4(p->slot_ids) ||
+        !aligned4(p->cu_seqlens) || !aligned4(accepted) || !aligned4(p->dev_err))
+        return GDN_ERR_ALIGN;
+
+    // Aliasing: o must not overlap any input; the pool must not overlap q/k/v/gates/metadata.
+    const int64_t H = p->heads;
+    const int64_t n_tok = p->cu_seqlens ? p->n_tok : (int64_t)p->batch * p->max_T;
+    const int64_t esz = p->qkv_dtype == GDN_BF16 ? 2 : 4;
+    const Range rq = range(p->q, n_tok * H * p->dk * esz);
+    const Range rk = range(p->k, n_tok * H * p->dk * esz);
+    const Range rv = range(p->v, n_tok * H * p->dv * esz);
+    const Range ra = range(p->alpha, n_tok * H * 4);
+    const Range rb = range(p->beta, n_tok * H * 4);
+    const Range rp = range(p->pool, p->pool_slots * H * p->dk * p->dv * 4);
+    const Range rs = range(p->slot_ids, (int64_t)p->batch * 4);
+    const Range rc = range(p->cu_seqlens, p->cu_seqlens ? ((int64_t)p->batch + 1) * 4 : 0);
+    const Range racc = range(accepted, with_acc ? (int64_t)p->batch * 4 : 0);
+    const Range re = range(p->dev_err, p->dev_err ? 4 : 0);
+    const Range others[] = {rq, rk, rv, ra, rb, rs, rc, racc, re};
+    for (const Range &x : others)
+        if (overlap(rp, x)) return GDN_ERR_ALIAS;
+    if (with_o) {
+        const Range ro = range(o, n_tok * H * p->dv * 4);
+        const Range all[] = {rq, rk, rv, ra, rb, rp, rs, rc, racc, re};
+        for (const Range &x : all)
+            if (overlap(ro, x)) return GDN_ERR_ALIAS;
+    }
+    return GDN_OK;
+}
+
+gdn::Args make_args(const gdn_problem *p, const int32_t *accepted, float *o) {
+    gdn::Args a;
+    a.B = p->batch;
+    a.H = p->heads;
+    a.dk = p->dk;
+    a.dv = p->dv;
+    a.max_T = p->max_T;
+    a.n_tok = p->cu_seqlens ? p->n_tok : (long long)p->batch * p->max_T;
+    a.cu_seqlens = p->cu_seqlens;
+    a.q = p->q;
+    a.k = p->k;
+    a.v = p->v;
+    a.alpha = p->alpha;
+    a.beta = p->beta;
+    a.pool = p->pool;
+    a.pool_slots = p->pool_slots;
+    a.slot_ids = p->slot_ids;
+    a.accepted = accepted;
+    a.o = o;
+    a.dev_err = p->dev_err;
+    return a;
+}
+
+gdn_status run(const gdn_problem *p, int mode, const int32_t *accepted, float *o,
+               cudaStream_t stream) {
+    int algo = 0;
+    bool empty = false;
+    const bool with_o = mode != gdn::kCommit;
+    const bool with_acc = mode != gdn::kVerify;
+    const gdn_status st = validate(p, with_o, o, with_acc, accepted, &algo, &empty);
+    if (st != GDN_OK || empty) return st;
+    const gdn::Args a = make_args(p, with_acc ? accepted : nullptr, with_o ? o : nullptr);
+    const bool bf16 = p->qkv_dtype == GDN_BF16;
+    const cudaError_t e = algo == GDN_ALGO_CHUNK ? gdn::launch_chunk(a, mode, stream)
+                                                 : gdn::launch_recurrent(a, mode, bf16, stream);
+    if (e != cudaSuccess) {
+        set_cuda_error(e, "kernel launch");
+        return GDN_ERR_CUDA;
+    }
+    return GDN_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+gdn_status gdn_verify(const gdn_problem *p, float *o, cudaStream_t stream) {
+    return run(p, gdn::kVerify, nullptr, o, stream);
+}
+
+gdn_status gdn_commit(const gdn_problem *p, const int32_t *accepted, cudaStream_t stream) {
+    return run(p, gdn::kCommit, accepted, nullptr, stream);
+}
+
+gdn_status gdn_verify_commit_fused(const gdn_problem *p, const int32_t *accepted, float *o,
+                                   cudaStream_t stream) {
+    return run(p, gdn::kFused, accepted, o, stream);
+}
+
+gdn_status gdn_read_device_error(const gdn_problem *p, cudaStream_t stream, int32_t *host_code) {
+    if (!p || !host_code) return GDN_ERR_NULL_PTR;
+    *host_code = 0;
+    if (!p->dev_err) return GDN_OK;
+    int32_t word = 0;
+    cudaError_t e = cudaMemcpyAsync(&word, p->dev_err, sizeof(word), cudaMemcpyDeviceToHost, stream);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(stream);
+    if (e != cudaSuccess) {
+        set_cuda_error(e, "gdn_read_device_error");
+        return GDN_ERR_CUDA;
+    }
+    *host_code = word;
+    return word ? GDN_ERR_DEVICE_ARG : GDN_OK;
+}
+
+int32_t gdn_select_algo(const gdn_problem *p) {
+    // Shape-level checks only: pointers are not needed to pick a kernel.
+    if (!p || !shape_ok(p)) return -1;
+    if (p->qkv_dtype != GDN_FP32 && p->qkv_dtype != GDN_BF16) return -1;
+    if (!dims_supported(p->dk, p->dv)) return -1;
+    if (p->algo < GDN_ALGO_AUTO || p->algo > GDN_ALGO_CHUNK) return -1;
+    return resolve_algo(p);
+}
+
+const char *gdn_status_string(gdn_status s) {
+    switch (s) {
+        case GDN_OK: return "ok";
+        case GDN_ERR_NULL_PTR: return "a required pointer is NULL";
+        case GDN_ERR_BAD_DIM: return "a size is out of range";
+        case GDN_ERR_BAD_DTYPE: return "unknown q/k/v dtype";
+        case GDN_ERR_UNSUPPORTED: return "shape or algo not supported";
+        case GDN_ERR_DEVICE_ARG:
+            return "a kernel reported a bad slot id, accepted length or sequence length";
+        case GDN_ERR_CUDA: return "a CUDA call failed";
+        case GDN_ERR_ALIGN: return "a pointer is not aligned (16 bytes for q/k/v/pool/o)";
+        case GDN_ERR_ALIAS: return "an output overlaps an input";
+    }
+    return "unknown status";
+}
+
+const char *gdn_last_error_string(void) { return g_last_error; }
+
+const char *gdn_version(void) { return "0.1.0"; }
+
+}  // extern "C"

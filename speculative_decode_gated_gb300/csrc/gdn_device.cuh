@@ -1,0 +1,87 @@
+// Shared device-side pieces of the Gated DeltaNet verify/commit kernels:
+// the kernel argument block, per-unit metadata resolution with the
+// device-side argument checks, and small load/convert helpers.
+#pragma once
+
+#include <cstdint>
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include "gdn.h"
+
+namespace gdn {
+
+enum Mode : int { kVerify = 0, kCommit = 1, kFused = 2 };
+
+// Everything a kernel needs; a plain copy of gdn_problem plus the call's outputs.
+struct Args {
+    int B, H, dk, dv, max_T;
+    long long n_tok;  // rows of the token arrays
+    const int32_t *cu_seqlens;
+    const void *q, *k, *v;
+    const float *alpha, *beta;
+    float *pool;
+    long long pool_slots;
+    const int32_t *slot_ids;
+    const int32_t *accepted;  // NULL for verify
+    float *o;                 // NULL for commit
+    int32_t *dev_err;
+};
+
+// Token range, accepted length and state tile of one (request r, head h).
+struct Unit {
+    int row0;     // first token row
+    int T;        // draft tokens T_r
+    int a;        // accepted length (-1 in verify)
+    float *tile;  // pool[slot_r][h], dk x dv
+};
+
+// Reads the unit's metadata and applies the device-side checks.  Every thread
+// of the block evaluates the same condition; thread 0 reports the error bit.
+// Returns false when the unit must be skipped (nothing is written for it).
+__device__ __forceinline__ bool resolve_unit(const Args &p, int r, int h, int mode, Unit &u) {
+    int err = 0;
+    if (p.cu_seqlens) {
+        u.row0 = p.cu_seqlens[r];
+        u.T = p.cu_seqlens[r + 1] - u.row0;
+        if (u.T < 0 || u.T > p.max_T || u.row0 < 0 || (long long)u.row0 + u.T > p.n_tok)
+            err |= GDN_DEVERR_SEQLEN;
+    } else {
+        u.row0 = r * p.max_T;
+        u.T = p.max_T;
+    }
+    const int slot = p.slot_ids[r];
+    if (slot < 0 || (long long)slot >= p.pool_slots) err |= GDN_DEVERR_SLOT;
+    u.a = -1;
+    if (mode != kVerify) {
+        u.a = p.accepted[r];
+        if (!err && (u.a < 0 || u.a > u.T)) err |= GDN_DEVERR_ACCEPTED;
+    }
+    if (err) {
+        if (threadIdx.x == 0 && p.dev_err) atomicOr(p.dev_err, err);
+        return false;
+    }
+    u.tile = p.pool + ((size_t)slot * p.H + h) * (size_t)p.dk * p.dv;
+    return true;
+}
+
+// Hides a pointer's value from the optimiser, so addresses derived from it are
+// recomputed where they are used instead of being kept live in registers.
+template <typename T>
+__device__ __forceinline__ T *opaque(T *ptr) {
+    asm volatile("" : "+l"(ptr));
+    return ptr;
+}
+
+// 8 bf16 (one 16-byte vector) -> 8 floats.
+__device__ __forceinline__ void bf16x8_to_f32(const uint4 &w, float *out) {
+    const uint32_t x[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+        out[2 * e] = __uint_as_float(x[e] << 16);
+        out[2 * e + 1] = __uint_as_float(x[e] & 0xFFFF0000u);
+    }
+}
+
+}  // namespace gdn

@@ -1,0 +1,19 @@
+// Host-side launchers of the kernels (internal to libgdn.so).
+#pragma once
+
+#include <cuda_runtime.h>
+
+#include "gdn_device.cuh"
+
+namespace gdn {
+
+// Recurrent kernel: dk in {32, 64, 128}; dv a multiple of 32, <= 128 or a
+// multiple of 128 up to 256; q/k/v bf16 or fp32; any max_T.
+cudaError_t launch_recurrent(const Args &p, int mode, bool bf16, cudaStream_t stream);
+
+// Chunked tensor-core kernel and its applicability.
+bool chunk_supported(bool bf16, int dk, int dv, int max_T);
+bool chunk_preferred(int max_T);
+cudaError_t launch_chunk(const Args &p, int mode, cudaStream_t stream);
+
+}  // namespace gdn

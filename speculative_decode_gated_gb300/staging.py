@@ -1,0 +1,95 @@
+"""Host problem (inputs.Problem, numpy) -> device tensors and a C problem.
+
+Plain data movement: dtype casts of already-rounded values, copies, and the
+placement of each request's checkpoint into its pool slot.
+"""
+from __future__ import annotations
+
+from typing import Optional
+
+import numpy as np
+import torch
+
+from . import binding
+from .inputs import POOL_SENTINEL_BITS, Problem, bf16_bits
+
+
+def qkv_tensor(x: np.ndarray, qkv_dtype: str, device) -> torch.Tensor:
+    if qkv_dtype == "bf16":
+        return torch.from_numpy(bf16_bits(x).view(np.int16)).view(torch.bfloat16).to(device)
+    return torch.from_numpy(np.ascontiguousarray(x, np.float32)).to(device)
+
+
+def new_pool(slots: int, heads: int, dk: int, dv: int, device, fill: str = "sentinel",
+             layers: Optional[int] = None) -> torch.Tensor:
+    shape = (slots, heads, dk, dv) if layers is None else (layers, slots, heads, dk, dv)
+    pool = torch.empty(shape, dtype=torch.float32, device=device)
+    if fill == "sentinel":
+        pool.view(torch.int32).fill_(POOL_SENTINEL_BITS)
+    elif fill == "zero":
+        pool.zero_()
+    elif fill != "none":
+        raise ValueError(fill)
+    return pool
+
+
+def place_checkpoints(pool: torch.Tensor, prob: Problem) -> None:
+    """pool[slot_ids[r]] <- the request's checkpoint tiles (all heads)."""
+    idx = torch.from_numpy(prob.slot_ids.astype(np.int64)).to(pool.device)
+    src = torch.from_numpy(np.ascontiguousarray(prob.s0, np.float32)).to(pool.device)
+    pool.index_copy_(0, idx, src)
+
+
+class DeviceProblem:
+    """Device copies of one layer-call's inputs and the matching C problem."""
+
+    def __init__(self, prob: Problem, device="cuda", pool: Optional[torch.Tensor] = None,
+                 pool_fill: str = "sentinel", algo: int = binding.GDN_ALGO_AUTO,
+                 with_dev_err: bool = True):
+        self.host = prob
+        dev = torch.device(device)
+        self.q = qkv_tensor(prob.q, prob.qkv_dtype, dev)
+        self.k = qkv_tensor(prob.k, prob.qkv_dtype, dev)
+        self.v = qkv_tensor(prob.v, prob.qkv_dtype, dev)
+        self.alpha = torch.from_numpy(np.ascontiguousarray(prob.alpha, np.float32)).to(dev)
+        self.beta = torch.from_numpy(np.ascontiguousarray(prob.beta, np.float32)).to(dev)
+        self.slot_ids = torch.from_numpy(prob.slot_ids.astype(np.int32)).to(dev)
+        self.accepted = torch.from_numpy(prob.accepted.astype(np.int32)).to(dev)
+        self.cu_seqlens = (torch.from_numpy(prob.cu_seqlens.astype(np.int32)).to(dev)
+                           if prob.ragged else None)
+        if pool is None:
+            pool = new_pool(prob.pool_slots, prob.heads, prob.dk, prob.dv, dev, pool_fill)
+        self.pool = pool
+        place_checkpoints(self.pool, prob)
+        self.dev_err = torch.zeros(1, dtype=torch.int32, device=dev) if with_dev_err else None
+        self.o = torch.zeros((prob.n_tok, prob.heads, prob.dv), dtype=torch.float32, device=dev)
+        self.c = binding.make_problem(q=self.q, k=self.k, v=self.v, alpha=self.alpha,
+                                      beta=self.beta, pool=self.pool, slot_ids=self.slot_ids,
+                                      max_T=prob.max_T, cu_seqlens=self.cu_seqlens,
+                                      dev_err=self.dev_err, algo=algo)
+
+    def verify(self, stream=None):
+        binding.gdn_verify(self.c, self.o, stream)
+
+    def commit(self, stream=None):
+        binding.gdn_commit(self.c, self.accepted, stream)
+
+    def fused(self, stream=None):
+        binding.gdn_verify_commit_fused(self.c, self.accepted, self.o, stream)
+
+    def launcher(self, mode: str, stream):
+        """A zero-argument callable issuing one call on `stream` with every
+        argument marshalled in advance (for timing loops and graph capture)."""
+        lib = binding.lib()
+        ref = self.c.ref
+        s = binding._stream(stream)
+        o, acc = self.o.data_ptr(), self.accepted.data_ptr()
+        fn = {"verify": lambda: lib.gdn_verify(ref, o, s),
+              "commit": lambda: lib.gdn_commit(ref, acc, s),
+              "fused": lambda: lib.gdn_verify_commit_fused(ref, acc, o, s)}[mode]
+
+        def call():
+            st = fn()
+            if st != binding.GDN_OK:
+                raise binding.GdnError(st, f"gdn {mode}")
+        return call

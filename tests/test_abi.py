@@ -1,0 +1,138 @@
+"""The C ABI without a GPU: the library builds and loads, exports every symbol
+include/gdn.h declares, the Python struct matches the C layout, and host-side
+validation rejects bad arguments before any CUDA call."""
+import ctypes
+import os
+import re
+import subprocess
+
+import pytest
+
+from speculative_decode_gated_gb300 import binding
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "gdn.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    if not os.path.exists(binding.LIB_PATH):
+        import speculative_decode_gated_gb300 as pkg
+        pkg.build()
+    return binding.lib()
+
+
+def declared_symbols():
+    text = open(HEADER).read()
+    return sorted(set(re.findall(r"GDN_API\s+[\w\s\*]+?\b(gdn_\w+)\s*\(", text)))
+
+
+def test_header_declares_the_bound_symbols():
+    assert declared_symbols() == sorted(binding.EXPORTED)
+
+
+def test_library_exports_every_declared_symbol(lib):
+    out = subprocess.run(["nm", "-D", "--defined-only", binding.LIB_PATH],
+                         capture_output=True, text=True, check=True).stdout
+    exported = set(re.findall(r"\bT (gdn_\w+)", out))
+    for name in declared_symbols():
+        assert name in exported, name
+        assert hasattr(lib, name)
+
+
+def test_struct_layout_matches_c(tmp_path):
+    fields = [f[0] for f in binding.gdn_problem._fields_]
+    prog = tmp_path / "layout.c"
+    body = "\n".join(f'printf("%zu ", offsetof(gdn_problem, {f}));' for f in fields)
+    prog.write_text(f'#include <stdio.h>\n#include <stddef.h>\n#include "gdn.h"\n'
+                    f'int main(void) {{ {body} printf("%zu\\n", sizeof(gdn_problem)); return 0; }}\n')
+    exe = tmp_path / "layout"
+    cuda_inc = os.path.join(os.environ.get("CUDA_HOME", "/usr/local/cuda"), "include")
+    subprocess.run(["gcc", "-I", os.path.join(ROOT, "include"), "-I", cuda_inc, str(prog),
+                    "-o", str(exe)], check=True)
+    c_vals = [int(x) for x in subprocess.run([str(exe)], capture_output=True, text=True,
+                                             check=True).stdout.split()]
+    py_vals = [getattr(binding.gdn_problem, f).offset for f in fields]
+    py_vals.append(ctypes.sizeof(binding.gdn_problem))
+    assert c_vals == py_vals
+
+
+def fake_problem(**over):
+    """A problem with plausible, aligned fake device addresses (never dereferenced)."""
+    c = binding.gdn_problem()
+    c.batch, c.heads, c.dk, c.dv, c.max_T = 2, 4, 128, 128, 8
+    c.qkv_dtype, c.algo, c.reserved = binding.GDN_BF16, 0, 0
+    base = 1 << 40
+    step = 1 << 32
+    c.q, c.k, c.v = base, base + step, base + 2 * step
+    c.alpha, c.beta = base + 3 * step, base + 4 * step
+    c.pool, c.pool_slots = base + 5 * step, 8
+    c.slot_ids = base + 6 * step
+    c.cu_seqlens = None
+    c.dev_err = base + 7 * step
+    c.n_tok = 16
+    for k, v in over.items():
+        setattr(c, k, v)
+    return c
+
+
+O_PTR = (1 << 40) + 9 * (1 << 32)
+ACC_PTR = (1 << 40) + 10 * (1 << 32)
+
+
+def call(lib, fn, c, o=O_PTR, acc=ACC_PTR):
+    if fn == "verify":
+        return lib.gdn_verify(ctypes.byref(c), o, None)
+    if fn == "commit":
+        return lib.gdn_commit(ctypes.byref(c), acc, None)
+    return lib.gdn_verify_commit_fused(ctypes.byref(c), acc, o, None)
+
+
+@pytest.mark.parametrize("fn", ["verify", "commit", "fused"])
+@pytest.mark.parametrize("over,status", [
+    (dict(heads=0), 2), (dict(batch=-1), 2), (dict(max_T=-1), 2), (dict(max_T=1025), 2),
+    (dict(reserved=1), 2), (dict(pool_slots=1), 2),
+    (dict(cu_seqlens=(1 << 40) + 11 * (1 << 32), n_tok=-1), 2),
+    (dict(qkv_dtype=5), 3),
+    (dict(dk=48), 4), (dict(dk=256), 4), (dict(dv=48), 4), (dict(dv=160), 4), (dict(algo=9), 4),
+    (dict(algo=2, qkv_dtype=0), 4), (dict(algo=2, max_T=17), 4),
+    (dict(pool=None), 1), (dict(slot_ids=None), 1), (dict(q=None), 1), (dict(beta=None), 1),
+    (dict(q=(1 << 40) + 8), 7), (dict(pool=(1 << 40) + 5 * (1 << 32) + 4), 7),
+    (dict(alpha=(1 << 40) + 3 * (1 << 32) + 2), 7),
+    (dict(pool=1 << 40), 8),  # pool over q
+])
+def test_host_validation_rejects(lib, fn, over, status):
+    assert call(lib, fn, fake_problem(**over)) == status
+
+
+def test_output_checks(lib):
+    c = fake_problem()
+    assert lib.gdn_verify(ctypes.byref(c), None, None) == 1
+    assert lib.gdn_commit(ctypes.byref(c), None, None) == 1
+    assert lib.gdn_verify(ctypes.byref(c), O_PTR + 4, None) == 7
+    assert lib.gdn_verify(ctypes.byref(c), c.v, None) == 8       # o over v
+    assert lib.gdn_verify(ctypes.byref(c), c.pool, None) == 8    # o over the pool
+    assert lib.gdn_verify(None, O_PTR, None) == 1
+
+
+def test_empty_batch_is_a_no_op(lib):
+    c = fake_problem(batch=0, q=None, k=None, v=None, pool=None)
+    for fn in ("verify", "commit", "fused"):
+        assert call(lib, fn, c) == 0
+
+
+def test_select_algo(lib):
+    assert lib.gdn_select_algo(ctypes.byref(fake_problem())) == binding.GDN_ALGO_CHUNK
+    assert lib.gdn_select_algo(ctypes.byref(fake_problem(algo=1))) == 1
+    assert lib.gdn_select_algo(ctypes.byref(fake_problem(qkv_dtype=0))) == 1
+    assert lib.gdn_select_algo(ctypes.byref(fake_problem(dk=64))) == 1
+    assert lib.gdn_select_algo(ctypes.byref(fake_problem(max_T=17))) == 1
+    assert lib.gdn_select_algo(ctypes.byref(fake_problem(dk=48))) == -1
+    assert lib.gdn_select_algo(ctypes.byref(fake_problem(max_T=4096))) == -1
+
+
+def test_status_strings(lib):
+    for s in range(9):
+        assert binding.gdn_status_string(s)
+    assert binding.gdn_version().count(".") == 2
+    assert binding.gdn_last_error_string() == ""

@@ -1,0 +1,189 @@
+"""GPU parity: the CUDA path (through the C ABI) against the float64 oracle.
+
+Small problems are compared on every unit; the full-size workloads on a sample
+of units (always including the first and last unit, requests with a_r = 0 and
+a_r = T_r and the shortest ragged request), in the same launch configuration
+the benchmark times.  Bookkeeping (which pool slots change) is compared bitwise
+over the whole pool in every case.
+"""
+import ctypes
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from oracle_pins import load_golden, problem_from_arrays
+from parity import (TOL, check_state_update, check_verify, gather_outputs, oracle_units,
+                    pick_units, rel_err)
+from speculative_decode_gated_gb300 import binding, inputs, staging
+
+pytestmark = pytest.mark.gpu
+
+AUTO, REC, CHUNK = binding.GDN_ALGO_AUTO, binding.GDN_ALGO_RECURRENT, binding.GDN_ALGO_CHUNK
+
+
+def custom(name, **kw):
+    kw.setdefault("qkv_dtype", "bf16")
+    kw.setdefault("accept", "uniform")
+    return lambda: inputs.make_custom(name=name, **kw)
+
+
+SMALL = {
+    "tiny_b1_h2_d32_t4": lambda: inputs.make_problem("tiny_b1_h2_d32_t4"),
+    "b8_h16_d128_t8": lambda: inputs.make_problem("b8_h16_d128_t8"),
+    "b3_h4_d128_t16": custom("b3_h4_d128_t16", batch=3, heads=4, dk=128, dv=128, T=16,
+                             pool_slots=9, accept="binom", seed=11),
+    "ragged_b6_d128": custom("ragged_b6_d128", batch=6, heads=3, dk=128, dv=128,
+                             lengths=[1, 16, 7, 3, 12, 16], pool_slots=40, seed=12),
+    "b4_h2_d64_t8": custom("b4_h2_d64_t8", batch=4, heads=2, dk=64, dv=64, T=8,
+                           pool_slots=6, seed=13),
+    "fp32_dk32_dv96_t5": custom("fp32_dk32_dv96_t5", batch=3, heads=2, dk=32, dv=96, T=5,
+                                qkv_dtype="fp32", pool_slots=3, seed=14),
+    "b2_h2_dk128_dv256_t6": custom("b2_h2_dk128_dv256_t6", batch=2, heads=2, dk=128, dv=256,
+                                   T=6, pool_slots=4, seed=15),
+    "b3_h2_dk64_dv32_t3": custom("b3_h2_dk64_dv32_t3", batch=3, heads=2, dk=64, dv=32, T=3,
+                                 pool_slots=3, seed=16),
+    "b2_h2_d128_t40": custom("b2_h2_d128_t40", batch=2, heads=2, dk=128, dv=128, T=40,
+                             pool_slots=5, seed=17),
+    "b4_h4_d128_t1": custom("b4_h4_d128_t1", batch=4, heads=4, dk=128, dv=128, T=1,
+                            pool_slots=4, seed=18),
+    "fp32_b2_h2_d128_t8": custom("fp32_b2_h2_d128_t8", batch=2, heads=2, dk=128, dv=128, T=8,
+                                 qkv_dtype="fp32", pool_slots=2, seed=19),
+    "accept_zero_b4_d128_t16": custom("accept_zero_b4_d128_t16", batch=4, heads=2, dk=128,
+                                      dv=128, T=16, pool_slots=8, accept="zero", seed=20),
+    "accept_full_b4_d128_t16": custom("accept_full_b4_d128_t16", batch=4, heads=2, dk=128,
+                                      dv=128, T=16, pool_slots=8, accept="full", seed=21),
+}
+
+_cache = {}
+
+
+def small(name):
+    if name not in _cache:
+        prob = SMALL[name]()
+        units = np.arange(prob.units)
+        _cache[name] = (prob, units, *oracle_units(prob, units))
+    return _cache[name]
+
+
+def algo_applies(prob, algo):
+    d = binding.gdn_problem()
+    d.batch, d.heads, d.dk, d.dv, d.max_T = prob.batch, prob.heads, prob.dk, prob.dv, prob.max_T
+    d.qkv_dtype = binding.GDN_BF16 if prob.qkv_dtype == "bf16" else binding.GDN_FP32
+    d.algo = algo
+    return binding.lib().gdn_select_algo(ctypes.byref(d)) >= 0
+
+
+def _params():
+    for name in SMALL:
+        for algo in (AUTO, REC, CHUNK):
+            for mode in ("verify", "commit", "fused"):
+                yield pytest.param(name, algo, mode,
+                                   id=f"{name}-{['auto', 'rec', 'chunk'][algo]}-{mode}")
+
+
+@pytest.mark.parametrize("name,algo,mode", list(_params()))
+def test_small_parity(name, algo, mode):
+    prob, units, o_ref, s_ref = small(name)
+    if not algo_applies(prob, algo):
+        pytest.skip("algo does not apply to this shape")
+    d = staging.DeviceProblem(prob, "cuda", algo=algo)
+    if mode == "verify":
+        check_verify(d, units, o_ref)
+    elif mode == "commit":
+        check_state_update(d, units, s_ref, d.commit)
+    else:
+        d.o.fill_(float("nan"))
+        check_state_update(d, units, s_ref, d.fused)
+        assert rel_err(gather_outputs(prob, units, d.o.cpu().numpy(), o_ref), o_ref) <= TOL
+
+
+FULL = ["b32_h32_d128_t16", "b64_h32_d128_t16_x24", "b128_h32_d128_ragged16"]
+
+
+@pytest.mark.parametrize("name", FULL)
+@pytest.mark.parametrize("mode", ["separate", "fused"])
+def test_full_size_sampled(name, mode):
+    layers = [0, 23] if name.endswith("x24") else [0]
+    for layer in layers:
+        prob = inputs.make_problem(name, layer=layer)
+        units = pick_units(prob, 40)
+        o_ref, s_ref = oracle_units(prob, units)
+        d = staging.DeviceProblem(prob, "cuda")
+        if mode == "separate":
+            check_verify(d, units, o_ref)
+            check_state_update(d, units, s_ref, d.commit)
+        else:
+            d.o.fill_(float("nan"))
+            check_state_update(d, units, s_ref, d.fused)
+            assert rel_err(gather_outputs(prob, units, d.o.cpu().numpy(), o_ref), o_ref) <= TOL
+        del d
+        torch.cuda.empty_cache()
+
+
+@pytest.mark.parametrize("golden", ["hand_2x2_t2.txt", "hand_dk3_dv2_t2.txt"])
+def test_hand_cases_exact_on_fp32_path(golden):
+    """The hand-worked fixtures hold exact binary fractions; the fp32 recurrent
+    path reproduces them exactly.  dk and dv are padded with zeros to the
+    smallest supported shape (zero rows/columns do not interact)."""
+    g = load_golden(golden)
+    dk, dv, T = int(g["dk"][0]), int(g["dv"][0]), int(g["T"][0])
+    DK, DV = 32, 32
+    s0 = np.zeros((DK, DV))
+    s0[:dk, :dv] = g["s0"].reshape(dk, dv)
+    pad = lambda x, d, Dp: np.pad(x.reshape(T, d), ((0, 0), (0, Dp - d)))
+    for a in range(T + 1):
+        prob = problem_from_arrays(s0, g["alpha"], g["beta"], pad(g["k"], dk, DK),
+                                   pad(g["v"], dv, DV), pad(g["q"], dk, DK), accepted=a)
+        d = staging.DeviceProblem(prob, "cuda", algo=REC)
+        d.fused()
+        torch.cuda.synchronize()
+        o = d.o.cpu().numpy()[:, 0, :dv]
+        assert np.array_equal(o, g["o"].reshape(T, dv).astype(np.float32))
+        st = d.pool.cpu().numpy()[0, 0, :dk, :dv]
+        assert np.array_equal(st, g[f"state_{a}"].reshape(dk, dv).astype(np.float32))
+
+
+def _with_bad(name, tweak, ragged_max_T=None, algo=AUTO):
+    lens = {"lengths": [10, 4, 6, 3]} if ragged_max_T else {"T": 8}
+    prob = inputs.make_custom(batch=4, heads=2, dk=128, dv=128, qkv_dtype="bf16",
+                              pool_slots=6, accept="uniform", seed=30, name=name, **lens)
+    d = staging.DeviceProblem(prob, "cuda", algo=algo)
+    if ragged_max_T is not None:
+        d.c.c.max_T = ragged_max_T
+    tweak(d, prob)
+    return prob, d
+
+
+@pytest.mark.parametrize("algo", [AUTO, REC])
+@pytest.mark.parametrize("kind", ["slot", "accepted", "seqlen"])
+def test_device_side_argument_errors(kind, algo):
+    """A bad slot id, accepted length or ragged length sets its error bit and the
+    unit is skipped: nothing is written for that request; the others are right."""
+    bad_r = 0
+    if kind == "slot":
+        prob, d = _with_bad("bad_slot", lambda d, p: d.slot_ids.__setitem__(bad_r, p.pool_slots + 3),
+                            algo=algo)
+        bit = binding.GDN_DEVERR_SLOT
+    elif kind == "accepted":
+        prob, d = _with_bad("bad_acc", lambda d, p: d.accepted.__setitem__(bad_r, 99), algo=algo)
+        bit = binding.GDN_DEVERR_ACCEPTED
+    else:
+        # request 0 has 10 tokens; the problem claims at most 8
+        prob, d = _with_bad("bad_len", lambda d, p: None, ragged_max_T=8, algo=algo)
+        bit = binding.GDN_DEVERR_SEQLEN
+    pool0 = d.pool.clone()
+    d.o.fill_(float("nan"))
+    d.fused()
+    code = binding.gdn_read_device_error(d.c)
+    assert code & bit
+    o = d.o.cpu().numpy()
+    rows = slice(int(prob.cu_seqlens[bad_r]), int(prob.cu_seqlens[bad_r + 1]))
+    assert np.isnan(o[rows]).all(), "skipped request's outputs were written"
+    slot = int(prob.slot_ids[bad_r])
+    assert torch.equal(d.pool[slot].view(torch.int32), pool0[slot].view(torch.int32))
+    good = [r for r in range(prob.batch) if r != bad_r]
+    units = np.array([r * prob.heads + hh for r in good for hh in range(prob.heads)])
+    o_ref, _ = oracle_units(prob, units)
+    assert rel_err(gather_outputs(prob, units, o, o_ref), o_ref) <= TOL
