@@ -219,12 +219,16 @@ def run_ours(args, rank, world, local_rank):
     torch.cuda.set_device(dev)
     binding.lib()  # fails loudly if the CUDA library is missing
     name = args.workload
-    layers = inputs.make_layers(name)
+    n_layers = inputs.WORKLOADS[name].get("layers", 1)
+    if args.layers:
+        n_layers = min(n_layers, args.layers)
+    layers = [inputs.make_problem(name, layer=l) for l in range(n_layers)]
     L = len(layers)
     p0 = layers[0]
+    multi = "layers" in inputs.WORKLOADS[name]
     pool = staging.new_pool(p0.pool_slots, p0.heads, p0.dk, p0.dv, dev, fill="zero",
-                            layers=L if L > 1 else None)
-    dps = [staging.DeviceProblem(pr, dev, pool=(pool[l] if L > 1 else pool), algo=args.algo)
+                            layers=L if multi else None)
+    dps = [staging.DeviceProblem(pr, dev, pool=(pool[l] if multi else pool), algo=args.algo)
            for l, pr in enumerate(layers)]
     fused = args.mode == "fused"
     kinds = ["f"] if fused else ["v", "c"]
@@ -408,6 +412,8 @@ def main():
                     help="separate verify + commit (default) or the fused call")
     ap.add_argument("--order", choices=["interleaved", "engine"], default="interleaved")
     ap.add_argument("--algo", type=int, default=0, help="0 auto, 1 recurrent, 2 chunk")
+    ap.add_argument("--layers", type=int, default=0,
+                    help="run only the first N layers (small cases for profiling; 0 = all)")
     ap.add_argument("--cpu-units", type=int, default=256)
     ap.add_argument("--ref-units", type=int, default=64)
     ap.add_argument("--e2e-steps", type=int, default=20)

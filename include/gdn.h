@@ -41,8 +41,10 @@
  * [0, T_r], a ragged length outside [0, max_T]) cannot be seen on the host
  * without a synchronisation; the kernel ORs a GDN_DEVERR_* bit into *dev_err
  * (when dev_err is not NULL) and skips that unit, writing nothing for it.  It
- * never traps.  Duplicate slot ids among the requests of one call are a
- * precondition violation: commit results are then undefined.
+ * never traps.  The chunked kernel's internal waits give up after about two
+ * seconds and report GDN_DEVERR_TIMEOUT instead of hanging.  Duplicate slot
+ * ids among the requests of one call are a precondition violation: commit
+ * results are then undefined.
  */
 #ifndef GDN_H
 #define GDN_H
@@ -90,6 +92,7 @@ typedef enum gdn_algo {
 #define GDN_DEVERR_SLOT     1   /* slot_ids[r] outside [0, pool_slots) */
 #define GDN_DEVERR_ACCEPTED 2   /* accepted[r] outside [0, T_r]        */
 #define GDN_DEVERR_SEQLEN   4   /* cu[r+1] - cu[r] outside [0, max_T], or rows outside [0, n_tok) */
+#define GDN_DEVERR_TIMEOUT  8   /* an internal pipeline wait gave up (about 2 s); results incomplete */
 
 /* Limits checked on the host. */
 #define GDN_MAX_T 1024          /* draft tokens per request */

@@ -37,33 +37,54 @@ struct Unit {
     float *tile;  // pool[slot_r][h], dk x dv
 };
 
-// Reads the unit's metadata and applies the device-side checks.  Every thread
-// of the block evaluates the same condition; thread 0 reports the error bit.
-// Returns false when the unit must be skipped (nothing is written for it).
-__device__ __forceinline__ bool resolve_unit(const Args &p, int r, int h, int mode, Unit &u) {
-    int err = 0;
+// A unit's metadata as loaded, before any check (so the loads can be issued
+// well ahead of their first use).
+struct RawMeta {
+    int cu0, cu1;  // token rows [cu0, cu1)
+    int slot;
+    int acc;       // accepted length, -1 in verify
+};
+
+__device__ __forceinline__ RawMeta load_meta(const Args &p, int r, int mode) {
+    RawMeta m;
     if (p.cu_seqlens) {
-        u.row0 = p.cu_seqlens[r];
-        u.T = p.cu_seqlens[r + 1] - u.row0;
-        if (u.T < 0 || u.T > p.max_T || u.row0 < 0 || (long long)u.row0 + u.T > p.n_tok)
-            err |= GDN_DEVERR_SEQLEN;
+        m.cu0 = p.cu_seqlens[r];
+        m.cu1 = p.cu_seqlens[r + 1];
     } else {
-        u.row0 = r * p.max_T;
-        u.T = p.max_T;
+        m.cu0 = r * p.max_T;
+        m.cu1 = m.cu0 + p.max_T;
     }
-    const int slot = p.slot_ids[r];
-    if (slot < 0 || (long long)slot >= p.pool_slots) err |= GDN_DEVERR_SLOT;
-    u.a = -1;
-    if (mode != kVerify) {
-        u.a = p.accepted[r];
-        if (!err && (u.a < 0 || u.a > u.T)) err |= GDN_DEVERR_ACCEPTED;
-    }
+    m.slot = p.slot_ids[r];
+    m.acc = mode != kVerify ? p.accepted[r] : -1;
+    return m;
+}
+
+// Applies the device-side checks to loaded metadata.  Only thread 0 of the
+// block reports an error bit, so callers on other threads stay silent.
+// Returns false when the unit must be skipped (nothing is written for it).
+__device__ __forceinline__ bool check_meta(const Args &p, const RawMeta &m, int h, int mode,
+                                           Unit &u) {
+    int err = 0;
+    u.row0 = m.cu0;
+    u.T = m.cu1 - m.cu0;
+    if (p.cu_seqlens && (u.T < 0 || u.T > p.max_T || u.row0 < 0 || (long long)m.cu1 > p.n_tok))
+        err |= GDN_DEVERR_SEQLEN;
+    if (m.slot < 0 || (long long)m.slot >= p.pool_slots) err |= GDN_DEVERR_SLOT;
+    u.a = m.acc;
+    if (mode != kVerify && !err && (u.a < 0 || u.a > u.T)) err |= GDN_DEVERR_ACCEPTED;
     if (err) {
         if (threadIdx.x == 0 && p.dev_err) atomicOr(p.dev_err, err);
         return false;
     }
-    u.tile = p.pool + ((size_t)slot * p.H + h) * (size_t)p.dk * p.dv;
+    u.tile = p.pool + ((size_t)m.slot * p.H + h) * (size_t)p.dk * p.dv;
     return true;
+}
+
+// Reads the unit's metadata and applies the device-side checks.  Every thread
+// of the block evaluates the same condition; thread 0 reports the error bit.
+// Returns false when the unit must be skipped (nothing is written for it).
+__device__ __forceinline__ bool resolve_unit(const Args &p, int r, int h, int mode, Unit &u) {
+    return check_meta(p, load_meta(p, r, mode), h, mode, u);
 }
 
 // Hides a pointer's value from the optimiser, so addresses derived from it are
