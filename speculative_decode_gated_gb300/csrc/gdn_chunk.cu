@@ -1,8 +1,8 @@
 // Chunked (WY) form of the gated delta rule for one block of up to 16 draft
 // tokens, with the two state-sized products on tensor cores, as a persistent
-// pipelined kernel: one block per SM walks its share of the units while a
-// producer warp streams their checkpoint tiles into a 3-stage shared-memory
-// ring with TMA.
+// kernel with two resident blocks per SM, each of which prefetches its next
+// unit's checkpoint tile and token block with TMA while it computes the
+// current unit.
 //
 // With the tile H_0 (dk x dv, H = S^T), tokens t = 0..T-1 and
 //   D[t][s] = prod_{s<r<=t} alpha_r        (D[t][t] = 1),   gamma_t = D[t][0] * alpha_0,
@@ -12,34 +12,36 @@
 //   w_t = beta_t (v_t - gamma_t Z_t) - sum_{s<t} A[t][s] w_s,  A[t][s] = beta_t D[t][s] k_t.k_s
 //   o_t = gamma_t P_t + sum_{s<=t} M[t][s] w_s,              M[t][s] = D[t][s] q_t.k_s
 //   H_a = gamma_{a-1} H_0 + sum_{s<a} D[a-1][s] k_s w_s^T    (tensor cores)
-// Each value column j is independent given the token block, so consumer warp
-// w owns the 32 columns [32w, 32w + 32) of the unit (request r, head h).
+// Each value column j is independent given the token block, so warp w of a
+// 4-warp block owns the 32 columns [32w, 32w + 32) of the unit (request r,
+// head h).
 //
-// Roles (block of 5 warps, one block per SM):
-//   warp 4 (producer, one lane): for each of the block's units, waits for a
-//     free stage, then loads the 64 KiB tile with four 3-D TMA copies (boxes of
-//     32 value columns x 128 key rows, 128-byte swizzle) onto the stage's
-//     "full" mbarrier.
-//   warps 0-3 (consumers): prefetch the next unit's q/k/v/gates into
-//     registers, stage the current unit's tokens in shared memory, build the
-//     small triangular matrices, wait for the tile, run the products, write
-//     the outputs and the committed tile, and release the stage on its
-//     "empty" mbarrier.
-// Every wait is bounded (about 2 s by %globaltimer); on expiry the block
-// reports GDN_DEVERR_TIMEOUT and stops, after waiting for its copies in flight.
+// Pipeline of one block (the block walks units blockIdx.x, + gridDim.x, ...):
+//   * thread 0 issues, for the next unit that has work, four 3-D TMA copies of
+//     its 64 KiB tile (boxes of 32 value columns x 128 key rows) into the
+//     block's single tile stage, and 16-token boxes of its k, q and v rows into
+//     the other of two token buffers, all with the 128-byte swizzle, as soon
+//     as the current unit has read the tile (right after the first product);
+//   * metadata is loaded two units ahead and the gates one unit ahead, so no
+//     thread ever waits on a load it has just issued.
+// Waits on the TMA mbarriers are bounded (about 2 s by %globaltimer); on expiry
+// the block reports GDN_DEVERR_TIMEOUT and stops after its copies have landed.
 //
 // Precision: q, k are bf16 (exact operands).  The fp32 operands (H_0 in the
 // first product, the scaled w in the second) are split into bf16 hi + lo and
 // both halves multiplied, with fp32 accumulation: about 16 mantissa bits per
 // operand.  The triangular solve and the outputs run in fp32 on CUDA cores.
+// Token rows past T_r (the next request's rows, or zero fill past the end) are
+// loaded with the box but never reach a result: w_t for t >= T_r is set to 0 by
+// selection, and every other use of those rows is multiplied by such a w_t.
 //
-// Fragment layout of H_0: lane (g = lane/4, c = lane%4) of consumer warp w
-// reads rows 16 kb + 2c + {0, 1, 8, 9} (kb = 0..7) and columns 32w + 4g + {0..3}.
-// This is at once the A-fragment layout of H_0^T for mma.m16n8k16 (value
-// columns as rows: fragment row g <-> column 4g + 2m, row g + 8 <-> 4g + 2m + 1
-// in m-tile m) and the accumulator layout of H_a^T; with the 128-byte swizzle
-// (16-byte chunk index XOR row % 8) the 16-byte shared loads are conflict-free,
-// and the committed tile leaves as 16-byte stores with full 32-byte sectors.
+// Fragment layout of H_0: lane (g = lane/4, c = lane%4) of warp w reads rows
+// 16 kb + 2c + {0, 1, 8, 9} (kb = 0..7) and columns 32w + 4g + {0..3}.  This is
+// at once the A-fragment layout of H_0^T for mma.m16n8k16 (value columns as
+// rows: fragment row g <-> column 4g + 2m, row g + 8 <-> 4g + 2m + 1 in m-tile
+// m) and the accumulator layout of H_a^T; with the 128-byte swizzle (16-byte
+// chunk index XOR row % 8) the 16-byte shared loads are conflict-free, and the
+// committed tile leaves as 16-byte stores with full 32-byte sectors.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
@@ -53,30 +55,41 @@ namespace {
 
 constexpr int CT = 16;   // token block
 constexpr int D = 128;   // dk = dv
-constexpr int KS = 136;  // bf16 row stride of the token tiles (padding: conflict-free fragments)
 constexpr int YS = 36;   // float row stride of the per-warp [column][P | Z] buffer
 constexpr int WS = 18;   // float row stride of the per-warp [column][scaled w] buffer
-constexpr int kStages = 3;
-constexpr int kConsumers = 4;  // consumer warps
-constexpr int kThreads = 32 * (kConsumers + 1);
-constexpr uint32_t kBoxBytes = 32 * D * 4;       // 32 value columns x 128 key rows
-constexpr uint32_t kTileBytes = 4 * kBoxBytes;   // 64 KiB
+constexpr int kThreads = 128;
+constexpr int kBlocksPerSM = 2;
+constexpr uint32_t kBoxBytes = 32 * D * 4;        // tile box: 32 value columns x 128 key rows
+constexpr uint32_t kTileBytes = 4 * kBoxBytes;    // 64 KiB
+constexpr uint32_t kTokHalfBytes = CT * 64 * 2;   // token box: 64 of 128 bf16 x 16 tokens
+constexpr uint32_t kTokBytes = 2 * kTokHalfBytes; // one [16][128] bf16 tile
 constexpr unsigned long long kWaitNs = 2000000000ull;
 
+struct TokBuf {  // 1024-byte aligned: three swizzled [16][128] bf16 tiles
+    unsigned char k[kTokBytes];
+    unsigned char q[kTokBytes];
+    unsigned char v[kTokBytes];
+};
+
 struct Aux {
-    __nv_bfloat16 k[CT][KS];
-    __nv_bfloat16 q[CT][KS];
     float gram[2][CT][CT];  // [0][t][s] = k_t.k_s, [1][t][s] = q_t.k_s
-    float A[CT][CT];        // beta_t D[t][s] k_t.k_s for s < t, else 0
+    float A[CT][CT];        // beta_t D[t][s] k_t.k_s for s < t < T, else 0
     float M[CT][CT];        // D[t][s] q_t.k_s for s <= t, else 0
     float alpha[CT], beta[CT], gamma[CT];
     float dcol[CT];         // D[a-1][s] for s < a, else 0
-    float y[kConsumers][32][YS];  // per warp; reused for the scaled w
-    unsigned long long full[kStages], empty[kStages];
-    int abort_flag;  // a consumer's wait expired: all consumers stop together
+    float y[4][32][YS];     // per warp; reused for the scaled w
+    unsigned long long tile_full, tok_full[2];
+    int abort_flag;
 };
-constexpr size_t kSmemBytes = 1024 + (size_t)kStages * kTileBytes + sizeof(Aux);
-static_assert(kSmemBytes <= 232448, "shared memory budget");
+
+struct Smem {
+    unsigned char tile[kTileBytes];
+    TokBuf tok[2];
+    Aux aux;
+};
+constexpr size_t kSmemBytes = 1024 + sizeof(Smem);
+static_assert(sizeof(TokBuf) % 1024 == 0, "token buffers stay 1024-byte aligned");
+static_assert(kBlocksPerSM * (kSmemBytes + 1024) <= 233472, "two blocks per SM");
 
 // ------------------------------------------------------------ PTX helpers
 
@@ -91,10 +104,6 @@ __device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
 __device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes) {
     asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;\n" ::"r"(bar), "r"(bytes)
                  : "memory");
-}
-
-__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
-    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];\n" ::"r"(bar) : "memory");
 }
 
 __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
@@ -130,21 +139,13 @@ __device__ __noinline__ bool wait_parity(uint32_t bar, uint32_t parity) {
     }
 }
 
-__device__ __forceinline__ void tma_load_box(uint32_t dst, const CUtensorMap *map, int c0, int c1,
-                                             int c2, uint32_t bar) {
+__device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap *map, int c0, int c1,
+                                            int c2, uint32_t bar) {
     asm volatile(
         "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
         " [%0], [%1, {%2, %3, %4}], [%5];\n" ::"r"(dst),
         "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(bar)
         : "memory");
-}
-
-__device__ __forceinline__ void consumer_sync() {
-    asm volatile("bar.sync 1, %0;\n" ::"n"(32 * kConsumers) : "memory");
-}
-
-__device__ __forceinline__ uint32_t lds32(const __nv_bfloat16 *p) {
-    return *reinterpret_cast<const uint32_t *>(p);
 }
 
 // fp32 pair -> bf16x2 hi and lo with x = hi + lo + O(2^-17 |x|).
@@ -167,31 +168,36 @@ __device__ __forceinline__ void mma(float &d0, float &d1, float &d2, float &d3, 
 }
 
 __device__ __forceinline__ void ldsm_x4_trans(uint32_t &r0, uint32_t &r1, uint32_t &r2,
-                                              uint32_t &r3, const void *row) {
+                                              uint32_t &r3, uint32_t addr) {
     asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];\n"
                  : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
-                 : "r"(smem_u32(row)));
+                 : "r"(addr));
 }
 
-// Row `row`, 16-byte chunk `chunk` of a 128-byte-swizzled box (32 floats per row).
-__device__ __forceinline__ float4 ld_box(const char *box, int row, int chunk) {
+// Row `row`, 16-byte chunk `chunk` of a 128-byte-swizzled tile box (32 floats per row).
+__device__ __forceinline__ float4 ld_box(const unsigned char *box, int row, int chunk) {
     return *reinterpret_cast<const float4 *>(box + row * 128 + ((chunk ^ (row & 7)) << 4));
 }
 
-// ------------------------------------------------------------ per-unit data
+// Byte offset of bf16 element (t, i) in a swizzled [16][128] token tile
+// (two boxes of 64 columns, 128 bytes per token row).
+__device__ __forceinline__ uint32_t tok_off(int t, int i) {
+    return (uint32_t)((i >> 6) * kTokHalfBytes + t * 128 + ((((i & 63) >> 3) ^ (t & 7)) << 4) +
+                      (i & 7) * 2);
+}
 
-// What both roles know about a unit; `skip` when nothing is to be done.
+__device__ __forceinline__ uint32_t ld_tok32(const unsigned char *tile, int t, int i) {
+    return *reinterpret_cast<const uint32_t *>(tile + tok_off(t, i));
+}
+
+// ------------------------------------------------------------ per-unit plan
+
 struct UnitPlan {
     Unit u;
     int h;
     int teff;  // tokens that matter: T_r, or a_r for commit
     bool skip;
 };
-
-template <int MODE>
-__device__ __forceinline__ RawMeta load_unit_meta(const Args &p, int unit) {
-    return load_meta(p, unit / p.H, MODE);
-}
 
 template <int MODE>
 __device__ __forceinline__ UnitPlan plan_unit(const Args &p, int unit, const RawMeta &m) {
@@ -203,215 +209,180 @@ __device__ __forceinline__ UnitPlan plan_unit(const Args &p, int unit, const Raw
     return pl;
 }
 
-// Token block of one unit held in registers by a consumer thread (tid < 128):
-// four 16-byte chunks of the k / q tiles, this lane's v column (raw bf16 bits,
-// converted only where used so the loads stay in flight), and alpha/beta of
-// token tid (tid < 16).
-struct TokRegs {
-    uint4 qk[4];
-    unsigned short v[CT];
-    float a, b;
+struct Maps {
+    CUtensorMap pool, q, k, v;
 };
 
+// Thread 0: the tile and token boxes of one unit, onto the given mbarriers.
 template <int MODE>
-__device__ __forceinline__ void load_tokens(const Args &p, const UnitPlan &pl, int tid, TokRegs &tr) {
-    const size_t row_stride = (size_t)p.H * D;
-    const size_t tok0 = ((size_t)pl.u.row0 * p.H + pl.h) * D;
-    const __nv_bfloat16 *gq = reinterpret_cast<const __nv_bfloat16 *>(p.q) + tok0;
-    const __nv_bfloat16 *gk = reinterpret_cast<const __nv_bfloat16 *>(p.k) + tok0;
-    const int T = pl.skip ? 0 : pl.teff;
+__device__ __forceinline__ void issue_unit(const Maps &maps, const Args &p, const UnitPlan &pl,
+                                           unsigned char *tile, TokBuf &tb, uint32_t tile_bar,
+                                           uint32_t tok_bar) {
+    const int slot_unit = (int)((pl.u.tile - p.pool) / (D * D));  // slot * H + h
+    mbar_arrive_expect_tx(tile_bar, kTileBytes);
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
-        const int e = tid + 128 * i;
-        const int which = e >> 8;  // 0: k, 1: q
-        const int t = (e >> 4) & (CT - 1);
-        const int ch = e & 15;
-        tr.qk[i] = make_uint4(0u, 0u, 0u, 0u);
-        if (t < T && (which == 0 || MODE != kCommit))
-            tr.qk[i] = *reinterpret_cast<const uint4 *>((which ? gq : gk) + t * row_stride + 8 * ch);
-    }
-    const unsigned short *gv = reinterpret_cast<const unsigned short *>(p.v) + tok0 + tid;
+    for (int b = 0; b < 4; ++b)
+        tma_load_3d(smem_u32(tile) + b * kBoxBytes, &maps.pool, 32 * b, 0, slot_unit, tile_bar);
+    const uint32_t tok_bytes = (MODE == kCommit ? 2u : 3u) * kTokBytes;
+    mbar_arrive_expect_tx(tok_bar, tok_bytes);
 #pragma unroll
-    for (int t = 0; t < CT; ++t) {
-        tr.v[t] = 0;
-        if (t < T) tr.v[t] = gv[t * row_stride];
+    for (int hb = 0; hb < 2; ++hb) {
+        tma_load_3d(smem_u32(tb.k) + hb * kTokHalfBytes, &maps.k, 64 * hb, pl.h, pl.u.row0, tok_bar);
+        tma_load_3d(smem_u32(tb.v) + hb * kTokHalfBytes, &maps.v, 64 * hb, pl.h, pl.u.row0, tok_bar);
+        if (MODE != kCommit)
+            tma_load_3d(smem_u32(tb.q) + hb * kTokHalfBytes, &maps.q, 64 * hb, pl.h, pl.u.row0,
+                        tok_bar);
     }
-    tr.a = 1.0f;
-    tr.b = 0.0f;
-    if (tid < T) {
-        const size_t x = (size_t)(pl.u.row0 + tid) * p.H + pl.h;
-        tr.a = p.alpha[x];
-        tr.b = p.beta[x];
-    }
-}
-
-__device__ __forceinline__ float bf16_bits_to_float(unsigned short b) {
-    return __uint_as_float((uint32_t)b << 16);
 }
 
 // ------------------------------------------------------------ the kernel
 
 template <int MODE>
-__global__ void __launch_bounds__(kThreads, 1)
-    chunk_kernel(const Args p, const __grid_constant__ CUtensorMap tmap) {
+__global__ void __launch_bounds__(kThreads, kBlocksPerSM)
+    chunk_kernel(const Args p, const __grid_constant__ Maps maps) {
     extern __shared__ unsigned char smem_raw[];
-    // 1024-byte alignment of the stage ring (required by the 128-byte swizzle).
     const uint32_t raw_addr = smem_u32(smem_raw);
-    unsigned char *stages = smem_raw + ((1024u - (raw_addr & 1023u)) & 1023u);
-    Aux &sm = *reinterpret_cast<Aux *>(stages + (size_t)kStages * kTileBytes);
+    Smem &sm = *reinterpret_cast<Smem *>(smem_raw + ((1024u - (raw_addr & 1023u)) & 1023u));
+    Aux &ax = sm.aux;
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int g = lane >> 2, c = lane & 3;
     const int U = p.B * p.H;
+    const int G = gridDim.x;
+    const size_t row_stride = (size_t)p.H * D;
+    const uint32_t tile_bar = smem_u32(&ax.tile_full);
 
     if (tid == 0) {
-        for (int s = 0; s < kStages; ++s) {
-            mbar_init(smem_u32(&sm.full[s]), 1);
-            mbar_init(smem_u32(&sm.empty[s]), kConsumers);
-        }
-        sm.abort_flag = 0;
+        mbar_init(tile_bar, 1);
+        mbar_init(smem_u32(&ax.tok_full[0]), 1);
+        mbar_init(smem_u32(&ax.tok_full[1]), 1);
+        ax.abort_flag = 0;
         asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
     }
     __syncthreads();
 
-    // ---------------------------------------------------------- producer
-    if (warp == kConsumers) {
-        if (lane != 0) return;
-        int stage = 0;
-        uint32_t phase = 0;
-        int issued = 0;
-        uint32_t last_parity[kStages] = {0, 0, 0};
-        bool timed_out = false;
-        // Metadata is loaded one unit ahead of its use.
-        RawMeta raw = load_unit_meta<MODE>(p, blockIdx.x < U ? blockIdx.x : 0);
-        for (int unit = blockIdx.x; unit < U; unit += gridDim.x) {
-            const UnitPlan pl = plan_unit<MODE>(p, unit, raw);
-            if (unit + (int)gridDim.x < U) raw = load_unit_meta<MODE>(p, unit + gridDim.x);
-            if (pl.skip) continue;
-            if (!wait_parity(smem_u32(&sm.empty[stage]), phase ^ 1u)) {
-                timed_out = true;
-                break;
-            }
-            const uint32_t full = smem_u32(&sm.full[stage]);
-            mbar_arrive_expect_tx(full, kTileBytes);
-            const int slot_unit = (int)((pl.u.tile - p.pool) / (D * D));  // slot * H + h
-            const uint32_t dst = smem_u32(stages + (size_t)stage * kTileBytes);
-#pragma unroll
-            for (int b = 0; b < 4; ++b) tma_load_box(dst + b * kBoxBytes, &tmap, 32 * b, 0, slot_unit, full);
-            last_parity[stage] = phase;
-            ++issued;
-            if (++stage == kStages) {
-                stage = 0;
-                phase ^= 1u;
-            }
-        }
-        // Copies still in flight must land before the block exits.
-        for (int s = 0; s < kStages && s < issued; ++s)
-            if (!wait_parity(smem_u32(&sm.full[s]), last_parity[s])) timed_out = true;
-        if (timed_out && p.dev_err) atomicOr(p.dev_err, GDN_DEVERR_TIMEOUT);
-        return;
-    }
-
-    // ---------------------------------------------------------- consumers
-    const int g = lane >> 2, c = lane & 3;
-    const size_t row_stride = (size_t)p.H * D;
-    int stage = 0;
-    uint32_t phase = 0;
-
-    // Pipeline of the consumers' own loads: metadata two units ahead, the token
-    // block one unit ahead, so no load is waited on in the iteration that issues it.
-    const int G = gridDim.x;
-    UnitPlan nxt;
-    TokRegs tn;
-    RawMeta raw2;
+    // Plans: `cur` is the unit being computed, `nxt` the next one (its loads are
+    // issued during `cur`), `raw` the metadata of the one after.
     int unit = blockIdx.x;
-    if (unit < U) {
-        nxt = plan_unit<MODE>(p, unit, load_unit_meta<MODE>(p, unit));
-        load_tokens<MODE>(p, nxt, tid, tn);
-        if (unit + G < U) raw2 = load_unit_meta<MODE>(p, unit + G);
-    }
-    for (; unit < U; unit += G) {
-        const UnitPlan cur = nxt;
-        const TokRegs tc = tn;
-        if (unit + G < U) {
-            nxt = plan_unit<MODE>(p, unit + G, raw2);
-            if (unit + 2 * G < U) raw2 = load_unit_meta<MODE>(p, unit + 2 * G);
-            load_tokens<MODE>(p, nxt, tid, tn);
-        }
-        if (cur.skip) continue;
-        const int T = cur.teff;
-        const bool write_state = MODE != kVerify && cur.u.a > 0;
+    UnitPlan cur, nxt;
+    RawMeta raw;
+    cur.skip = true;
+    nxt.skip = true;
+    if (unit < U) cur = plan_unit<MODE>(p, unit, load_meta(p, unit / p.H, MODE));
+    if (unit + G < U) nxt = plan_unit<MODE>(p, unit + G, load_meta(p, (unit + G) / p.H, MODE));
+    if (unit + 2 * G < U) raw = load_meta(p, (unit + 2 * G) / p.H, MODE);
 
-        // 1. Stage the token block (the previous unit is done with it).
-        consumer_sync();
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            const int e = tid + 128 * i;
-            const int t = (e >> 4) & (CT - 1);
-            const int ch = e & 15;
-            *reinterpret_cast<uint4 *>((e >> 8) ? &sm.q[t][8 * ch] : &sm.k[t][8 * ch]) = tc.qk[i];
+    int issued = 0;     // units whose loads were issued
+    int processed = 0;  // units computed
+    if (tid == 0 && !cur.skip) {
+        issue_unit<MODE>(maps, p, cur, sm.tile, sm.tok[0], tile_bar, smem_u32(&ax.tok_full[0]));
+    }
+    if (!cur.skip) ++issued;
+    // Gates of the current unit: thread t < 16 holds alpha_t, beta_t.
+    float ga = 1.0f, gb = 0.0f;
+    if (!cur.skip && tid < cur.teff) {
+        const size_t x = (size_t)(cur.u.row0 + tid) * p.H + cur.h;
+        ga = p.alpha[x];
+        gb = p.beta[x];
+    }
+
+    bool aborted = false;
+    for (; unit < U; unit += G) {
+        // Advance the metadata pipeline.
+        const UnitPlan me = cur;
+        cur = nxt;
+        nxt.skip = true;
+        if (unit + 2 * G < U) nxt = plan_unit<MODE>(p, unit + 2 * G, raw);
+        if (unit + 3 * G < U) raw = load_meta(p, (unit + 3 * G) / p.H, MODE);
+        // Gates of the next unit (consumed one iteration later).
+        float na = 1.0f, nb = 0.0f;
+        if (!cur.skip && tid < cur.teff) {
+            const size_t x = (size_t)(cur.u.row0 + tid) * p.H + cur.h;
+            na = p.alpha[x];
+            nb = p.beta[x];
         }
+        if (me.skip) {
+            ga = na;
+            gb = nb;
+            if (tid == 0 && !cur.skip && issued == processed) {
+                // Nothing is in the stage: the next unit's loads can go now.
+                issue_unit<MODE>(maps, p, cur, sm.tile, sm.tok[issued & 1], tile_bar,
+                                 smem_u32(&ax.tok_full[issued & 1]));
+            }
+            if (!cur.skip && issued == processed) ++issued;
+            continue;
+        }
+        const int T = me.teff;
+        const int buf = processed & 1;
+        const TokBuf &tb = sm.tok[buf];
+        const bool write_state = MODE != kVerify && me.u.a > 0;
+
+        // 1. Gates into shared memory; token block arrival.
+        __syncthreads();  // the previous unit is done with the small matrices
         if (tid < CT) {
-            sm.alpha[tid] = tc.a;
-            sm.beta[tid] = tc.b;
+            ax.alpha[tid] = ga;
+            ax.beta[tid] = gb;
         }
-        consumer_sync();
+        ga = na;
+        gb = nb;
+        if (!wait_parity(smem_u32(&ax.tok_full[buf]), (processed >> 1) & 1)) ax.abort_flag = 1;
+        __syncthreads();
+        if (ax.abort_flag) {
+            aborted = true;
+            break;
+        }
 
         // 2. Gram blocks k_t.k_s and q_t.k_s: warp w computes matrix w/2, columns 8 (w%2) + [0, 8).
         {
-            const __nv_bfloat16(*At)[KS] = (warp >> 1) ? sm.q : sm.k;
+            const unsigned char *At = (warp >> 1) ? tb.q : tb.k;
             const int nt = warp & 1;
-            float acc[4] = {0.f, 0.f, 0.f, 0.f};
+            float a0[4] = {0.f, 0.f, 0.f, 0.f}, a1[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
             for (int kb = 0; kb < 8; ++kb) {
                 const int col = 16 * kb + 2 * c;
-                mma(acc[0], acc[1], acc[2], acc[3], lds32(&At[g][col]), lds32(&At[g + 8][col]),
-                    lds32(&At[g][col + 8]), lds32(&At[g + 8][col + 8]),
-                    lds32(&sm.k[8 * nt + g][col]), lds32(&sm.k[8 * nt + g][col + 8]));
+                float *acc = (kb & 1) ? a1 : a0;
+                mma(acc[0], acc[1], acc[2], acc[3], ld_tok32(At, g, col), ld_tok32(At, g + 8, col),
+                    ld_tok32(At, g, col + 8), ld_tok32(At, g + 8, col + 8),
+                    ld_tok32(tb.k, 8 * nt + g, col), ld_tok32(tb.k, 8 * nt + g, col + 8));
             }
-            float(*G)[CT] = sm.gram[warp >> 1];
-            G[g][8 * nt + 2 * c] = acc[0];
-            G[g][8 * nt + 2 * c + 1] = acc[1];
-            G[g + 8][8 * nt + 2 * c] = acc[2];
-            G[g + 8][8 * nt + 2 * c + 1] = acc[3];
+            float(*Gm)[CT] = ax.gram[warp >> 1];
+            Gm[g][8 * nt + 2 * c] = a0[0] + a1[0];
+            Gm[g][8 * nt + 2 * c + 1] = a0[1] + a1[1];
+            Gm[g + 8][8 * nt + 2 * c] = a0[2] + a1[2];
+            Gm[g + 8][8 * nt + 2 * c + 1] = a0[3] + a1[3];
         }
-        consumer_sync();
+        __syncthreads();
 
-        // 3. Decay products and the two triangular matrices (lane t of warp 0 owns row t).
-        if (warp == 0 && lane < CT) {
-            const int t = lane;
-            const int a_last = (MODE == kVerify) ? -1 : cur.u.a - 1;
-            float d = 1.0f;  // D[t][s], walking s = t, t-1, ..., 0
+        // 3. Decay products and the triangular matrices, two (t, s) pairs per thread.
 #pragma unroll
-            for (int s = CT - 1; s >= 0; --s) {
-                if (s <= t) {
-                    sm.A[t][s] = s < t ? sm.beta[t] * d * sm.gram[0][t][s] : 0.0f;
-                    sm.M[t][s] = d * sm.gram[1][t][s];
-                    if (t == a_last) sm.dcol[s] = d;
-                    d *= sm.alpha[s];  // D[t][s-1] = D[t][s] alpha_s; after s = 0: gamma_t
-                } else {
-                    sm.A[t][s] = 0.0f;
-                    sm.M[t][s] = 0.0f;
-                    if (t == a_last) sm.dcol[s] = 0.0f;
-                }
-            }
-            sm.gamma[t] = d;
+        for (int e2 = 0; e2 < 2; ++e2) {
+            const int e = tid + 128 * e2;
+            const int t = e >> 4, s = e & 15;
+            float d = 1.0f;  // D[t][s] = prod_{s<r<=t} alpha_r
+#pragma unroll
+            for (int r = 1; r < CT; ++r)
+                if (r > s && r <= t) d *= ax.alpha[r];
+            ax.A[t][s] = (s < t && t < T) ? ax.beta[t] * d * ax.gram[0][t][s] : 0.0f;
+            ax.M[t][s] = (s <= t) ? d * ax.gram[1][t][s] : 0.0f;
+            if (s == 0) ax.gamma[t] = d * ax.alpha[0];
+            if (MODE != kVerify && t == me.u.a - 1) ax.dcol[s] = (s <= t) ? d : 0.0f;
         }
-        consumer_sync();
+        __syncthreads();
 
-        // 4. The checkpoint tile of this unit.  Every consumer thread's wait is
-        //    bounded; they then agree, so none is left at a barrier alone.
-        if (!wait_parity(smem_u32(&sm.full[stage]), phase)) sm.abort_flag = 1;
-        consumer_sync();
-        if (sm.abort_flag) {
-            if (tid == 0 && p.dev_err) atomicOr(p.dev_err, GDN_DEVERR_TIMEOUT);
+        // 4. The checkpoint tile of this unit.
+        if (!wait_parity(tile_bar, processed & 1)) ax.abort_flag = 1;
+        __syncthreads();
+        if (ax.abort_flag) {
+            aborted = true;
             break;
         }
-        const char *box = reinterpret_cast<const char *>(stages + (size_t)stage * kTileBytes) +
-                          warp * kBoxBytes;
+        const unsigned char *box = sm.tile + warp * kBoxBytes;
 
         // 5. P = H_0^T Q^T and Z = H_0^T K^T for this warp's 32 columns (N-tiles: Q 0-7,
-        //    Q 8-15, K 0-7, K 8-15; commit needs only Z).
+        //    Q 8-15, K 0-7, K 8-15; commit needs only Z).  The tile is kept in
+        //    registers when the commit needs it again.
         constexpr int NT0 = (MODE == kCommit) ? 2 : 0;
+        float hr[8][4][4];
         float y[2][4][4];
 #pragma unroll
         for (int m = 0; m < 2; ++m)
@@ -421,46 +392,52 @@ __global__ void __launch_bounds__(kThreads, 1)
                 for (int e = 0; e < 4; ++e) y[m][nt][e] = 0.0f;
 #pragma unroll
         for (int kb = 0; kb < 8; ++kb) {
-            float hv[4][4];
 #pragma unroll
             for (int rr = 0; rr < 4; ++rr) {
                 const float4 x = ld_box(box, 16 * kb + 2 * c + (rr & 1) + 8 * (rr >> 1), g);
-                hv[rr][0] = x.x;
-                hv[rr][1] = x.y;
-                hv[rr][2] = x.z;
-                hv[rr][3] = x.w;
+                hr[kb][rr][0] = x.x;
+                hr[kb][rr][1] = x.y;
+                hr[kb][rr][2] = x.z;
+                hr[kb][rr][3] = x.w;
             }
             uint32_t b[4][2];
 #pragma unroll
             for (int nt = NT0; nt < 4; ++nt) {
-                const __nv_bfloat16(*Bt)[KS] = nt < 2 ? sm.q : sm.k;
+                const unsigned char *Bt = nt < 2 ? tb.q : tb.k;
                 const int tok = 8 * (nt & 1) + g;
-                b[nt][0] = lds32(&Bt[tok][16 * kb + 2 * c]);
-                b[nt][1] = lds32(&Bt[tok][16 * kb + 2 * c + 8]);
+                b[nt][0] = ld_tok32(Bt, tok, 16 * kb + 2 * c);
+                b[nt][1] = ld_tok32(Bt, tok, 16 * kb + 2 * c + 8);
             }
 #pragma unroll
             for (int m = 0; m < 2; ++m) {
                 uint32_t ah[4], al[4];
-                split2(hv[0][2 * m], hv[1][2 * m], ah[0], al[0]);
-                split2(hv[0][2 * m + 1], hv[1][2 * m + 1], ah[1], al[1]);
-                split2(hv[2][2 * m], hv[3][2 * m], ah[2], al[2]);
-                split2(hv[2][2 * m + 1], hv[3][2 * m + 1], ah[3], al[3]);
+                split2(hr[kb][0][2 * m], hr[kb][1][2 * m], ah[0], al[0]);
+                split2(hr[kb][0][2 * m + 1], hr[kb][1][2 * m + 1], ah[1], al[1]);
+                split2(hr[kb][2][2 * m], hr[kb][3][2 * m], ah[2], al[2]);
+                split2(hr[kb][2][2 * m + 1], hr[kb][3][2 * m + 1], ah[3], al[3]);
 #pragma unroll
-                for (int nt = NT0; nt < 4; ++nt) {
-                    float *d = y[m][nt];
-                    mma(d[0], d[1], d[2], d[3], ah[0], ah[1], ah[2], ah[3], b[nt][0], b[nt][1]);
-                    mma(d[0], d[1], d[2], d[3], al[0], al[1], al[2], al[3], b[nt][0], b[nt][1]);
-                }
+                for (int nt = NT0; nt < 4; ++nt)
+                    mma(y[m][nt][0], y[m][nt][1], y[m][nt][2], y[m][nt][3], ah[0], ah[1], ah[2],
+                        ah[3], b[nt][0], b[nt][1]);
+#pragma unroll
+                for (int nt = NT0; nt < 4; ++nt)
+                    mma(y[m][nt][0], y[m][nt][1], y[m][nt][2], y[m][nt][3], al[0], al[1], al[2],
+                        al[3], b[nt][0], b[nt][1]);
             }
         }
-        const uint32_t empty = smem_u32(&sm.empty[stage]);
-        if (!write_state) {  // the tile is not read again: hand the stage back now
-            __syncwarp();
-            if (lane == 0) mbar_arrive(empty);
+        ++processed;
+
+        // The tile stage is free: thread 0 sends the next unit's loads.
+        __syncthreads();
+        if (!cur.skip) {
+            if (tid == 0)
+                issue_unit<MODE>(maps, p, cur, sm.tile, sm.tok[issued & 1], tile_bar,
+                                 smem_u32(&ax.tok_full[issued & 1]));
+            ++issued;
         }
 
         // 6. Fragments -> per-warp [column][P | Z] buffer -> lane j holds column 32w + j.
-        float(*yb)[YS] = sm.y[warp];
+        float(*yb)[YS] = ax.y[warp];
 #pragma unroll
         for (int m = 0; m < 2; ++m)
 #pragma unroll
@@ -489,38 +466,52 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
         }
 
-        // 7. Forward substitution for w (fp32), one column per lane.
+        // 7. Forward substitution for w (fp32), one column per lane; w_t = 0 past T.
         float w[CT];
 #pragma unroll
         for (int t = 0; t < CT; ++t) {
-            float acc = sm.beta[t] * (bf16_bits_to_float(tc.v[t]) - sm.gamma[t] * z[t]);
+            const uint32_t vb = *reinterpret_cast<const unsigned short *>(
+                tb.v + tok_off(t, 32 * warp + lane));
+            float acc = ax.beta[t] * (__uint_as_float(vb << 16) - ax.gamma[t] * z[t]);
 #pragma unroll
-            for (int s = 0; s < t; ++s) acc = fmaf(-sm.A[t][s], w[s], acc);
-            w[t] = acc;
+            for (int s4 = 0; s4 < t; s4 += 4) {
+                const float4 a4 = *reinterpret_cast<const float4 *>(&ax.A[t][s4]);
+                acc = fmaf(-a4.x, w[s4], acc);
+                if (s4 + 1 < t) acc = fmaf(-a4.y, w[s4 + 1], acc);
+                if (s4 + 2 < t) acc = fmaf(-a4.z, w[s4 + 2], acc);
+                if (s4 + 3 < t) acc = fmaf(-a4.w, w[s4 + 3], acc);
+            }
+            w[t] = t < T ? acc : 0.0f;
         }
 
         // 8. Outputs o_t for t < T_r.
         if (MODE != kCommit) {
-            float *go = p.o + ((size_t)cur.u.row0 * p.H + cur.h) * D + 32 * warp + lane;
+            float *go = p.o + ((size_t)me.u.row0 * p.H + me.h) * D + 32 * warp + lane;
 #pragma unroll
             for (int t = 0; t < CT; ++t) {
                 if (t < T) {
-                    float acc = sm.gamma[t] * pq[t];
+                    float acc = ax.gamma[t] * pq[t];
 #pragma unroll
-                    for (int s = 0; s <= t; ++s) acc = fmaf(sm.M[t][s], w[s], acc);
+                    for (int s4 = 0; s4 <= t; s4 += 4) {
+                        const float4 m4 = *reinterpret_cast<const float4 *>(&ax.M[t][s4]);
+                        acc = fmaf(m4.x, w[s4], acc);
+                        if (s4 + 1 <= t) acc = fmaf(m4.y, w[s4 + 1], acc);
+                        if (s4 + 2 <= t) acc = fmaf(m4.z, w[s4 + 2], acc);
+                        if (s4 + 3 <= t) acc = fmaf(m4.w, w[s4 + 3], acc);
+                    }
                     go[t * row_stride] = acc;
                 }
             }
         }
 
-        // 9. Commit: H_a^T = gamma_{a-1} H_0^T + (D[a-1][.] w)^T K, tile by tile of 16 rows.
+        // 9. Commit: H_a^T = gamma_{a-1} H_0^T + (D[a-1][.] w)^T K, accumulated in hr.
         if (write_state) {
             __syncwarp();  // yb is reused
-            float(*wb)[WS] = reinterpret_cast<float(*)[WS]>(&sm.y[warp][0][0]);
+            float(*wb)[WS] = reinterpret_cast<float(*)[WS]>(&ax.y[warp][0][0]);
 #pragma unroll
             for (int s = 0; s < CT; s += 2)
                 *reinterpret_cast<float2 *>(&wb[lane][s]) =
-                    make_float2(sm.dcol[s] * w[s], sm.dcol[s + 1] * w[s + 1]);
+                    make_float2(ax.dcol[s] * w[s], ax.dcol[s + 1] * w[s + 1]);
             __syncwarp();
             uint32_t ah[2][4], al[2][4];
 #pragma unroll
@@ -532,50 +523,51 @@ __global__ void __launch_bounds__(kThreads, 1)
                 split2(r0[2 * c + 8], r0[2 * c + 9], ah[m][2], al[m][2]);
                 split2(r1[2 * c + 8], r1[2 * c + 9], ah[m][3], al[m][3]);
             }
-            const float gam = sm.gamma[cur.u.a - 1];
+            const float gam = ax.gamma[me.u.a - 1];
             // ldmatrix.trans row address of this lane: matrix lane/8 -> (token half, dk half).
             const int mi = lane >> 3;
-            const __nv_bfloat16 *krow = &sm.k[(lane & 7) + 8 * (mi & 1)][8 * (mi >> 1)];
-            float *dst = opaque(cur.u.tile) + 32 * warp + 4 * g;
+            const int krow = (lane & 7) + 8 * (mi & 1);
+            float *dst = opaque(me.u.tile) + 32 * warp + 4 * g;
 #pragma unroll
             for (int kb = 0; kb < 8; ++kb) {
-                float hv[4][4];
 #pragma unroll
-                for (int rr = 0; rr < 4; ++rr) {
-                    const float4 x = ld_box(box, 16 * kb + 2 * c + (rr & 1) + 8 * (rr >> 1), g);
-                    hv[rr][0] = gam * x.x;
-                    hv[rr][1] = gam * x.y;
-                    hv[rr][2] = gam * x.z;
-                    hv[rr][3] = gam * x.w;
-                }
+                for (int rr = 0; rr < 4; ++rr)
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) hr[kb][rr][e] *= gam;
                 uint32_t b00, b01, b10, b11;  // (n-tile 2kb: b0, b1), (n-tile 2kb+1: b0, b1)
-                ldsm_x4_trans(b00, b01, b10, b11, krow + 16 * kb);
+                ldsm_x4_trans(b00, b01, b10, b11,
+                              smem_u32(tb.k) + tok_off(krow, 16 * kb + 8 * (mi >> 1)));
 #pragma unroll
                 for (int m = 0; m < 2; ++m) {
-                    mma(hv[0][2 * m], hv[1][2 * m], hv[0][2 * m + 1], hv[1][2 * m + 1], ah[m][0],
-                        ah[m][1], ah[m][2], ah[m][3], b00, b01);
-                    mma(hv[0][2 * m], hv[1][2 * m], hv[0][2 * m + 1], hv[1][2 * m + 1], al[m][0],
-                        al[m][1], al[m][2], al[m][3], b00, b01);
-                    mma(hv[2][2 * m], hv[3][2 * m], hv[2][2 * m + 1], hv[3][2 * m + 1], ah[m][0],
-                        ah[m][1], ah[m][2], ah[m][3], b10, b11);
-                    mma(hv[2][2 * m], hv[3][2 * m], hv[2][2 * m + 1], hv[3][2 * m + 1], al[m][0],
-                        al[m][1], al[m][2], al[m][3], b10, b11);
+                    mma(hr[kb][0][2 * m], hr[kb][1][2 * m], hr[kb][0][2 * m + 1],
+                        hr[kb][1][2 * m + 1], ah[m][0], ah[m][1], ah[m][2], ah[m][3], b00, b01);
+                    mma(hr[kb][2][2 * m], hr[kb][3][2 * m], hr[kb][2][2 * m + 1],
+                        hr[kb][3][2 * m + 1], ah[m][0], ah[m][1], ah[m][2], ah[m][3], b10, b11);
+                }
+#pragma unroll
+                for (int m = 0; m < 2; ++m) {
+                    mma(hr[kb][0][2 * m], hr[kb][1][2 * m], hr[kb][0][2 * m + 1],
+                        hr[kb][1][2 * m + 1], al[m][0], al[m][1], al[m][2], al[m][3], b00, b01);
+                    mma(hr[kb][2][2 * m], hr[kb][3][2 * m], hr[kb][2][2 * m + 1],
+                        hr[kb][3][2 * m + 1], al[m][0], al[m][1], al[m][2], al[m][3], b10, b11);
                 }
 #pragma unroll
                 for (int rr = 0; rr < 4; ++rr) {
                     const int row = 16 * kb + 2 * c + (rr & 1) + 8 * (rr >> 1);
                     *reinterpret_cast<float4 *>(dst + row * D) =
-                        make_float4(hv[rr][0], hv[rr][1], hv[rr][2], hv[rr][3]);
+                        make_float4(hr[kb][rr][0], hr[kb][rr][1], hr[kb][rr][2], hr[kb][rr][3]);
                 }
             }
-            __syncwarp();
-            if (lane == 0) mbar_arrive(empty);
-        }
-        if (++stage == kStages) {
-            stage = 0;
-            phase ^= 1u;
         }
     }
+
+    // Copies still in flight must land before the block exits.
+    if (tid == 0 && issued > processed) {
+        bool ok = wait_parity(tile_bar, processed & 1);
+        ok = wait_parity(smem_u32(&ax.tok_full[processed & 1]), (processed >> 1) & 1) && ok;
+        if (!ok) aborted = true;
+    }
+    if (tid == 0 && aborted && p.dev_err) atomicOr(p.dev_err, GDN_DEVERR_TIMEOUT);
 }
 
 // ------------------------------------------------------------ host side
@@ -594,6 +586,20 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
     return fn;
 }
 
+// A [rows][H][128] bf16 token array as a 3-D tensor (dk, head, row); boxes of
+// 64 dk x 1 head x 16 rows, 128-byte swizzle.  Rows past `rows` read as zero.
+bool encode_tokens(PFN_cuTensorMapEncodeTiled_v12000 encode, CUtensorMap *map, const void *base,
+                   int H, long long rows) {
+    const cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)H, (cuuint64_t)(rows > 0 ? rows : 1)};
+    const cuuint64_t strides[2] = {(cuuint64_t)D * 2, (cuuint64_t)H * D * 2};
+    const cuuint32_t box[3] = {64, 1, (cuuint32_t)CT};
+    const cuuint32_t elem[3] = {1, 1, 1};
+    return encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(base), dims, strides,
+                  box, elem, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 constexpr int kMaxDevices = 64;
 
 struct DeviceInfo {
@@ -605,7 +611,7 @@ DeviceInfo g_dev[kMaxDevices];
 std::mutex g_dev_mutex;
 
 template <int MODE>
-cudaError_t launch_mode(const Args &p, const CUtensorMap &map, cudaStream_t stream) {
+cudaError_t launch_mode(const Args &p, const Maps &maps, cudaStream_t stream) {
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
@@ -627,8 +633,9 @@ cudaError_t launch_mode(const Args &p, const CUtensorMap &map, cudaStream_t stre
         sms = info.sms;
     }
     const int units = p.B * p.H;
-    const int grid = units < sms ? units : sms;
-    chunk_kernel<MODE><<<grid, kThreads, kSmemBytes, stream>>>(p, map);
+    const int slots = kBlocksPerSM * sms;
+    const int grid = units < slots ? units : slots;
+    chunk_kernel<MODE><<<grid, kThreads, kSmemBytes, stream>>>(p, maps);
     return cudaGetLastError();
 }
 
@@ -641,24 +648,28 @@ bool chunk_supported(bool bf16, int dk, int dv, int max_T) {
 bool chunk_preferred(int max_T) { return max_T >= 1; }
 
 cudaError_t launch_chunk(const Args &p, int mode, cudaStream_t stream) {
-    // The pool as a 3-D tensor: value column (contiguous), key row, slot * H + head.
     const unsigned long long tiles = (unsigned long long)p.pool_slots * (unsigned long long)p.H;
-    if (tiles == 0 || tiles > (1ull << 31)) return cudaErrorInvalidValue;
+    if (tiles == 0 || tiles > (1ull << 31) || p.n_tok > (1ll << 31)) return cudaErrorInvalidValue;
     PFN_cuTensorMapEncodeTiled_v12000 encode = encode_fn();
     if (!encode) return cudaErrorNotSupported;
-    CUtensorMap map;
+    Maps maps;
+    // The pool as a 3-D tensor: value column (contiguous), key row, slot * H + head.
     const cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)D, (cuuint64_t)tiles};
     const cuuint64_t strides[2] = {(cuuint64_t)D * 4, (cuuint64_t)D * D * 4};
     const cuuint32_t box[3] = {32, (cuuint32_t)D, 1};
     const cuuint32_t elem[3] = {1, 1, 1};
-    if (encode(&map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, p.pool, dims, strides, box, elem,
+    if (encode(&maps.pool, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, p.pool, dims, strides, box, elem,
                CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
         return cudaErrorInvalidValue;
+    if (!encode_tokens(encode, &maps.k, p.k, p.H, p.n_tok) ||
+        !encode_tokens(encode, &maps.v, p.v, p.H, p.n_tok) ||
+        !encode_tokens(encode, &maps.q, p.q, p.H, p.n_tok))
+        return cudaErrorInvalidValue;
     switch (mode) {
-        case kVerify: return launch_mode<kVerify>(p, map, stream);
-        case kCommit: return launch_mode<kCommit>(p, map, stream);
-        default: return launch_mode<kFused>(p, map, stream);
+        case kVerify: return launch_mode<kVerify>(p, maps, stream);
+        case kCommit: return launch_mode<kCommit>(p, maps, stream);
+        default: return launch_mode<kFused>(p, maps, stream);
     }
 }
 
