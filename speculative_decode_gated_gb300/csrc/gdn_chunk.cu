@@ -12,9 +12,14 @@
 //   w_t = beta_t (v_t - gamma_t Z_t) - sum_{s<t} A[t][s] w_s,  A[t][s] = beta_t D[t][s] k_t.k_s
 //   o_t = gamma_t P_t + sum_{s<=t} M[t][s] w_s,              M[t][s] = D[t][s] q_t.k_s
 //   H_a = gamma_{a-1} H_0 + sum_{s<a} D[a-1][s] k_s w_s^T    (tensor cores)
+// In matrix form, with Tinv = (I + A)^-1 (lower triangular, rows t >= T_r zeroed)
+// and R = diag(beta) (V - diag(gamma) Z), both small solves are products:
+//   W^T = R^T Tinv^T,   O^T = P^T diag(gamma) + W^T M^T          (tensor cores)
 // Each value column j is independent given the token block, so warp w of a
 // 4-warp block owns the 32 columns [32w, 32w + 32) of the unit (request r,
-// head h).
+// head h); every product keeps the value columns as fragment rows, so the
+// accumulator of one product is the A operand of the next without any
+// shuffle or shared-memory transpose.
 //
 // Pipeline of one block (the block walks units blockIdx.x, + gridDim.x, ...):
 //   * thread 0 issues, for the next unit that has work, four 3-D TMA copies of
@@ -22,6 +27,8 @@
 //     block's single tile stage, and 16-token boxes of its k, q and v rows into
 //     the other of two token buffers, all with the 128-byte swizzle, as soon
 //     as the current unit has read the tile (right after the first product);
+//   * at the same time it asks TMA to pull the unit after that into L2, so the
+//     shared-memory loads issued one unit later hit in L2;
 //   * metadata is loaded two units ahead and the gates one unit ahead, so no
 //     thread ever waits on a load it has just issued.
 // Waits on the TMA mbarriers are bounded (about 2 s by %globaltimer); on expiry
@@ -55,8 +62,6 @@ namespace {
 
 constexpr int CT = 16;   // token block
 constexpr int D = 128;   // dk = dv
-constexpr int YS = 36;   // float row stride of the per-warp [column][P | Z] buffer
-constexpr int WS = 18;   // float row stride of the per-warp [column][scaled w] buffer
 constexpr int kThreads = 128;
 constexpr int kBlocksPerSM = 2;
 constexpr uint32_t kBoxBytes = 32 * D * 4;        // tile box: 32 value columns x 128 key rows
@@ -75,9 +80,9 @@ struct Aux {
     float gram[2][CT][CT];  // [0][t][s] = k_t.k_s, [1][t][s] = q_t.k_s
     float A[CT][CT];        // beta_t D[t][s] k_t.k_s for s < t < T, else 0
     float M[CT][CT];        // D[t][s] q_t.k_s for s <= t, else 0
+    float Tinv[CT][CT];     // (I + A)^-1, rows t >= T zeroed
     float alpha[CT], beta[CT], gamma[CT];
     float dcol[CT];         // D[a-1][s] for s < a, else 0
-    float y[4][32][YS];     // per warp; reused for the scaled w
     unsigned long long tile_full, tok_full[2];
     int abort_flag;
 };
@@ -148,6 +153,13 @@ __device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap *map
         : "memory");
 }
 
+__device__ __forceinline__ void tma_prefetch_3d(const CUtensorMap *map, int c0, int c1, int c2) {
+    asm volatile("cp.async.bulk.prefetch.tensor.3d.L2.global.tile [%0, {%1, %2, %3}];\n" ::"l"(
+                     reinterpret_cast<uint64_t>(map)),
+                 "r"(c0), "r"(c1), "r"(c2)
+                 : "memory");
+}
+
 // fp32 pair -> bf16x2 hi and lo with x = hi + lo + O(2^-17 |x|).
 __device__ __forceinline__ void split2(float x0, float x1, uint32_t &hi, uint32_t &lo) {
     const __nv_bfloat162 h = __floats2bfloat162_rn(x0, x1);
@@ -213,18 +225,11 @@ struct Maps {
     CUtensorMap pool, q, k, v;
 };
 
-// Thread 0: the tile and token boxes of one unit, onto the given mbarriers.
+// Thread 0: the token boxes (k, v and, unless committing, q) of one unit.
 template <int MODE>
-__device__ __forceinline__ void issue_unit(const Maps &maps, const Args &p, const UnitPlan &pl,
-                                           unsigned char *tile, TokBuf &tb, uint32_t tile_bar,
-                                           uint32_t tok_bar) {
-    const int slot_unit = (int)((pl.u.tile - p.pool) / (D * D));  // slot * H + h
-    mbar_arrive_expect_tx(tile_bar, kTileBytes);
-#pragma unroll
-    for (int b = 0; b < 4; ++b)
-        tma_load_3d(smem_u32(tile) + b * kBoxBytes, &maps.pool, 32 * b, 0, slot_unit, tile_bar);
-    const uint32_t tok_bytes = (MODE == kCommit ? 2u : 3u) * kTokBytes;
-    mbar_arrive_expect_tx(tok_bar, tok_bytes);
+__device__ __forceinline__ void issue_tokens(const Maps &maps, const UnitPlan &pl, TokBuf &tb,
+                                             uint32_t tok_bar) {
+    mbar_arrive_expect_tx(tok_bar, (MODE == kCommit ? 2u : 3u) * kTokBytes);
 #pragma unroll
     for (int hb = 0; hb < 2; ++hb) {
         tma_load_3d(smem_u32(tb.k) + hb * kTokHalfBytes, &maps.k, 64 * hb, pl.h, pl.u.row0, tok_bar);
@@ -233,6 +238,31 @@ __device__ __forceinline__ void issue_unit(const Maps &maps, const Args &p, cons
             tma_load_3d(smem_u32(tb.q) + hb * kTokHalfBytes, &maps.q, 64 * hb, pl.h, pl.u.row0,
                         tok_bar);
     }
+}
+
+// Thread 0: the four tile boxes of one unit.
+__device__ __forceinline__ void issue_tile(const Maps &maps, const Args &p, const UnitPlan &pl,
+                                           unsigned char *tile, uint32_t tile_bar) {
+    const int slot_unit = (int)((pl.u.tile - p.pool) / (D * D));  // slot * H + h
+    mbar_arrive_expect_tx(tile_bar, kTileBytes);
+#pragma unroll
+    for (int b = 0; b < 4; ++b)
+        tma_load_3d(smem_u32(tile) + b * kBoxBytes, &maps.pool, 32 * b, 0, slot_unit, tile_bar);
+}
+
+// Thread 0: pull the tile and token rows of a later unit into L2 (no shared
+// memory, no barrier), so its shared-memory loads, issued later, hit in L2.
+template <int MODE>
+__device__ __forceinline__ void prefetch_unit(const Maps &maps, const Args &p, const UnitPlan &pl) {
+    const int slot_unit = (int)((pl.u.tile - p.pool) / (D * D));
+#pragma unroll
+    for (int hb = 0; hb < 2; ++hb) {
+        tma_prefetch_3d(&maps.k, 64 * hb, pl.h, pl.u.row0);
+        tma_prefetch_3d(&maps.v, 64 * hb, pl.h, pl.u.row0);
+        if (MODE != kCommit) tma_prefetch_3d(&maps.q, 64 * hb, pl.h, pl.u.row0);
+    }
+#pragma unroll
+    for (int b = 0; b < 4; ++b) tma_prefetch_3d(&maps.pool, 32 * b, 0, slot_unit);
 }
 
 // ------------------------------------------------------------ the kernel
@@ -272,12 +302,21 @@ __global__ void __launch_bounds__(kThreads, kBlocksPerSM)
     if (unit + G < U) nxt = plan_unit<MODE>(p, unit + G, load_meta(p, (unit + G) / p.H, MODE));
     if (unit + 2 * G < U) raw = load_meta(p, (unit + 2 * G) / p.H, MODE);
 
-    int issued = 0;     // units whose loads were issued
+    // Unit k (in the order this block computes them) uses token buffer k & 1.
+    // Its token boxes go out when unit k-1 starts (that buffer was last used by
+    // unit k-2), its tile when unit k-1 has read the tile.
+    int issued = 0;     // units whose tile load was issued
+    int tok_issued = 0; // units whose token load was issued
     int processed = 0;  // units computed
     if (tid == 0 && !cur.skip) {
-        issue_unit<MODE>(maps, p, cur, sm.tile, sm.tok[0], tile_bar, smem_u32(&ax.tok_full[0]));
+        issue_tokens<MODE>(maps, cur, sm.tok[0], smem_u32(&ax.tok_full[0]));
+        issue_tile(maps, p, cur, sm.tile, tile_bar);
     }
-    if (!cur.skip) ++issued;
+    if (tid == 0 && !nxt.skip) prefetch_unit<MODE>(maps, p, nxt);
+    if (!cur.skip) {
+        ++issued;
+        ++tok_issued;
+    }
     // Gates of the current unit: thread t < 16 holds alpha_t, beta_t.
     float ga = 1.0f, gb = 0.0f;
     if (!cur.skip && tid < cur.teff) {
@@ -294,22 +333,26 @@ __global__ void __launch_bounds__(kThreads, kBlocksPerSM)
         nxt.skip = true;
         if (unit + 2 * G < U) nxt = plan_unit<MODE>(p, unit + 2 * G, raw);
         if (unit + 3 * G < U) raw = load_meta(p, (unit + 3 * G) / p.H, MODE);
-        // Gates of the next unit (consumed one iteration later).
-        float na = 1.0f, nb = 0.0f;
-        if (!cur.skip && tid < cur.teff) {
-            const size_t x = (size_t)(cur.u.row0 + tid) * p.H + cur.h;
-            na = p.alpha[x];
-            nb = p.beta[x];
-        }
         if (me.skip) {
-            ga = na;
-            gb = nb;
-            if (tid == 0 && !cur.skip && issued == processed) {
-                // Nothing is in the stage: the next unit's loads can go now.
-                issue_unit<MODE>(maps, p, cur, sm.tile, sm.tok[issued & 1], tile_bar,
-                                 smem_u32(&ax.tok_full[issued & 1]));
+            // Gates of the next unit (consumed one iteration later).
+            ga = 1.0f;
+            gb = 0.0f;
+            if (!cur.skip && tid < cur.teff) {
+                const size_t x = (size_t)(cur.u.row0 + tid) * p.H + cur.h;
+                ga = ld_early(p.alpha + x);
+                gb = ld_early(p.beta + x);
             }
-            if (!cur.skip && issued == processed) ++issued;
+            if (!cur.skip && issued == processed) {
+                // Nothing is in flight: the next unit's loads can all go now.
+                if (tid == 0) {
+                    issue_tokens<MODE>(maps, cur, sm.tok[tok_issued & 1],
+                                       smem_u32(&ax.tok_full[tok_issued & 1]));
+                    issue_tile(maps, p, cur, sm.tile, tile_bar);
+                }
+                ++issued;
+                ++tok_issued;
+            }
+            if (tid == 0 && !nxt.skip) prefetch_unit<MODE>(maps, p, nxt);
             continue;
         }
         const int T = me.teff;
@@ -319,12 +362,26 @@ __global__ void __launch_bounds__(kThreads, kBlocksPerSM)
 
         // 1. Gates into shared memory; token block arrival.
         __syncthreads();  // the previous unit is done with the small matrices
+        // The next unit's token block goes into the other buffer now.
+        if (!cur.skip && tok_issued == processed + 1) {
+            if (tid == 0)
+                issue_tokens<MODE>(maps, cur, sm.tok[tok_issued & 1],
+                                   smem_u32(&ax.tok_full[tok_issued & 1]));
+            ++tok_issued;
+        }
         if (tid < CT) {
             ax.alpha[tid] = ga;
             ax.beta[tid] = gb;
         }
-        ga = na;
-        gb = nb;
+        // Gates of the next unit, loaded straight into the registers just freed
+        // (consumed one iteration later, so this load is never waited on here).
+        ga = 1.0f;
+        gb = 0.0f;
+        if (!cur.skip && tid < cur.teff) {
+            const size_t x = (size_t)(cur.u.row0 + tid) * p.H + cur.h;
+            ga = ld_early(p.alpha + x);
+            gb = ld_early(p.beta + x);
+        }
         if (!wait_parity(smem_u32(&ax.tok_full[buf]), (processed >> 1) & 1)) ax.abort_flag = 1;
         __syncthreads();
         if (ax.abort_flag) {
@@ -354,18 +411,28 @@ __global__ void __launch_bounds__(kThreads, kBlocksPerSM)
         __syncthreads();
 
         // 3. Decay products and the triangular matrices, two (t, s) pairs per thread.
+        {
+            float al[CT];
 #pragma unroll
-        for (int e2 = 0; e2 < 2; ++e2) {
-            const int e = tid + 128 * e2;
-            const int t = e >> 4, s = e & 15;
-            float d = 1.0f;  // D[t][s] = prod_{s<r<=t} alpha_r
+            for (int r4 = 0; r4 < CT; r4 += 4) {
+                const float4 a4 = *reinterpret_cast<const float4 *>(&ax.alpha[r4]);
+                al[r4] = a4.x;
+                al[r4 + 1] = a4.y;
+                al[r4 + 2] = a4.z;
+                al[r4 + 3] = a4.w;
+            }
 #pragma unroll
-            for (int r = 1; r < CT; ++r)
-                if (r > s && r <= t) d *= ax.alpha[r];
-            ax.A[t][s] = (s < t && t < T) ? ax.beta[t] * d * ax.gram[0][t][s] : 0.0f;
-            ax.M[t][s] = (s <= t) ? d * ax.gram[1][t][s] : 0.0f;
-            if (s == 0) ax.gamma[t] = d * ax.alpha[0];
-            if (MODE != kVerify && t == me.u.a - 1) ax.dcol[s] = (s <= t) ? d : 0.0f;
+            for (int e2 = 0; e2 < 2; ++e2) {
+                const int e = tid + 128 * e2;
+                const int t = e >> 4, s = e & 15;
+                float d = 1.0f;  // D[t][s] = prod_{s<r<=t} alpha_r
+#pragma unroll
+                for (int r = 1; r < CT; ++r) d *= (r > s && r <= t) ? al[r] : 1.0f;
+                ax.A[t][s] = (s < t && t < T) ? ax.beta[t] * d * ax.gram[0][t][s] : 0.0f;
+                ax.M[t][s] = (s <= t) ? d * ax.gram[1][t][s] : 0.0f;
+                if (s == 0) ax.gamma[t] = d * al[0];
+                if (MODE != kVerify && t == me.u.a - 1) ax.dcol[s] = (s <= t) ? d : 0.0f;
+            }
         }
         __syncthreads();
 
@@ -382,6 +449,13 @@ __global__ void __launch_bounds__(kThreads, kBlocksPerSM)
         //    Q 8-15, K 0-7, K 8-15; commit needs only Z).  The tile is kept in
         //    registers when the commit needs it again.
         constexpr int NT0 = (MODE == kCommit) ? 2 : 0;
+        // Interleaved with the products (it only needs A, finished above):
+        // Tinv = (I + A)^-1 by forward substitution, rows 2kb and 2kb+1 in
+        // iteration kb.  Every lane computes column j = w + 4 (lane % 4); lanes
+        // 0..3 store it.  x_t = [t == j, t < T] - sum_{s<t} A[t][s] x_s gives
+        // zeros above the diagonal and in rows t >= T (A is zero there).
+        const int tj = warp + 4 * (lane & 3);
+        float xt[CT];
         float hr[8][4][4];
         float y[2][4][4];
 #pragma unroll
@@ -392,6 +466,20 @@ __global__ void __launch_bounds__(kThreads, kBlocksPerSM)
                 for (int e = 0; e < 4; ++e) y[m][nt][e] = 0.0f;
 #pragma unroll
         for (int kb = 0; kb < 8; ++kb) {
+#pragma unroll
+            for (int t = 2 * kb; t < 2 * kb + 2; ++t) {
+                float acc = (t == tj && t < T) ? 1.0f : 0.0f;
+#pragma unroll
+                for (int s4 = 0; s4 < t; s4 += 4) {
+                    const float4 a4 = *reinterpret_cast<const float4 *>(&ax.A[t][s4]);
+                    acc = fmaf(-a4.x, xt[s4], acc);
+                    if (s4 + 1 < t) acc = fmaf(-a4.y, xt[s4 + 1], acc);
+                    if (s4 + 2 < t) acc = fmaf(-a4.z, xt[s4 + 2], acc);
+                    if (s4 + 3 < t) acc = fmaf(-a4.w, xt[s4 + 3], acc);
+                }
+                xt[t] = acc;
+                if (lane < 4) ax.Tinv[t][tj] = acc;
+            }
 #pragma unroll
             for (int rr = 0; rr < 4; ++rr) {
                 const float4 x = ld_box(box, 16 * kb + 2 * c + (rr & 1) + 8 * (rr >> 1), g);
@@ -430,98 +518,106 @@ __global__ void __launch_bounds__(kThreads, kBlocksPerSM)
         // The tile stage is free: thread 0 sends the next unit's loads.
         __syncthreads();
         if (!cur.skip) {
-            if (tid == 0)
-                issue_unit<MODE>(maps, p, cur, sm.tile, sm.tok[issued & 1], tile_bar,
-                                 smem_u32(&ax.tok_full[issued & 1]));
+            if (tid == 0) issue_tile(maps, p, cur, sm.tile, tile_bar);
             ++issued;
         }
+        if (tid == 0 && !nxt.skip) prefetch_unit<MODE>(maps, p, nxt);
 
-        // 6. Fragments -> per-warp [column][P | Z] buffer -> lane j holds column 32w + j.
-        float(*yb)[YS] = ax.y[warp];
+        // Token indices of this thread in the fragments: n-tile half ntt, element e:
+        //   t = 8 ntt + 2c + (e & 1);   column = 32w + 4g + 2m + (e >> 1).
+        // 6. R^T = beta_t (v_t - gamma_t Z_t), zero for t >= T.
+        float rr_[2][2][4];
 #pragma unroll
         for (int m = 0; m < 2; ++m)
 #pragma unroll
-            for (int nt = NT0; nt < 4; ++nt) {
-                const int tk = 16 * (nt >> 1) + 8 * (nt & 1) + 2 * c;
-                *reinterpret_cast<float2 *>(&yb[4 * g + 2 * m][tk]) =
-                    make_float2(y[m][nt][0], y[m][nt][1]);
-                *reinterpret_cast<float2 *>(&yb[4 * g + 2 * m + 1][tk]) =
-                    make_float2(y[m][nt][2], y[m][nt][3]);
-            }
-        __syncwarp();
-        float pq[CT], z[CT];
+            for (int ntt = 0; ntt < 2; ++ntt)
 #pragma unroll
-        for (int t4 = 0; t4 < CT; t4 += 4) {
-            const float4 zz = *reinterpret_cast<const float4 *>(&yb[lane][16 + t4]);
-            z[t4] = zz.x;
-            z[t4 + 1] = zz.y;
-            z[t4 + 2] = zz.z;
-            z[t4 + 3] = zz.w;
-            if (MODE != kCommit) {
-                const float4 pp = *reinterpret_cast<const float4 *>(&yb[lane][t4]);
-                pq[t4] = pp.x;
-                pq[t4 + 1] = pp.y;
-                pq[t4 + 2] = pp.z;
-                pq[t4 + 3] = pp.w;
+                for (int eo = 0; eo < 2; ++eo) {
+                    const int t = 8 * ntt + 2 * c + eo;
+                    const int col = 32 * warp + 4 * g + 2 * m;
+                    const uint32_t vv = *reinterpret_cast<const uint32_t *>(tb.v + tok_off(t, col));
+                    const float v0 = __uint_as_float(vv << 16), v1 = __uint_as_float(vv & 0xFFFF0000u);
+                    const float bt = ax.beta[t], gt = ax.gamma[t];
+                    const bool live = t < T;
+                    rr_[m][ntt][eo] = live ? bt * (v0 - gt * y[m][2 + ntt][eo]) : 0.0f;
+                    rr_[m][ntt][2 + eo] = live ? bt * (v1 - gt * y[m][2 + ntt][2 + eo]) : 0.0f;
+                }
+
+        // 7. W^T = R^T Tinv^T: A = R^T (accumulator layout, split), B = Tinv^T (split).
+        float wq[2][2][4];
+        {
+            uint32_t bh[2][2], bl[2][2];
+#pragma unroll
+            for (int nt = 0; nt < 2; ++nt) {
+                const float *tr = ax.Tinv[8 * nt + g];
+                split2(tr[2 * c], tr[2 * c + 1], bh[nt][0], bl[nt][0]);
+                split2(tr[2 * c + 8], tr[2 * c + 9], bh[nt][1], bl[nt][1]);
+            }
+#pragma unroll
+            for (int m = 0; m < 2; ++m) {
+                uint32_t ah[4], al[4];
+                split2(rr_[m][0][0], rr_[m][0][1], ah[0], al[0]);
+                split2(rr_[m][0][2], rr_[m][0][3], ah[1], al[1]);
+                split2(rr_[m][1][0], rr_[m][1][1], ah[2], al[2]);
+                split2(rr_[m][1][2], rr_[m][1][3], ah[3], al[3]);
+#pragma unroll
+                for (int nt = 0; nt < 2; ++nt) {
+                    float *d = wq[m][nt];
+                    d[0] = d[1] = d[2] = d[3] = 0.0f;
+                    mma(d[0], d[1], d[2], d[3], ah[0], ah[1], ah[2], ah[3], bh[nt][0], bh[nt][1]);
+                    mma(d[0], d[1], d[2], d[3], ah[0], ah[1], ah[2], ah[3], bl[nt][0], bl[nt][1]);
+                    mma(d[0], d[1], d[2], d[3], al[0], al[1], al[2], al[3], bh[nt][0], bh[nt][1]);
+                }
             }
         }
 
-        // 7. Forward substitution for w (fp32), one column per lane; w_t = 0 past T.
-        float w[CT];
-#pragma unroll
-        for (int t = 0; t < CT; ++t) {
-            const uint32_t vb = *reinterpret_cast<const unsigned short *>(
-                tb.v + tok_off(t, 32 * warp + lane));
-            float acc = ax.beta[t] * (__uint_as_float(vb << 16) - ax.gamma[t] * z[t]);
-#pragma unroll
-            for (int s4 = 0; s4 < t; s4 += 4) {
-                const float4 a4 = *reinterpret_cast<const float4 *>(&ax.A[t][s4]);
-                acc = fmaf(-a4.x, w[s4], acc);
-                if (s4 + 1 < t) acc = fmaf(-a4.y, w[s4 + 1], acc);
-                if (s4 + 2 < t) acc = fmaf(-a4.z, w[s4 + 2], acc);
-                if (s4 + 3 < t) acc = fmaf(-a4.w, w[s4 + 3], acc);
-            }
-            w[t] = t < T ? acc : 0.0f;
-        }
-
-        // 8. Outputs o_t for t < T_r.
+        // 8. O^T = P^T diag(gamma) + W^T M^T, stored as float2 pairs of adjacent columns.
         if (MODE != kCommit) {
-            float *go = p.o + ((size_t)me.u.row0 * p.H + me.h) * D + 32 * warp + lane;
+            uint32_t bh[2][2], bl[2][2];
 #pragma unroll
-            for (int t = 0; t < CT; ++t) {
-                if (t < T) {
-                    float acc = ax.gamma[t] * pq[t];
+            for (int nt = 0; nt < 2; ++nt) {
+                const float *mr = ax.M[8 * nt + g];
+                split2(mr[2 * c], mr[2 * c + 1], bh[nt][0], bl[nt][0]);
+                split2(mr[2 * c + 8], mr[2 * c + 9], bh[nt][1], bl[nt][1]);
+            }
+            float *go = p.o + ((size_t)me.u.row0 * p.H + me.h) * D + 32 * warp + 4 * g;
 #pragma unroll
-                    for (int s4 = 0; s4 <= t; s4 += 4) {
-                        const float4 m4 = *reinterpret_cast<const float4 *>(&ax.M[t][s4]);
-                        acc = fmaf(m4.x, w[s4], acc);
-                        if (s4 + 1 <= t) acc = fmaf(m4.y, w[s4 + 1], acc);
-                        if (s4 + 2 <= t) acc = fmaf(m4.z, w[s4 + 2], acc);
-                        if (s4 + 3 <= t) acc = fmaf(m4.w, w[s4 + 3], acc);
-                    }
-                    go[t * row_stride] = acc;
+            for (int m = 0; m < 2; ++m) {
+                uint32_t ah[4], al[4];
+                split2(wq[m][0][0], wq[m][0][1], ah[0], al[0]);
+                split2(wq[m][0][2], wq[m][0][3], ah[1], al[1]);
+                split2(wq[m][1][0], wq[m][1][1], ah[2], al[2]);
+                split2(wq[m][1][2], wq[m][1][3], ah[3], al[3]);
+#pragma unroll
+                for (int nt = 0; nt < 2; ++nt) {
+                    const int t0 = 8 * nt + 2 * c;
+                    const float g0 = ax.gamma[t0], g1 = ax.gamma[t0 + 1];
+                    float d[4] = {g0 * y[m][nt][0], g1 * y[m][nt][1], g0 * y[m][nt][2],
+                                  g1 * y[m][nt][3]};
+                    mma(d[0], d[1], d[2], d[3], ah[0], ah[1], ah[2], ah[3], bh[nt][0], bh[nt][1]);
+                    mma(d[0], d[1], d[2], d[3], ah[0], ah[1], ah[2], ah[3], bl[nt][0], bl[nt][1]);
+                    mma(d[0], d[1], d[2], d[3], al[0], al[1], al[2], al[3], bh[nt][0], bh[nt][1]);
+                    if (t0 < T)
+                        *reinterpret_cast<float2 *>(go + t0 * row_stride + 2 * m) = make_float2(d[0], d[2]);
+                    if (t0 + 1 < T)
+                        *reinterpret_cast<float2 *>(go + (t0 + 1) * row_stride + 2 * m) =
+                            make_float2(d[1], d[3]);
                 }
             }
         }
 
         // 9. Commit: H_a^T = gamma_{a-1} H_0^T + (D[a-1][.] w)^T K, accumulated in hr.
         if (write_state) {
-            __syncwarp();  // yb is reused
-            float(*wb)[WS] = reinterpret_cast<float(*)[WS]>(&ax.y[warp][0][0]);
-#pragma unroll
-            for (int s = 0; s < CT; s += 2)
-                *reinterpret_cast<float2 *>(&wb[lane][s]) =
-                    make_float2(ax.dcol[s] * w[s], ax.dcol[s + 1] * w[s + 1]);
-            __syncwarp();
             uint32_t ah[2][4], al[2][4];
 #pragma unroll
-            for (int m = 0; m < 2; ++m) {
-                const float *r0 = wb[4 * g + 2 * m];
-                const float *r1 = wb[4 * g + 2 * m + 1];
-                split2(r0[2 * c], r0[2 * c + 1], ah[m][0], al[m][0]);
-                split2(r1[2 * c], r1[2 * c + 1], ah[m][1], al[m][1]);
-                split2(r0[2 * c + 8], r0[2 * c + 9], ah[m][2], al[m][2]);
-                split2(r1[2 * c + 8], r1[2 * c + 9], ah[m][3], al[m][3]);
+            for (int ntt = 0; ntt < 2; ++ntt) {
+                const float d0 = ax.dcol[8 * ntt + 2 * c], d1 = ax.dcol[8 * ntt + 2 * c + 1];
+#pragma unroll
+                for (int m = 0; m < 2; ++m) {
+                    split2(d0 * wq[m][ntt][0], d1 * wq[m][ntt][1], ah[m][2 * ntt], al[m][2 * ntt]);
+                    split2(d0 * wq[m][ntt][2], d1 * wq[m][ntt][3], ah[m][2 * ntt + 1],
+                           al[m][2 * ntt + 1]);
+                }
             }
             const float gam = ax.gamma[me.u.a - 1];
             // ldmatrix.trans row address of this lane: matrix lane/8 -> (token half, dk half).
@@ -562,9 +658,11 @@ __global__ void __launch_bounds__(kThreads, kBlocksPerSM)
     }
 
     // Copies still in flight must land before the block exits.
-    if (tid == 0 && issued > processed) {
-        bool ok = wait_parity(tile_bar, processed & 1);
-        ok = wait_parity(smem_u32(&ax.tok_full[processed & 1]), (processed >> 1) & 1) && ok;
+    if (tid == 0) {
+        bool ok = true;
+        if (issued > processed) ok = wait_parity(tile_bar, processed & 1) && ok;
+        for (int k = processed; k < tok_issued; ++k)
+            ok = wait_parity(smem_u32(&ax.tok_full[k & 1]), (k >> 1) & 1) && ok;
         if (!ok) aborted = true;
     }
     if (tid == 0 && aborted && p.dev_err) atomicOr(p.dev_err, GDN_DEVERR_TIMEOUT);

@@ -45,17 +45,31 @@ struct RawMeta {
     int acc;       // accepted length, -1 in verify
 };
 
+// Read-only loads that stay where they are written: issued early on purpose,
+// their first use is an iteration later (the optimiser would otherwise sink
+// them next to the use and expose their latency).
+__device__ __forceinline__ int ld_early(const int32_t *ptr) {
+    int v;
+    asm volatile("ld.global.nc.b32 %0, [%1];" : "=r"(v) : "l"(ptr));
+    return v;
+}
+__device__ __forceinline__ float ld_early(const float *ptr) {
+    float v;
+    asm volatile("ld.global.nc.f32 %0, [%1];" : "=f"(v) : "l"(ptr));
+    return v;
+}
+
 __device__ __forceinline__ RawMeta load_meta(const Args &p, int r, int mode) {
     RawMeta m;
     if (p.cu_seqlens) {
-        m.cu0 = p.cu_seqlens[r];
-        m.cu1 = p.cu_seqlens[r + 1];
+        m.cu0 = ld_early(p.cu_seqlens + r);
+        m.cu1 = ld_early(p.cu_seqlens + r + 1);
     } else {
         m.cu0 = r * p.max_T;
         m.cu1 = m.cu0 + p.max_T;
     }
-    m.slot = p.slot_ids[r];
-    m.acc = mode != kVerify ? p.accepted[r] : -1;
+    m.slot = ld_early(p.slot_ids + r);
+    m.acc = mode != kVerify ? ld_early(p.accepted + r) : -1;
     return m;
 }
 
