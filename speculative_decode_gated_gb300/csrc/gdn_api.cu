@@ -48,7 +48,9 @@ bool shape_ok(const gdn_problem *p) {
 // Which kernel AUTO picks.  The chunked tensor-core kernel covers bf16 q/k/v at
 // dk = dv = 128 with up to 16 tokens per request; the recurrent kernel the rest.
 int resolve_algo(const gdn_problem *p) {
-    const bool chunk_ok = gdn::chunk_supported(p->qkv_dtype == GDN_BF16, p->dk, p->dv, p->max_T);
+    // The chunked kernel also needs at least one token row (ragged input may have none).
+    const bool chunk_ok = gdn::chunk_supported(p->qkv_dtype == GDN_BF16, p->dk, p->dv, p->max_T) &&
+                          (!p->cu_seqlens || p->n_tok >= 1);
     if (p->algo == GDN_ALGO_RECURRENT) return GDN_ALGO_RECURRENT;
     if (p->algo == GDN_ALGO_CHUNK) return chunk_ok ? GDN_ALGO_CHUNK : -1;
     return (chunk_ok && gdn::chunk_preferred(p->max_T)) ? GDN_ALGO_CHUNK : GDN_ALGO_RECURRENT;

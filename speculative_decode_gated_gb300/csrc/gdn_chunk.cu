@@ -62,7 +62,6 @@ namespace {
 
 constexpr int CT = 16;   // token block
 constexpr int D = 128;   // dk = dv
-constexpr int kThreads = 128;
 constexpr int kBlocksPerSM = 2;
 constexpr uint32_t kBoxBytes = 32 * D * 4;        // tile box: 32 value columns x 128 key rows
 constexpr uint32_t kTileBytes = 4 * kBoxBytes;    // 64 KiB
@@ -77,7 +76,7 @@ struct TokBuf {  // 1024-byte aligned: three swizzled [16][128] bf16 tiles
 };
 
 struct Aux {
-    float gram[2][CT][CT];  // [0][t][s] = k_t.k_s, [1][t][s] = q_t.k_s
+    float gram[2][2][CT][CT];  // [part][0][t][s] = k_t.k_s, [part][1][t][s] = q_t.k_s (partial sums)
     float A[CT][CT];        // beta_t D[t][s] k_t.k_s for s < t < T, else 0
     float M[CT][CT];        // D[t][s] q_t.k_s for s <= t, else 0
     float Tinv[CT][CT];     // (I + A)^-1, rows t >= T zeroed
@@ -186,11 +185,6 @@ __device__ __forceinline__ void ldsm_x4_trans(uint32_t &r0, uint32_t &r1, uint32
                  : "r"(addr));
 }
 
-// Row `row`, 16-byte chunk `chunk` of a 128-byte-swizzled tile box (32 floats per row).
-__device__ __forceinline__ float4 ld_box(const unsigned char *box, int row, int chunk) {
-    return *reinterpret_cast<const float4 *>(box + row * 128 + ((chunk ^ (row & 7)) << 4));
-}
-
 // Byte offset of bf16 element (t, i) in a swizzled [16][128] token tile
 // (two boxes of 64 columns, 128 bytes per token row).
 __device__ __forceinline__ uint32_t tok_off(int t, int i) {
@@ -205,11 +199,30 @@ __device__ __forceinline__ uint32_t ld_tok32(const unsigned char *tile, int t, i
 // ------------------------------------------------------------ per-unit plan
 
 struct UnitPlan {
-    Unit u;
-    int h;
-    int teff;  // tokens that matter: T_r, or a_r for commit
-    bool skip;
+    Unit u = {0, 0, -1, nullptr};
+    int h = 0;
+    int teff = 0;  // tokens that matter: T_r, or a_r for commit
+    bool skip = true;
 };
+
+// Metadata of `unit`, loaded unconditionally (the unit index is clamped to a
+// valid one) so that no select or branch ever waits on these loads: they are
+// consumed an iteration later, when the plan decides whether the unit exists.
+template <int MODE, bool RAGGED>
+__device__ __forceinline__ RawMeta load_unit_meta(const Args &p, int unit, int U) {
+    const int r = (unit < U ? unit : U - 1) / p.H;
+    RawMeta m;
+    if (RAGGED) {
+        m.cu0 = ld_early(p.cu_seqlens + r);
+        m.cu1 = ld_early(p.cu_seqlens + r + 1);
+    } else {
+        m.cu0 = r * p.max_T;
+        m.cu1 = m.cu0 + p.max_T;
+    }
+    m.slot = ld_early(p.slot_ids + r);
+    m.acc = MODE != kVerify ? ld_early(p.accepted + r) : -1;
+    return m;
+}
 
 template <int MODE>
 __device__ __forceinline__ UnitPlan plan_unit(const Args &p, int unit, const RawMeta &m) {
@@ -265,11 +278,59 @@ __device__ __forceinline__ void prefetch_unit(const Maps &maps, const Args &p, c
     for (int b = 0; b < 4; ++b) tma_prefetch_3d(&maps.pool, 32 * b, 0, slot_unit);
 }
 
+// Gate of token min(tid, T - 1) of a unit (any clamped row when the unit is
+// skipped or tid >= T): always a valid address (the chunk kernel runs only
+// with n_tok >= 1), so the load never sits behind a branch.
+__device__ __forceinline__ float gate_load(const float *gate, const Args &p, const UnitPlan &pl,
+                                           int tid) {
+    long long row = (long long)pl.u.row0 + (tid < pl.teff ? tid : pl.teff - 1);
+    row = row < 0 ? 0 : (row >= p.n_tok ? p.n_tok - 1 : row);
+    const int h = pl.h < 0 ? 0 : (pl.h >= p.H ? p.H - 1 : pl.h);
+    return ld_early(gate + (size_t)row * p.H + h);
+}
+
 // ------------------------------------------------------------ the kernel
 
-template <int MODE>
-__global__ void __launch_bounds__(kThreads, kBlocksPerSM)
+// NW warps per block share one unit: warp w owns CW = 128 / NW value columns,
+// MT = CW / 16 m-tiles of 16 columns; lane (g, c) holds CPT = 2 MT adjacent
+// columns CPT g + {0..CPT-1} of the warp's slice (m-tile m: fragment row g is
+// column CPT g + 2m, row g + 8 is CPT g + 2m + 1).
+template <int NW>
+struct Cfg {
+    static constexpr int kThreads = 32 * NW;
+    static constexpr int CW = D / NW;
+    static constexpr int MT = CW / 16;
+    static constexpr int CPT = 2 * MT;
+    static constexpr int kTinvLanes = CT / NW;  // Tinv columns per warp
+};
+
+// Columns CPT g + [0, CPT) of warp w's slice, row `row`, from the swizzled tile.
+template <int NW>
+__device__ __forceinline__ void ld_tile_row(const unsigned char *tile, int warp, int g, int row,
+                                            float *out) {
+    using C = Cfg<NW>;
+    const int col = warp * C::CW + C::CPT * g;  // first column, 0..127
+    const unsigned char *box = tile + (col >> 5) * kBoxBytes;
+    const int chunk = (col & 31) >> 2;
+    const unsigned char *ptr = box + row * 128 + ((chunk ^ (row & 7)) << 4) + (col & 3) * 4;
+    if (C::CPT == 4) {
+        const float4 x = *reinterpret_cast<const float4 *>(ptr);
+        out[0] = x.x;
+        out[1] = x.y;
+        out[2] = x.z;
+        out[3] = x.w;
+    } else {
+        const float2 x = *reinterpret_cast<const float2 *>(ptr);
+        out[0] = x.x;
+        out[1] = x.y;
+    }
+}
+
+template <int MODE, int NW, bool RAGGED>
+__global__ void __launch_bounds__(32 * NW, kBlocksPerSM)
     chunk_kernel(const Args p, const __grid_constant__ Maps maps) {
+    using C = Cfg<NW>;
+    constexpr int MT = C::MT, CPT = C::CPT, NTH = C::kThreads;
     extern __shared__ unsigned char smem_raw[];
     const uint32_t raw_addr = smem_u32(smem_raw);
     Smem &sm = *reinterpret_cast<Smem *>(smem_raw + ((1024u - (raw_addr & 1023u)) & 1023u));
@@ -281,6 +342,7 @@ __global__ void __launch_bounds__(kThreads, kBlocksPerSM)
     const int G = gridDim.x;
     const size_t row_stride = (size_t)p.H * D;
     const uint32_t tile_bar = smem_u32(&ax.tile_full);
+    const int col0 = warp * C::CW + CPT * g;  // this thread's first value column
 
     if (tid == 0) {
         mbar_init(tile_bar, 1);
@@ -298,16 +360,16 @@ __global__ void __launch_bounds__(kThreads, kBlocksPerSM)
     RawMeta raw;
     cur.skip = true;
     nxt.skip = true;
-    if (unit < U) cur = plan_unit<MODE>(p, unit, load_meta(p, unit / p.H, MODE));
-    if (unit + G < U) nxt = plan_unit<MODE>(p, unit + G, load_meta(p, (unit + G) / p.H, MODE));
-    if (unit + 2 * G < U) raw = load_meta(p, (unit + 2 * G) / p.H, MODE);
+    if (unit < U) cur = plan_unit<MODE>(p, unit, load_unit_meta<MODE, RAGGED>(p, unit, U));
+    if (unit + G < U) nxt = plan_unit<MODE>(p, unit + G, load_unit_meta<MODE, RAGGED>(p, unit + G, U));
+    raw = load_unit_meta<MODE, RAGGED>(p, unit + 2 * G, U);
 
     // Unit k (in the order this block computes them) uses token buffer k & 1.
     // Its token boxes go out when unit k-1 starts (that buffer was last used by
-    // unit k-2), its tile when unit k-1 has read the tile.
-    int issued = 0;     // units whose tile load was issued
-    int tok_issued = 0; // units whose token load was issued
-    int processed = 0;  // units computed
+    // unit k-2), its tile when unit k-1 is done with the tile stage.
+    int issued = 0;      // units whose tile load was issued
+    int tok_issued = 0;  // units whose token load was issued
+    int processed = 0;   // units computed
     if (tid == 0 && !cur.skip) {
         issue_tokens<MODE>(maps, cur, sm.tok[0], smem_u32(&ax.tok_full[0]));
         issue_tile(maps, p, cur, sm.tile, tile_bar);
@@ -317,13 +379,10 @@ __global__ void __launch_bounds__(kThreads, kBlocksPerSM)
         ++issued;
         ++tok_issued;
     }
-    // Gates of the current unit: thread t < 16 holds alpha_t, beta_t.
-    float ga = 1.0f, gb = 0.0f;
-    if (!cur.skip && tid < cur.teff) {
-        const size_t x = (size_t)(cur.u.row0 + tid) * p.H + cur.h;
-        ga = p.alpha[x];
-        gb = p.beta[x];
-    }
+    // Gates of the current unit: thread t < 16 holds alpha_t, beta_t, loaded
+    // unconditionally from a clamped (always valid) row; rows t >= T are
+    // replaced by alpha = 1, beta = 0 where the values are used.
+    float ga = gate_load(p.alpha, p, cur, tid), gb = gate_load(p.beta, p, cur, tid);
 
     bool aborted = false;
     for (; unit < U; unit += G) {
@@ -332,16 +391,11 @@ __global__ void __launch_bounds__(kThreads, kBlocksPerSM)
         cur = nxt;
         nxt.skip = true;
         if (unit + 2 * G < U) nxt = plan_unit<MODE>(p, unit + 2 * G, raw);
-        if (unit + 3 * G < U) raw = load_meta(p, (unit + 3 * G) / p.H, MODE);
+        raw = load_unit_meta<MODE, RAGGED>(p, unit + 3 * G, U);
         if (me.skip) {
             // Gates of the next unit (consumed one iteration later).
-            ga = 1.0f;
-            gb = 0.0f;
-            if (!cur.skip && tid < cur.teff) {
-                const size_t x = (size_t)(cur.u.row0 + tid) * p.H + cur.h;
-                ga = ld_early(p.alpha + x);
-                gb = ld_early(p.beta + x);
-            }
+            ga = gate_load(p.alpha, p, cur, tid);
+            gb = gate_load(p.beta, p, cur, tid);
             if (!cur.skip && issued == processed) {
                 // Nothing is in flight: the next unit's loads can all go now.
                 if (tid == 0) {
@@ -359,6 +413,11 @@ __global__ void __launch_bounds__(kThreads, kBlocksPerSM)
         const int buf = processed & 1;
         const TokBuf &tb = sm.tok[buf];
         const bool write_state = MODE != kVerify && me.u.a > 0;
+        // With 4 warps the tile also stays in registers for the commit (so the
+        // stage is free right after the first product); with 8 warps (half the
+        // registers) the commit re-reads it and the stage is held until then.
+        constexpr bool kRegTile = NW == 4;
+        const bool keep_tile = write_state && !kRegTile;
 
         // 1. Gates into shared memory; token block arrival.
         __syncthreads();  // the previous unit is done with the small matrices
@@ -370,18 +429,13 @@ __global__ void __launch_bounds__(kThreads, kBlocksPerSM)
             ++tok_issued;
         }
         if (tid < CT) {
-            ax.alpha[tid] = ga;
-            ax.beta[tid] = gb;
+            ax.alpha[tid] = tid < T ? ga : 1.0f;
+            ax.beta[tid] = tid < T ? gb : 0.0f;
         }
         // Gates of the next unit, loaded straight into the registers just freed
         // (consumed one iteration later, so this load is never waited on here).
-        ga = 1.0f;
-        gb = 0.0f;
-        if (!cur.skip && tid < cur.teff) {
-            const size_t x = (size_t)(cur.u.row0 + tid) * p.H + cur.h;
-            ga = ld_early(p.alpha + x);
-            gb = ld_early(p.beta + x);
-        }
+        ga = gate_load(p.alpha, p, cur, tid);
+        gb = gate_load(p.beta, p, cur, tid);
         if (!wait_parity(smem_u32(&ax.tok_full[buf]), (processed >> 1) & 1)) ax.abort_flag = 1;
         __syncthreads();
         if (ax.abort_flag) {
@@ -389,20 +443,24 @@ __global__ void __launch_bounds__(kThreads, kBlocksPerSM)
             break;
         }
 
-        // 2. Gram blocks k_t.k_s and q_t.k_s: warp w computes matrix w/2, columns 8 (w%2) + [0, 8).
+        // 2. Gram blocks k_t.k_s and q_t.k_s: block (matrix (w/2)%2, columns 8 (w%2) + [0, 8)),
+        //    k-steps split over NW/4 warps into partial sums.
         {
-            const unsigned char *At = (warp >> 1) ? tb.q : tb.k;
-            const int nt = warp & 1;
+            const int blk = warp & 3, part = warp >> 2;
+            constexpr int KPW = 8 / (NW / 4);  // k-steps per warp
+            const unsigned char *At = (blk >> 1) ? tb.q : tb.k;
+            const int nt = blk & 1;
             float a0[4] = {0.f, 0.f, 0.f, 0.f}, a1[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-            for (int kb = 0; kb < 8; ++kb) {
+            for (int kk = 0; kk < KPW; ++kk) {
+                const int kb = part * KPW + kk;
                 const int col = 16 * kb + 2 * c;
-                float *acc = (kb & 1) ? a1 : a0;
+                float *acc = (kk & 1) ? a1 : a0;
                 mma(acc[0], acc[1], acc[2], acc[3], ld_tok32(At, g, col), ld_tok32(At, g + 8, col),
                     ld_tok32(At, g, col + 8), ld_tok32(At, g + 8, col + 8),
                     ld_tok32(tb.k, 8 * nt + g, col), ld_tok32(tb.k, 8 * nt + g, col + 8));
             }
-            float(*Gm)[CT] = ax.gram[warp >> 1];
+            float(*Gm)[CT] = ax.gram[part][blk >> 1];
             Gm[g][8 * nt + 2 * c] = a0[0] + a1[0];
             Gm[g][8 * nt + 2 * c + 1] = a0[1] + a1[1];
             Gm[g + 8][8 * nt + 2 * c] = a0[2] + a1[2];
@@ -410,7 +468,7 @@ __global__ void __launch_bounds__(kThreads, kBlocksPerSM)
         }
         __syncthreads();
 
-        // 3. Decay products and the triangular matrices, two (t, s) pairs per thread.
+        // 3. Decay products and the triangular matrices, 256 / NTH (t, s) pairs per thread.
         {
             float al[CT];
 #pragma unroll
@@ -422,14 +480,19 @@ __global__ void __launch_bounds__(kThreads, kBlocksPerSM)
                 al[r4 + 3] = a4.w;
             }
 #pragma unroll
-            for (int e2 = 0; e2 < 2; ++e2) {
-                const int e = tid + 128 * e2;
+            for (int e2 = 0; e2 < CT * CT / NTH; ++e2) {
+                const int e = tid + NTH * e2;
                 const int t = e >> 4, s = e & 15;
                 float d = 1.0f;  // D[t][s] = prod_{s<r<=t} alpha_r
 #pragma unroll
                 for (int r = 1; r < CT; ++r) d *= (r > s && r <= t) ? al[r] : 1.0f;
-                ax.A[t][s] = (s < t && t < T) ? ax.beta[t] * d * ax.gram[0][t][s] : 0.0f;
-                ax.M[t][s] = (s <= t) ? d * ax.gram[1][t][s] : 0.0f;
+                float kk = ax.gram[0][0][t][s], qk = ax.gram[0][1][t][s];
+                if (NW == 8) {
+                    kk += ax.gram[1][0][t][s];
+                    qk += ax.gram[1][1][t][s];
+                }
+                ax.A[t][s] = (s < t && t < T) ? ax.beta[t] * d * kk : 0.0f;
+                ax.M[t][s] = (s <= t) ? d * qk : 0.0f;
                 if (s == 0) ax.gamma[t] = d * al[0];
                 if (MODE != kVerify && t == me.u.a - 1) ax.dcol[s] = (s <= t) ? d : 0.0f;
             }
@@ -443,23 +506,21 @@ __global__ void __launch_bounds__(kThreads, kBlocksPerSM)
             aborted = true;
             break;
         }
-        const unsigned char *box = sm.tile + warp * kBoxBytes;
 
-        // 5. P = H_0^T Q^T and Z = H_0^T K^T for this warp's 32 columns (N-tiles: Q 0-7,
-        //    Q 8-15, K 0-7, K 8-15; commit needs only Z).  The tile is kept in
-        //    registers when the commit needs it again.
+        // 5. P = H_0^T Q^T and Z = H_0^T K^T for this warp's columns (N-tiles: Q 0-7,
+        //    Q 8-15, K 0-7, K 8-15; commit needs only Z).
         constexpr int NT0 = (MODE == kCommit) ? 2 : 0;
         // Interleaved with the products (it only needs A, finished above):
         // Tinv = (I + A)^-1 by forward substitution, rows 2kb and 2kb+1 in
-        // iteration kb.  Every lane computes column j = w + 4 (lane % 4); lanes
-        // 0..3 store it.  x_t = [t == j, t < T] - sum_{s<t} A[t][s] x_s gives
-        // zeros above the diagonal and in rows t >= T (A is zero there).
-        const int tj = warp + 4 * (lane & 3);
+        // iteration kb.  Lane groups compute column j = w + NW (lane % (16/NW));
+        // the first 16/NW lanes store it.  x_t = [t == j, t < T] - sum_{s<t} A[t][s] x_s
+        // gives zeros above the diagonal and in rows t >= T (A is zero there).
+        const int tj = warp + NW * (lane % C::kTinvLanes);
         float xt[CT];
-        float hr[8][4][4];
-        float y[2][4][4];
+        float hr[kRegTile ? 8 : 1][4][CPT];  // the tile in registers (4-warp layout)
+        float y[MT][4][4];
 #pragma unroll
-        for (int m = 0; m < 2; ++m)
+        for (int m = 0; m < MT; ++m)
 #pragma unroll
             for (int nt = 0; nt < 4; ++nt)
 #pragma unroll
@@ -478,15 +539,15 @@ __global__ void __launch_bounds__(kThreads, kBlocksPerSM)
                     if (s4 + 3 < t) acc = fmaf(-a4.w, xt[s4 + 3], acc);
                 }
                 xt[t] = acc;
-                if (lane < 4) ax.Tinv[t][tj] = acc;
+                if (lane < C::kTinvLanes) ax.Tinv[t][tj] = acc;
             }
+            float hv[4][CPT];
 #pragma unroll
             for (int rr = 0; rr < 4; ++rr) {
-                const float4 x = ld_box(box, 16 * kb + 2 * c + (rr & 1) + 8 * (rr >> 1), g);
-                hr[kb][rr][0] = x.x;
-                hr[kb][rr][1] = x.y;
-                hr[kb][rr][2] = x.z;
-                hr[kb][rr][3] = x.w;
+                ld_tile_row<NW>(sm.tile, warp, g, 16 * kb + 2 * c + (rr & 1) + 8 * (rr >> 1), hv[rr]);
+                if (kRegTile && MODE != kVerify)
+#pragma unroll
+                    for (int e = 0; e < CPT; ++e) hr[kRegTile ? kb : 0][rr][e] = hv[rr][e];
             }
             uint32_t b[4][2];
 #pragma unroll
@@ -497,12 +558,12 @@ __global__ void __launch_bounds__(kThreads, kBlocksPerSM)
                 b[nt][1] = ld_tok32(Bt, tok, 16 * kb + 2 * c + 8);
             }
 #pragma unroll
-            for (int m = 0; m < 2; ++m) {
+            for (int m = 0; m < MT; ++m) {
                 uint32_t ah[4], al[4];
-                split2(hr[kb][0][2 * m], hr[kb][1][2 * m], ah[0], al[0]);
-                split2(hr[kb][0][2 * m + 1], hr[kb][1][2 * m + 1], ah[1], al[1]);
-                split2(hr[kb][2][2 * m], hr[kb][3][2 * m], ah[2], al[2]);
-                split2(hr[kb][2][2 * m + 1], hr[kb][3][2 * m + 1], ah[3], al[3]);
+                split2(hv[0][2 * m], hv[1][2 * m], ah[0], al[0]);
+                split2(hv[0][2 * m + 1], hv[1][2 * m + 1], ah[1], al[1]);
+                split2(hv[2][2 * m], hv[3][2 * m], ah[2], al[2]);
+                split2(hv[2][2 * m + 1], hv[3][2 * m + 1], ah[3], al[3]);
 #pragma unroll
                 for (int nt = NT0; nt < 4; ++nt)
                     mma(y[m][nt][0], y[m][nt][1], y[m][nt][2], y[m][nt][3], ah[0], ah[1], ah[2],
@@ -515,27 +576,27 @@ __global__ void __launch_bounds__(kThreads, kBlocksPerSM)
         }
         ++processed;
 
-        // The tile stage is free: thread 0 sends the next unit's loads.
+        // Tinv is complete; when the tile is not needed again, the stage is free
+        // and thread 0 sends the next unit's tile.
         __syncthreads();
-        if (!cur.skip) {
+        if (!keep_tile && !cur.skip) {
             if (tid == 0) issue_tile(maps, p, cur, sm.tile, tile_bar);
             ++issued;
         }
         if (tid == 0 && !nxt.skip) prefetch_unit<MODE>(maps, p, nxt);
 
         // Token indices of this thread in the fragments: n-tile half ntt, element e:
-        //   t = 8 ntt + 2c + (e & 1);   column = 32w + 4g + 2m + (e >> 1).
+        //   t = 8 ntt + 2c + (e & 1);   column = col0 + 2m + (e >> 1).
         // 6. R^T = beta_t (v_t - gamma_t Z_t), zero for t >= T.
-        float rr_[2][2][4];
+        float rr_[MT][2][4];
 #pragma unroll
-        for (int m = 0; m < 2; ++m)
+        for (int m = 0; m < MT; ++m)
 #pragma unroll
             for (int ntt = 0; ntt < 2; ++ntt)
 #pragma unroll
                 for (int eo = 0; eo < 2; ++eo) {
                     const int t = 8 * ntt + 2 * c + eo;
-                    const int col = 32 * warp + 4 * g + 2 * m;
-                    const uint32_t vv = *reinterpret_cast<const uint32_t *>(tb.v + tok_off(t, col));
+                    const uint32_t vv = *reinterpret_cast<const uint32_t *>(tb.v + tok_off(t, col0 + 2 * m));
                     const float v0 = __uint_as_float(vv << 16), v1 = __uint_as_float(vv & 0xFFFF0000u);
                     const float bt = ax.beta[t], gt = ax.gamma[t];
                     const bool live = t < T;
@@ -544,7 +605,7 @@ __global__ void __launch_bounds__(kThreads, kBlocksPerSM)
                 }
 
         // 7. W^T = R^T Tinv^T: A = R^T (accumulator layout, split), B = Tinv^T (split).
-        float wq[2][2][4];
+        float wq[MT][2][4];
         {
             uint32_t bh[2][2], bl[2][2];
 #pragma unroll
@@ -554,7 +615,7 @@ __global__ void __launch_bounds__(kThreads, kBlocksPerSM)
                 split2(tr[2 * c + 8], tr[2 * c + 9], bh[nt][1], bl[nt][1]);
             }
 #pragma unroll
-            for (int m = 0; m < 2; ++m) {
+            for (int m = 0; m < MT; ++m) {
                 uint32_t ah[4], al[4];
                 split2(rr_[m][0][0], rr_[m][0][1], ah[0], al[0]);
                 split2(rr_[m][0][2], rr_[m][0][3], ah[1], al[1]);
@@ -580,9 +641,9 @@ __global__ void __launch_bounds__(kThreads, kBlocksPerSM)
                 split2(mr[2 * c], mr[2 * c + 1], bh[nt][0], bl[nt][0]);
                 split2(mr[2 * c + 8], mr[2 * c + 9], bh[nt][1], bl[nt][1]);
             }
-            float *go = p.o + ((size_t)me.u.row0 * p.H + me.h) * D + 32 * warp + 4 * g;
+            float *go = p.o + ((size_t)me.u.row0 * p.H + me.h) * D + col0;
 #pragma unroll
-            for (int m = 0; m < 2; ++m) {
+            for (int m = 0; m < MT; ++m) {
                 uint32_t ah[4], al[4];
                 split2(wq[m][0][0], wq[m][0][1], ah[0], al[0]);
                 split2(wq[m][0][2], wq[m][0][3], ah[1], al[1]);
@@ -606,14 +667,15 @@ __global__ void __launch_bounds__(kThreads, kBlocksPerSM)
             }
         }
 
-        // 9. Commit: H_a^T = gamma_{a-1} H_0^T + (D[a-1][.] w)^T K, accumulated in hr.
+        // 9. Commit: H_a^T = gamma_{a-1} H_0^T + (D[a-1][.] w)^T K, 16 key rows at a
+        //    time: accumulators start from the tile (re-read from shared memory).
         if (write_state) {
-            uint32_t ah[2][4], al[2][4];
+            uint32_t ah[MT][4], al[MT][4];
 #pragma unroll
             for (int ntt = 0; ntt < 2; ++ntt) {
                 const float d0 = ax.dcol[8 * ntt + 2 * c], d1 = ax.dcol[8 * ntt + 2 * c + 1];
 #pragma unroll
-                for (int m = 0; m < 2; ++m) {
+                for (int m = 0; m < MT; ++m) {
                     split2(d0 * wq[m][ntt][0], d1 * wq[m][ntt][1], ah[m][2 * ntt], al[m][2 * ntt]);
                     split2(d0 * wq[m][ntt][2], d1 * wq[m][ntt][3], ah[m][2 * ntt + 1],
                            al[m][2 * ntt + 1]);
@@ -623,36 +685,56 @@ __global__ void __launch_bounds__(kThreads, kBlocksPerSM)
             // ldmatrix.trans row address of this lane: matrix lane/8 -> (token half, dk half).
             const int mi = lane >> 3;
             const int krow = (lane & 7) + 8 * (mi & 1);
-            float *dst = opaque(me.u.tile) + 32 * warp + 4 * g;
+            float *dst = opaque(me.u.tile) + col0;
 #pragma unroll
             for (int kb = 0; kb < 8; ++kb) {
+                float hv[4][CPT];
 #pragma unroll
-                for (int rr = 0; rr < 4; ++rr)
+                for (int rr = 0; rr < 4; ++rr) {
+                    if (kRegTile) {
 #pragma unroll
-                    for (int e = 0; e < 4; ++e) hr[kb][rr][e] *= gam;
+                        for (int e = 0; e < CPT; ++e) hv[rr][e] = hr[kRegTile ? kb : 0][rr][e];
+                    } else {
+                        ld_tile_row<NW>(sm.tile, warp, g, 16 * kb + 2 * c + (rr & 1) + 8 * (rr >> 1),
+                                        hv[rr]);
+                    }
+#pragma unroll
+                    for (int e = 0; e < CPT; ++e) hv[rr][e] *= gam;
+                }
                 uint32_t b00, b01, b10, b11;  // (n-tile 2kb: b0, b1), (n-tile 2kb+1: b0, b1)
                 ldsm_x4_trans(b00, b01, b10, b11,
                               smem_u32(tb.k) + tok_off(krow, 16 * kb + 8 * (mi >> 1)));
 #pragma unroll
-                for (int m = 0; m < 2; ++m) {
-                    mma(hr[kb][0][2 * m], hr[kb][1][2 * m], hr[kb][0][2 * m + 1],
-                        hr[kb][1][2 * m + 1], ah[m][0], ah[m][1], ah[m][2], ah[m][3], b00, b01);
-                    mma(hr[kb][2][2 * m], hr[kb][3][2 * m], hr[kb][2][2 * m + 1],
-                        hr[kb][3][2 * m + 1], ah[m][0], ah[m][1], ah[m][2], ah[m][3], b10, b11);
+                for (int m = 0; m < MT; ++m) {
+                    mma(hv[0][2 * m], hv[1][2 * m], hv[0][2 * m + 1], hv[1][2 * m + 1], ah[m][0],
+                        ah[m][1], ah[m][2], ah[m][3], b00, b01);
+                    mma(hv[2][2 * m], hv[3][2 * m], hv[2][2 * m + 1], hv[3][2 * m + 1], ah[m][0],
+                        ah[m][1], ah[m][2], ah[m][3], b10, b11);
                 }
 #pragma unroll
-                for (int m = 0; m < 2; ++m) {
-                    mma(hr[kb][0][2 * m], hr[kb][1][2 * m], hr[kb][0][2 * m + 1],
-                        hr[kb][1][2 * m + 1], al[m][0], al[m][1], al[m][2], al[m][3], b00, b01);
-                    mma(hr[kb][2][2 * m], hr[kb][3][2 * m], hr[kb][2][2 * m + 1],
-                        hr[kb][3][2 * m + 1], al[m][0], al[m][1], al[m][2], al[m][3], b10, b11);
+                for (int m = 0; m < MT; ++m) {
+                    mma(hv[0][2 * m], hv[1][2 * m], hv[0][2 * m + 1], hv[1][2 * m + 1], al[m][0],
+                        al[m][1], al[m][2], al[m][3], b00, b01);
+                    mma(hv[2][2 * m], hv[3][2 * m], hv[2][2 * m + 1], hv[3][2 * m + 1], al[m][0],
+                        al[m][1], al[m][2], al[m][3], b10, b11);
                 }
 #pragma unroll
                 for (int rr = 0; rr < 4; ++rr) {
-                    const int row = 16 * kb + 2 * c + (rr & 1) + 8 * (rr >> 1);
-                    *reinterpret_cast<float4 *>(dst + row * D) =
-                        make_float4(hr[kb][rr][0], hr[kb][rr][1], hr[kb][rr][2], hr[kb][rr][3]);
+                    float *rowp = dst + (16 * kb + 2 * c + (rr & 1) + 8 * (rr >> 1)) * D;
+                    if (CPT == 4)
+                        *reinterpret_cast<float4 *>(rowp) =
+                            make_float4(hv[rr][0], hv[rr][1], hv[rr][2], hv[rr][3]);
+                    else
+                        *reinterpret_cast<float2 *>(rowp) = make_float2(hv[rr][0], hv[rr][1]);
                 }
+            }
+        }
+        if (keep_tile) {
+            // The commit has read the tile: the stage is free now.
+            __syncthreads();
+            if (!cur.skip) {
+                if (tid == 0) issue_tile(maps, p, cur, sm.tile, tile_bar);
+                ++issued;
             }
         }
     }
@@ -702,14 +784,21 @@ constexpr int kMaxDevices = 64;
 
 struct DeviceInfo {
     int sms = 0;
-    bool smem_set[3] = {false, false, false};
+    bool smem_set[3][2] = {{false, false}, {false, false}, {false, false}};
 };
 
 DeviceInfo g_dev[kMaxDevices];
 std::mutex g_dev_mutex;
 
+// Warps per block for each mode.
 template <int MODE>
+struct ModeWarps {
+    static constexpr int NW = 4;
+};
+
+template <int MODE, bool RAGGED>
 cudaError_t launch_mode(const Args &p, const Maps &maps, cudaStream_t stream) {
+    constexpr int NW = ModeWarps<MODE>::NW;
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
@@ -722,18 +811,18 @@ cudaError_t launch_mode(const Args &p, const Maps &maps, cudaStream_t stream) {
             e = cudaDeviceGetAttribute(&info.sms, cudaDevAttrMultiProcessorCount, dev);
             if (e != cudaSuccess) return e;
         }
-        if (!info.smem_set[MODE]) {
-            e = cudaFuncSetAttribute(chunk_kernel<MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                     (int)kSmemBytes);
+        if (!info.smem_set[MODE][RAGGED]) {
+            e = cudaFuncSetAttribute(chunk_kernel<MODE, NW, RAGGED>,
+                                     cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
             if (e != cudaSuccess) return e;
-            info.smem_set[MODE] = true;
+            info.smem_set[MODE][RAGGED] = true;
         }
         sms = info.sms;
     }
     const int units = p.B * p.H;
     const int slots = kBlocksPerSM * sms;
     const int grid = units < slots ? units : slots;
-    chunk_kernel<MODE><<<grid, kThreads, kSmemBytes, stream>>>(p, maps);
+    chunk_kernel<MODE, NW, RAGGED><<<grid, Cfg<NW>::kThreads, kSmemBytes, stream>>>(p, maps);
     return cudaGetLastError();
 }
 
@@ -747,7 +836,8 @@ bool chunk_preferred(int max_T) { return max_T >= 1; }
 
 cudaError_t launch_chunk(const Args &p, int mode, cudaStream_t stream) {
     const unsigned long long tiles = (unsigned long long)p.pool_slots * (unsigned long long)p.H;
-    if (tiles == 0 || tiles > (1ull << 31) || p.n_tok > (1ll << 31)) return cudaErrorInvalidValue;
+    if (tiles == 0 || tiles > (1ull << 31) || p.n_tok < 1 || p.n_tok > (1ll << 31))
+        return cudaErrorInvalidValue;
     PFN_cuTensorMapEncodeTiled_v12000 encode = encode_fn();
     if (!encode) return cudaErrorNotSupported;
     Maps maps;
@@ -764,10 +854,17 @@ cudaError_t launch_chunk(const Args &p, int mode, cudaStream_t stream) {
         !encode_tokens(encode, &maps.v, p.v, p.H, p.n_tok) ||
         !encode_tokens(encode, &maps.q, p.q, p.H, p.n_tok))
         return cudaErrorInvalidValue;
+    const bool ragged = p.cu_seqlens != nullptr;
     switch (mode) {
-        case kVerify: return launch_mode<kVerify>(p, maps, stream);
-        case kCommit: return launch_mode<kCommit>(p, maps, stream);
-        default: return launch_mode<kFused>(p, maps, stream);
+        case kVerify:
+            return ragged ? launch_mode<kVerify, true>(p, maps, stream)
+                          : launch_mode<kVerify, false>(p, maps, stream);
+        case kCommit:
+            return ragged ? launch_mode<kCommit, true>(p, maps, stream)
+                          : launch_mode<kCommit, false>(p, maps, stream);
+        default:
+            return ragged ? launch_mode<kFused, true>(p, maps, stream)
+                          : launch_mode<kFused, false>(p, maps, stream);
     }
 }
 
