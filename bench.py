@@ -180,6 +180,18 @@ def cpu_oracle_time(prob, n_units: int, threads: int):
     return dt, dt / len(units) * prob.units * 1e6, len(units)
 
 
+def max_over_ranks(value: float, world: int, device=None) -> float:
+    """The largest `value` over all ranks (the job's time is its slowest rank's)."""
+    if world <= 1:
+        return value
+    import torch
+    import torch.distributed as dist
+
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
 # ----------------------------------------------------------------- arms
 
 def run_reference(args, rank):
@@ -283,11 +295,7 @@ def run_ours(args, rank, world, local_rank):
     torch.cuda.synchronize()
     barrier()
     clk = clocks.stop()
-    ms_total = t_start.elapsed_time(t_end)
-    if world > 1:
-        t = torch.tensor([ms_total], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms_total = float(t.item())
+    ms_total = max_over_ranks(t_start.elapsed_time(t_end), world, dev)
     ms_step = ms_total / args.steps
     us_call = ms_step * 1e3 / L
 
