@@ -344,14 +344,24 @@ __global__ void __launch_bounds__(32 * NW, kBlocksPerSM)
     const uint32_t tile_bar = smem_u32(&ax.tile_full);
     const int col0 = warp * C::CW + CPT * g;  // this thread's first value column
 
+    // Programmatic dependent launch: the next kernel on the stream may be
+    // launched right away (its blocks become resident as ours exit and wait in
+    // their own prologue), and this kernel touches no global memory until the
+    // previous kernel on the stream has completed.  Stream order is kept.
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     if (tid == 0) {
         mbar_init(tile_bar, 1);
         mbar_init(smem_u32(&ax.tok_full[0]), 1);
         mbar_init(smem_u32(&ax.tok_full[1]), 1);
         ax.abort_flag = 0;
         asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
+#pragma unroll
+        for (int m = 0; m < 4; ++m)
+            asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&maps.pool + m))
+                         : "memory");
     }
     __syncthreads();
+    asm volatile("griddepcontrol.wait;" ::: "memory");
 
     // Plans: `cur` is the unit being computed, `nxt` the next one (its loads are
     // issued during `cur`), `raw` the metadata of the one after.
@@ -822,8 +832,17 @@ cudaError_t launch_mode(const Args &p, const Maps &maps, cudaStream_t stream) {
     const int units = p.B * p.H;
     const int slots = kBlocksPerSM * sms;
     const int grid = units < slots ? units : slots;
-    chunk_kernel<MODE, NW, RAGGED><<<grid, Cfg<NW>::kThreads, kSmemBytes, stream>>>(p, maps);
-    return cudaGetLastError();
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)grid);
+    cfg.blockDim = dim3((unsigned)Cfg<NW>::kThreads);
+    cfg.dynamicSmemBytes = kSmemBytes;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, chunk_kernel<MODE, NW, RAGGED>, p, maps);
 }
 
 }  // namespace
