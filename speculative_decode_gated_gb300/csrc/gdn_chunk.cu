@@ -278,6 +278,48 @@ __device__ __forceinline__ void prefetch_unit(const Maps &maps, const Args &p, c
     for (int b = 0; b < 4; ++b) tma_prefetch_3d(&maps.pool, 32 * b, 0, slot_unit);
 }
 
+// Read through L2 only (no L1 line is left behind), for the hints below.
+__device__ __forceinline__ int ld_l2(const int32_t *ptr) {
+    int v;
+    asm volatile("ld.global.cg.b32 %0, [%1];" : "=r"(v) : "l"(ptr));
+    return v;
+}
+
+// Thread 0, before the wait on the previous kernel of the stream: ask for the
+// tiles and token rows of this block's first two units in L2.  Prefetches
+// change no memory, so issuing them early is safe even when the previous
+// kernel is still writing what they touch (the real loads come after the wait
+// and read the current data from L2).  The metadata read here may be stale for
+// the same reason; it only picks addresses, clamped into the arrays, and is
+// read again after the wait.
+template <int MODE, bool RAGGED>
+__device__ __forceinline__ void early_prefetch(const Maps &maps, const Args &p, int unit0, int G,
+                                               int U) {
+    int h[2], row0[2], slot[2];
+#pragma unroll
+    for (int j = 0; j < 2; ++j) {
+        const int unit = unit0 + j * G < U ? unit0 + j * G : U - 1;
+        const int r = unit / p.H;
+        h[j] = unit - r * p.H;
+        row0[j] = RAGGED ? ld_l2(p.cu_seqlens + r) : r * p.max_T;
+        slot[j] = ld_l2(p.slot_ids + r);
+    }
+#pragma unroll
+    for (int j = 0; j < 2; ++j) {
+        if (unit0 + j * G >= U) break;
+        const long long row = row0[j] < 0 ? 0 : (row0[j] >= p.n_tok ? p.n_tok - 1 : row0[j]);
+        const long long sl = slot[j] < 0 ? 0 : (slot[j] >= p.pool_slots ? p.pool_slots - 1 : slot[j]);
+#pragma unroll
+        for (int hb = 0; hb < 2; ++hb) {
+            tma_prefetch_3d(&maps.k, 64 * hb, h[j], (int)row);
+            tma_prefetch_3d(&maps.v, 64 * hb, h[j], (int)row);
+            if (MODE != kCommit) tma_prefetch_3d(&maps.q, 64 * hb, h[j], (int)row);
+        }
+#pragma unroll
+        for (int b = 0; b < 4; ++b) tma_prefetch_3d(&maps.pool, 32 * b, 0, (int)(sl * p.H + h[j]));
+    }
+}
+
 // Gate of token min(tid, T - 1) of a unit (any clamped row when the unit is
 // skipped or tid >= T): always a valid address (the chunk kernel runs only
 // with n_tok >= 1), so the load never sits behind a branch.
@@ -346,7 +388,7 @@ __global__ void __launch_bounds__(32 * NW, kBlocksPerSM)
 
     // Programmatic dependent launch: the next kernel on the stream may be
     // launched right away (its blocks become resident as ours exit and wait in
-    // their own prologue), and this kernel touches no global memory until the
+    // their own prologue), and this kernel issues only L2 prefetches until the
     // previous kernel on the stream has completed.  Stream order is kept.
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     if (tid == 0) {
@@ -361,6 +403,7 @@ __global__ void __launch_bounds__(32 * NW, kBlocksPerSM)
                          : "memory");
     }
     __syncthreads();
+    if (tid == 0) early_prefetch<MODE, RAGGED>(maps, p, blockIdx.x, G, U);
     asm volatile("griddepcontrol.wait;" ::: "memory");
 
     // Plans: `cur` is the unit being computed, `nxt` the next one (its loads are
