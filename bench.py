@@ -43,7 +43,8 @@ WORKLOAD = "b64_h32_d128_t16_x24"
 METRIC = "us per layer-call (verify+commit) and achieved HBM GB/s vs ~8 TB/s, 1xGB300"
 UNIT = "us/layer-call"
 NOMINAL_HBM_GBS = 8000.0
-MODE_NAME = {"v": "verify", "c": "commit", "f": "fused"}
+MODE_NAME = {"v": "verify", "c": "commit", "f": "fused",
+             "C": "commit_layers", "F": "fused_layers"}  # upper case: one launch, all layers
 
 
 # ----------------------------------------------------------------- accounting
@@ -242,17 +243,32 @@ def run_ours(args, rank, world, local_rank):
                             layers=L if multi else None)
     dps = [staging.DeviceProblem(pr, dev, pool=(pool[l] if multi else pool), algo=args.algo)
            for l, pr in enumerate(layers)]
+    if multi:
+        staging.share_request_arrays(dps)  # one step's requests, as an engine holds them
     fused = args.mode == "fused"
-    kinds = ["f"] if fused else ["v", "c"]
-    bytes_of = {m: [alg_bytes(pr, MODE_NAME[m]) for pr in layers] for m in ("v", "c", "f")}
-    bytes_call = sum(sum(bytes_of[m]) for m in kinds) / L
+    batched = args.batch_layers
+    if batched and not (multi and (fused or args.order == "engine")):
+        raise SystemExit("--batch-layers needs a multi-layer workload and --mode fused or "
+                         "--order engine")
     stream = torch.cuda.current_stream(dev)
-
-    if args.order == "engine" and not fused:
-        order = [(d, "v") for d in dps] + [(d, "c") for d in dps]
+    per_layer = {m: [alg_bytes(pr, MODE_NAME[m]) for pr in layers] for m in ("v", "c", "f")}
+    # bytes_of[kind]: algorithmic bytes of each launch of that kind in one step
+    bytes_of = dict(per_layer, C=[sum(per_layer["c"])], F=[sum(per_layer["f"])])
+    if batched and fused:
+        kinds = ["F"]
+        calls = [("F", staging.layers_launcher(dps, "fused", stream))]
+    elif batched:
+        kinds = ["v", "C"]
+        calls = ([("v", d.launcher("verify", stream)) for d in dps]
+                 + [("C", staging.layers_launcher(dps, "commit", stream))])
     else:
-        order = [(d, m) for d in dps for m in kinds]
-    calls = [(m, d.launcher(MODE_NAME[m], stream)) for d, m in order]
+        kinds = ["f"] if fused else ["v", "c"]
+        if args.order == "engine" and not fused:
+            order = [(d, "v") for d in dps] + [(d, "c") for d in dps]
+        else:
+            order = [(d, m) for d in dps for m in kinds]
+        calls = [(m, d.launcher(MODE_NAME[m], stream)) for d, m in order]
+    bytes_call = sum(sum(bytes_of[m]) for m in kinds) / L
 
     def step(events=None):
         if events is None:
@@ -277,7 +293,7 @@ def run_ours(args, rank, world, local_rank):
         if world > 1:
             dist.barrier()
 
-    n_per_step = {m: sum(1 for _, mm in order if mm == m) for m in kinds}
+    n_per_step = {m: sum(1 for mm, _ in calls if mm == m) for m in kinds}
     events = {m: [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
                   for _ in range(n_per_step[m] * args.steps)] for m in kinds}
     events["i"] = {m: 0 for m in kinds}
@@ -309,7 +325,7 @@ def run_ours(args, rank, world, local_rank):
 
     avg_ms = {m: statistics.fmean(a.elapsed_time(b) for a, b in events[m]) for m in kinds}
     dominant = max(kinds, key=lambda m: avg_ms[m] * n_per_step[m])
-    per_launch_bytes = {m: sum(bytes_of[m]) / L for m in kinds}
+    per_launch_bytes = {m: sum(bytes_of[m]) / len(bytes_of[m]) for m in kinds}
     peak, peak_kind = measured_peaks()
     achieved = per_launch_bytes[dominant] / (avg_ms[dominant] * 1e-3) / 1e9
     algo_used = binding.gdn_select_algo(dps[0].c)
@@ -317,7 +333,7 @@ def run_ours(args, rank, world, local_rank):
             + "_" + MODE_NAME[dominant])
     traffic = profile_traffic(ktag, name)
 
-    e2e = run_e2e(args, dps, stream, dev, fused) if not args.no_e2e else None
+    e2e = run_e2e(args, dps, stream, dev, fused) if not (args.no_e2e or batched) else None
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -339,7 +355,9 @@ def run_ours(args, rank, world, local_rank):
                 "description": (f"batch {p0.batch}, heads {p0.heads}, dk {p0.dk}, dv {p0.dv}, "
                                 f"draft {p0.max_T}, {L} layer(s), pool {p0.pool_slots} slots/layer, "
                                 f"q/k/v {p0.qkv_dtype}, gates/state/o fp32"),
-                "order": ("fused per layer" if fused else
+                "order": ("fused, all layers in one launch" if fused and batched else
+                          "fused per layer" if fused else
+                          "all verifies, then all layers' commits in one launch" if batched else
                           "verify then commit per layer" if args.order == "interleaved" else
                           "all verifies then all commits"),
                 "l2": "inputs larger than L2 (each step touches ~%.1f GB)" % (bytes_call * L / 1e9),
@@ -434,6 +452,8 @@ def main():
     ap.add_argument("--ref-units", type=int, default=64)
     ap.add_argument("--e2e-steps", type=int, default=20)
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--batch-layers", action="store_true",
+                    help="all layers' commits (or fused calls) in one layer-batch launch")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()
     if args.mode is None:

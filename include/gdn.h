@@ -72,7 +72,8 @@ typedef enum gdn_status {
     GDN_ERR_DEVICE_ARG = 5,   /* reported by gdn_read_device_error only */
     GDN_ERR_CUDA = 6,         /* a CUDA call failed; see gdn_last_error_string */
     GDN_ERR_ALIGN = 7,        /* a pointer is not aligned (16 bytes for q/k/v/pool/o) */
-    GDN_ERR_ALIAS = 8         /* o overlaps an input, or the pool overlaps q/k/v/o */
+    GDN_ERR_ALIAS = 8,        /* o overlaps an input, or the pool overlaps q/k/v/o */
+    GDN_ERR_LAYER_MISMATCH = 9 /* the problems of a layer batch disagree on a shared field */
 } gdn_status;
 
 typedef enum gdn_dtype {
@@ -135,6 +136,29 @@ GDN_API gdn_status gdn_commit(const gdn_problem *p, const int32_t *accepted, cud
  * checkpoint is read once, o is written for every token, the state once. */
 GDN_API gdn_status gdn_verify_commit_fused(const gdn_problem *p, const int32_t *accepted,
                                            float *o, cudaStream_t stream);
+
+/* Layer batches: the same calls for the n_layers problems of one step (one per
+ * model layer), in as few launches as possible (the chunked kernel takes up to
+ * 32 layers per launch, so the fill and drain of a launch are paid once for
+ * all of them instead of once per layer).
+ *
+ * problems: host array of n_layers gdn_problem.  They must agree on the
+ * request-level fields (batch, heads, dk, dv, max_T, qkv_dtype, algo,
+ * cu_seqlens, slot_ids, pool_slots, and n_tok when ragged), else
+ * GDN_ERR_LAYER_MISMATCH; each names its own q, k, v, alpha, beta, pool (that
+ * layer's pool) and dev_err.  o: host array of n_layers device pointers, o[l]
+ * for problem l as in gdn_verify.  accepted: one device array, shared by all
+ * layers.  Each problem is validated as by the single-problem call; besides,
+ * no layer's o, nor (commit, fused) its pool, may overlap another layer's
+ * arrays (GDN_ERR_ALIAS).  The results equal those of the single-problem call
+ * made once per layer.  n_layers = 0 launches nothing. */
+GDN_API gdn_status gdn_verify_layers(const gdn_problem *problems, int32_t n_layers,
+                                     float *const *o, cudaStream_t stream);
+GDN_API gdn_status gdn_commit_layers(const gdn_problem *problems, int32_t n_layers,
+                                     const int32_t *accepted, cudaStream_t stream);
+GDN_API gdn_status gdn_verify_commit_fused_layers(const gdn_problem *problems, int32_t n_layers,
+                                                  const int32_t *accepted, float *const *o,
+                                                  cudaStream_t stream);
 
 /* Waits for `stream`, copies *p->dev_err to *host_code (0 when dev_err is NULL).
  * Returns GDN_ERR_DEVICE_ARG when the word is non-zero, GDN_OK when it is zero. */

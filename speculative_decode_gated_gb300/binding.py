@@ -18,6 +18,7 @@ LIB_PATH = os.path.join(_PKG, "_lib", "libgdn.so")
 
 GDN_OK = 0
 GDN_ERR_DEVICE_ARG = 5
+GDN_ERR_ALIAS, GDN_ERR_LAYER_MISMATCH = 8, 9
 GDN_FP32, GDN_BF16 = 0, 1
 GDN_ALGO_AUTO, GDN_ALGO_RECURRENT, GDN_ALGO_CHUNK = 0, 1, 2
 GDN_DEVERR_SLOT, GDN_DEVERR_ACCEPTED, GDN_DEVERR_SEQLEN = 1, 2, 4
@@ -25,8 +26,10 @@ GDN_MAX_T = 1024
 
 # Every symbol include/gdn.h declares.
 EXPORTED = (
-    "gdn_verify", "gdn_commit", "gdn_verify_commit_fused", "gdn_read_device_error",
-    "gdn_select_algo", "gdn_status_string", "gdn_last_error_string", "gdn_version",
+    "gdn_verify", "gdn_commit", "gdn_verify_commit_fused",
+    "gdn_verify_layers", "gdn_commit_layers", "gdn_verify_commit_fused_layers",
+    "gdn_read_device_error", "gdn_select_algo", "gdn_status_string", "gdn_last_error_string",
+    "gdn_version",
 )
 
 
@@ -69,10 +72,15 @@ def lib() -> ctypes.CDLL:
         h.gdn_verify.argtypes = [P, S, S]
         h.gdn_commit.argtypes = [P, S, S]
         h.gdn_verify_commit_fused.argtypes = [P, S, S, S]
+        I32 = ctypes.c_int32
+        h.gdn_verify_layers.argtypes = [P, I32, S, S]
+        h.gdn_commit_layers.argtypes = [P, I32, S, S]
+        h.gdn_verify_commit_fused_layers.argtypes = [P, I32, S, S, S]
         h.gdn_read_device_error.argtypes = [P, S, ctypes.POINTER(ctypes.c_int32)]
         h.gdn_select_algo.argtypes = [P]
         h.gdn_status_string.argtypes = [ctypes.c_int]
         for name in ("gdn_verify", "gdn_commit", "gdn_verify_commit_fused",
+                     "gdn_verify_layers", "gdn_commit_layers", "gdn_verify_commit_fused_layers",
                      "gdn_read_device_error", "gdn_select_algo"):
             getattr(h, name).restype = ctypes.c_int
         for name in ("gdn_status_string", "gdn_last_error_string", "gdn_version"):
@@ -177,6 +185,51 @@ def gdn_verify_commit_fused(prob: Problem, accepted: torch.Tensor, o: torch.Tens
     _check(o, "o", (torch.float32,), None)
     _raise(lib().gdn_verify_commit_fused(prob.ref, _ptr(accepted), _ptr(o), _stream(stream)),
            "gdn_verify_commit_fused")
+
+
+class ProblemArray:
+    """A host array of gdn_problem (one per layer) for the layer-batch calls."""
+
+    def __init__(self, problems):
+        self.problems = list(problems)
+        n = len(self.problems)
+        self.c = (gdn_problem * max(n, 1))()
+        for i, p in enumerate(self.problems):
+            self.c[i] = p.c
+        self.n = n
+
+    @property
+    def ref(self):
+        return ctypes.cast(self.c, ctypes.POINTER(gdn_problem))
+
+
+def _ptr_array(tensors) -> ctypes.Array:
+    arr = (ctypes.c_void_p * max(len(tensors), 1))()
+    for i, t in enumerate(tensors):
+        _check(t, f"o[{i}]", (torch.float32,), None)
+        arr[i] = _ptr(t)
+    return arr
+
+
+def gdn_verify_layers(probs: ProblemArray, o, stream=None) -> None:
+    """o: one fp32 output tensor per layer."""
+    arr = _ptr_array(o)
+    _raise(lib().gdn_verify_layers(probs.ref, probs.n, arr, _stream(stream)), "gdn_verify_layers")
+
+
+def gdn_commit_layers(probs: ProblemArray, accepted: torch.Tensor, stream=None) -> None:
+    _check(accepted, "accepted", (torch.int32,), None)
+    _raise(lib().gdn_commit_layers(probs.ref, probs.n, _ptr(accepted), _stream(stream)),
+           "gdn_commit_layers")
+
+
+def gdn_verify_commit_fused_layers(probs: ProblemArray, accepted: torch.Tensor, o,
+                                   stream=None) -> None:
+    _check(accepted, "accepted", (torch.int32,), None)
+    arr = _ptr_array(o)
+    _raise(lib().gdn_verify_commit_fused_layers(probs.ref, probs.n, _ptr(accepted), arr,
+                                                _stream(stream)),
+           "gdn_verify_commit_fused_layers")
 
 
 def gdn_read_device_error(prob: Problem, stream=None) -> int:

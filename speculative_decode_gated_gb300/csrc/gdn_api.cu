@@ -34,6 +34,34 @@ bool overlap(Range a, Range b) {
     return a.lo < b.hi && b.lo < a.hi;
 }
 
+// Rows of the token arrays.
+int64_t token_rows(const gdn_problem *p) {
+    return p->cu_seqlens ? p->n_tok : (int64_t)p->batch * p->max_T;
+}
+
+// The byte ranges of one problem's per-layer arrays.
+struct LayerRanges {
+    Range q, k, v, alpha, beta, pool;
+};
+
+LayerRanges layer_ranges(const gdn_problem *p) {
+    const int64_t H = p->heads;
+    const int64_t n_tok = token_rows(p);
+    const int64_t esz = p->qkv_dtype == GDN_BF16 ? 2 : 4;
+    LayerRanges r;
+    r.q = range(p->q, n_tok * H * p->dk * esz);
+    r.k = range(p->k, n_tok * H * p->dk * esz);
+    r.v = range(p->v, n_tok * H * p->dv * esz);
+    r.alpha = range(p->alpha, n_tok * H * 4);
+    r.beta = range(p->beta, n_tok * H * 4);
+    r.pool = range(p->pool, p->pool_slots * H * p->dk * p->dv * 4);
+    return r;
+}
+
+Range o_range(const gdn_problem *p, const float *o) {
+    return range(o, token_rows(p) * p->heads * p->dv * 4);
+}
+
 bool dims_supported(int dk, int dv) {
     const bool dk_ok = dk == 32 || dk == 64 || dk == 128;
     const bool dv_ok = dv >= 32 && dv <= 256 && dv % 32 == 0 && (dv <= 128 || dv % 128 == 0);
@@ -82,15 +110,8 @@ gdn_status validate(const gdn_problem *p, bool with_o, const float *o, bool with
         return GDN_ERR_ALIGN;
 
     // Aliasing: o must not overlap any input; the pool must not overlap q/k/v/gates/metadata.
-    const int64_t H = p->heads;
-    const int64_t n_tok = p->cu_seqlens ? p->n_tok : (int64_t)p->batch * p->max_T;
-    const int64_t esz = p->qkv_dtype == GDN_BF16 ? 2 : 4;
-    const Range rq = range(p->q, n_tok * H * p->dk * esz);
-    const Range rk = range(p->k, n_tok * H * p->dk * esz);
-    const Range rv = range(p->v, n_tok * H * p->dv * esz);
-    const Range ra = range(p->alpha, n_tok * H * 4);
-    const Range rb = range(p->beta, n_tok * H * 4);
-    const Range rp = range(p->pool, p->pool_slots * H * p->dk * p->dv * 4);
+    const LayerRanges lr = layer_ranges(p);
+    const Range rq = lr.q, rk = lr.k, rv = lr.v, ra = lr.alpha, rb = lr.beta, rp = lr.pool;
     const Range rs = range(p->slot_ids, (int64_t)p->batch * 4);
     const Range rc = range(p->cu_seqlens, p->cu_seqlens ? ((int64_t)p->batch + 1) * 4 : 0);
     const Range racc = range(accepted, with_acc ? (int64_t)p->batch * 4 : 0);
@@ -99,7 +120,7 @@ gdn_status validate(const gdn_problem *p, bool with_o, const float *o, bool with
     for (const Range &x : others)
         if (overlap(rp, x)) return GDN_ERR_ALIAS;
     if (with_o) {
-        const Range ro = range(o, n_tok * H * p->dv * 4);
+        const Range ro = o_range(p, o);
         const Range all[] = {rq, rk, rv, ra, rb, rp, rs, rc, racc, re};
         for (const Range &x : all)
             if (overlap(ro, x)) return GDN_ERR_ALIAS;
@@ -140,11 +161,77 @@ gdn_status run(const gdn_problem *p, int mode, const int32_t *accepted, float *o
     if (st != GDN_OK || empty) return st;
     const gdn::Args a = make_args(p, with_acc ? accepted : nullptr, with_o ? o : nullptr);
     const bool bf16 = p->qkv_dtype == GDN_BF16;
-    const cudaError_t e = algo == GDN_ALGO_CHUNK ? gdn::launch_chunk(a, mode, stream)
+    const cudaError_t e = algo == GDN_ALGO_CHUNK ? gdn::launch_chunk(&a, 1, mode, stream)
                                                  : gdn::launch_recurrent(a, mode, bf16, stream);
     if (e != cudaSuccess) {
         set_cuda_error(e, "kernel launch");
         return GDN_ERR_CUDA;
+    }
+    return GDN_OK;
+}
+
+// The request-level fields that all problems of a layer batch share.
+bool same_requests(const gdn_problem *a, const gdn_problem *b) {
+    return a->batch == b->batch && a->heads == b->heads && a->dk == b->dk && a->dv == b->dv &&
+           a->max_T == b->max_T && a->qkv_dtype == b->qkv_dtype && a->algo == b->algo &&
+           a->cu_seqlens == b->cu_seqlens && a->slot_ids == b->slot_ids &&
+           a->pool_slots == b->pool_slots && (!a->cu_seqlens || a->n_tok == b->n_tok);
+}
+
+// Layer batch: every problem passes the single-problem checks, all share the
+// request-level fields, and no layer's output (o, or the pool it commits
+// into) overlaps another layer's arrays.  Then up to gdn::kChunkMaxLayers
+// layers go into each launch of the chunked kernel; the recurrent kernel runs
+// once per layer.
+gdn_status run_layers(const gdn_problem *ps, int32_t n, int mode, const int32_t *accepted,
+                      float *const *o, cudaStream_t stream) {
+    if (n < 0) return GDN_ERR_BAD_DIM;
+    if (n == 0) return GDN_OK;
+    if (!ps) return GDN_ERR_NULL_PTR;
+    const bool with_o = mode != gdn::kCommit;
+    const bool with_acc = mode != gdn::kVerify;
+    if (with_o && !o) return GDN_ERR_NULL_PTR;
+    int algo = 0;
+    bool empty = false;
+    for (int32_t l = 0; l < n; ++l) {
+        const gdn_status st =
+            validate(&ps[l], with_o, with_o ? o[l] : nullptr, with_acc, accepted, &algo, &empty);
+        if (st != GDN_OK) return st;
+        if (l > 0 && !same_requests(&ps[0], &ps[l])) return GDN_ERR_LAYER_MISMATCH;
+    }
+    if (empty) return GDN_OK;
+    for (int32_t i = 0; i < n; ++i) {
+        const Range ro = with_o ? o_range(&ps[i], o[i]) : Range{0, 0};
+        const Range rpool = layer_ranges(&ps[i]).pool;
+        for (int32_t j = 0; j < n; ++j) {
+            if (i == j) continue;
+            const LayerRanges r = layer_ranges(&ps[j]);
+            const Range ins[] = {r.q, r.k, r.v, r.alpha, r.beta, r.pool};
+            for (const Range &x : ins) {
+                if (with_o && overlap(ro, x)) return GDN_ERR_ALIAS;
+                if (with_acc && overlap(rpool, x)) return GDN_ERR_ALIAS;
+            }
+            if (with_o && overlap(ro, o_range(&ps[j], o[j]))) return GDN_ERR_ALIAS;
+        }
+    }
+    const bool bf16 = ps[0].qkv_dtype == GDN_BF16;
+    for (int32_t l0 = 0; l0 < n; l0 += gdn::kChunkMaxLayers) {
+        const int m = n - l0 < gdn::kChunkMaxLayers ? n - l0 : gdn::kChunkMaxLayers;
+        gdn::Args a[gdn::kChunkMaxLayers];
+        for (int l = 0; l < m; ++l)
+            a[l] = make_args(&ps[l0 + l], with_acc ? accepted : nullptr,
+                             with_o ? o[l0 + l] : nullptr);
+        cudaError_t e = cudaSuccess;
+        if (algo == GDN_ALGO_CHUNK) {
+            e = gdn::launch_chunk(a, m, mode, stream);
+        } else {
+            for (int l = 0; l < m && e == cudaSuccess; ++l)
+                e = gdn::launch_recurrent(a[l], mode, bf16, stream);
+        }
+        if (e != cudaSuccess) {
+            set_cuda_error(e, "kernel launch");
+            return GDN_ERR_CUDA;
+        }
     }
     return GDN_OK;
 }
@@ -164,6 +251,22 @@ gdn_status gdn_commit(const gdn_problem *p, const int32_t *accepted, cudaStream_
 gdn_status gdn_verify_commit_fused(const gdn_problem *p, const int32_t *accepted, float *o,
                                    cudaStream_t stream) {
     return run(p, gdn::kFused, accepted, o, stream);
+}
+
+gdn_status gdn_verify_layers(const gdn_problem *problems, int32_t n_layers, float *const *o,
+                             cudaStream_t stream) {
+    return run_layers(problems, n_layers, gdn::kVerify, nullptr, o, stream);
+}
+
+gdn_status gdn_commit_layers(const gdn_problem *problems, int32_t n_layers,
+                             const int32_t *accepted, cudaStream_t stream) {
+    return run_layers(problems, n_layers, gdn::kCommit, accepted, nullptr, stream);
+}
+
+gdn_status gdn_verify_commit_fused_layers(const gdn_problem *problems, int32_t n_layers,
+                                          const int32_t *accepted, float *const *o,
+                                          cudaStream_t stream) {
+    return run_layers(problems, n_layers, gdn::kFused, accepted, o, stream);
 }
 
 gdn_status gdn_read_device_error(const gdn_problem *p, cudaStream_t stream, int32_t *host_code) {
@@ -202,6 +305,8 @@ const char *gdn_status_string(gdn_status s) {
         case GDN_ERR_CUDA: return "a CUDA call failed";
         case GDN_ERR_ALIGN: return "a pointer is not aligned (16 bytes for q/k/v/pool/o)";
         case GDN_ERR_ALIAS: return "an output overlaps an input";
+        case GDN_ERR_LAYER_MISMATCH:
+            return "the problems of a layer batch disagree on a request-level field";
     }
     return "unknown status";
 }

@@ -201,16 +201,33 @@ __device__ __forceinline__ uint32_t ld_tok32(const unsigned char *tile, int t, i
 struct UnitPlan {
     Unit u = {0, 0, -1, nullptr};
     int h = 0;
-    int teff = 0;  // tokens that matter: T_r, or a_r for commit
+    int layer = 0;  // which problem of the launch
+    int tile = 0;   // slot * H + h: the tile's index in its layer's pool
+    int teff = 0;   // tokens that matter: T_r, or a_r for commit
     bool skip = true;
 };
 
-// Metadata of `unit`, loaded unconditionally (the unit index is clamped to a
-// valid one) so that no select or branch ever waits on these loads: they are
+struct Maps {
+    CUtensorMap pool, q, k, v;
+};
+
+// One launch: NL problems that share every request-level field (batch, heads,
+// lengths, slot ids, accepted lengths) and differ in their tokens, gates,
+// outputs and pool.  Unit w of the launch is unit w % U of layer w / U.
+template <int NL>
+struct Launch {
+    Maps maps[NL];
+    Args a[NL];
+    int n;  // layers in use, 1..NL
+};
+
+// Metadata of launch unit `w`, loaded unconditionally (the index is clamped to
+// a valid one) so that no select or branch ever waits on these loads: they are
 // consumed an iteration later, when the plan decides whether the unit exists.
-template <int MODE, bool RAGGED>
-__device__ __forceinline__ RawMeta load_unit_meta(const Args &p, int unit, int U) {
-    const int r = (unit < U ? unit : U - 1) / p.H;
+template <int MODE, bool RAGGED, int NL>
+__device__ __forceinline__ RawMeta load_unit_meta(const Args &p, int w, int W, int U) {
+    const int wc = w < W ? w : W - 1;
+    const int r = (NL == 1 ? wc : wc % U) / p.H;
     RawMeta m;
     if (RAGGED) {
         m.cu0 = ld_early(p.cu_seqlens + r);
@@ -224,19 +241,19 @@ __device__ __forceinline__ RawMeta load_unit_meta(const Args &p, int unit, int U
     return m;
 }
 
-template <int MODE>
-__device__ __forceinline__ UnitPlan plan_unit(const Args &p, int unit, const RawMeta &m) {
+template <int MODE, int NL>
+__device__ __forceinline__ UnitPlan plan_unit(const Launch<NL> &L, int w, int U, const RawMeta &m) {
     UnitPlan pl;
+    pl.layer = NL == 1 ? 0 : w / U;
+    const int unit = w - pl.layer * U;
+    const Args &p = L.a[pl.layer];
     pl.h = unit - (unit / p.H) * p.H;
     const bool ok = check_meta(p, m, pl.h, MODE, pl.u);
+    pl.tile = ok ? m.slot * p.H + pl.h : 0;
     pl.teff = ok ? ((MODE == kCommit) ? pl.u.a : pl.u.T) : 0;
     pl.skip = !ok || pl.teff == 0;
     return pl;
 }
-
-struct Maps {
-    CUtensorMap pool, q, k, v;
-};
 
 // Thread 0: the token boxes (k, v and, unless committing, q) of one unit.
 template <int MODE>
@@ -254,20 +271,18 @@ __device__ __forceinline__ void issue_tokens(const Maps &maps, const UnitPlan &p
 }
 
 // Thread 0: the four tile boxes of one unit.
-__device__ __forceinline__ void issue_tile(const Maps &maps, const Args &p, const UnitPlan &pl,
+__device__ __forceinline__ void issue_tile(const Maps &maps, const UnitPlan &pl,
                                            unsigned char *tile, uint32_t tile_bar) {
-    const int slot_unit = (int)((pl.u.tile - p.pool) / (D * D));  // slot * H + h
     mbar_arrive_expect_tx(tile_bar, kTileBytes);
 #pragma unroll
     for (int b = 0; b < 4; ++b)
-        tma_load_3d(smem_u32(tile) + b * kBoxBytes, &maps.pool, 32 * b, 0, slot_unit, tile_bar);
+        tma_load_3d(smem_u32(tile) + b * kBoxBytes, &maps.pool, 32 * b, 0, pl.tile, tile_bar);
 }
 
 // Thread 0: pull the tile and token rows of a later unit into L2 (no shared
 // memory, no barrier), so its shared-memory loads, issued later, hit in L2.
 template <int MODE>
-__device__ __forceinline__ void prefetch_unit(const Maps &maps, const Args &p, const UnitPlan &pl) {
-    const int slot_unit = (int)((pl.u.tile - p.pool) / (D * D));
+__device__ __forceinline__ void prefetch_unit(const Maps &maps, const UnitPlan &pl) {
 #pragma unroll
     for (int hb = 0; hb < 2; ++hb) {
         tma_prefetch_3d(&maps.k, 64 * hb, pl.h, pl.u.row0);
@@ -275,7 +290,7 @@ __device__ __forceinline__ void prefetch_unit(const Maps &maps, const Args &p, c
         if (MODE != kCommit) tma_prefetch_3d(&maps.q, 64 * hb, pl.h, pl.u.row0);
     }
 #pragma unroll
-    for (int b = 0; b < 4; ++b) tma_prefetch_3d(&maps.pool, 32 * b, 0, slot_unit);
+    for (int b = 0; b < 4; ++b) tma_prefetch_3d(&maps.pool, 32 * b, 0, pl.tile);
 }
 
 // Read through L2 only (no L1 line is left behind), for the hints below.
@@ -292,13 +307,15 @@ __device__ __forceinline__ int ld_l2(const int32_t *ptr) {
 // and read the current data from L2).  The metadata read here may be stale for
 // the same reason; it only picks addresses, clamped into the arrays, and is
 // read again after the wait.
-template <int MODE, bool RAGGED>
-__device__ __forceinline__ void early_prefetch(const Maps &maps, const Args &p, int unit0, int G,
-                                               int U) {
-    int h[2], row0[2], slot[2];
+template <int MODE, bool RAGGED, int NL>
+__device__ __forceinline__ void early_prefetch(const Launch<NL> &L, int w0, int G, int W, int U) {
+    const Args &p = L.a[0];
+    int h[2], row0[2], slot[2], layer[2];
 #pragma unroll
     for (int j = 0; j < 2; ++j) {
-        const int unit = unit0 + j * G < U ? unit0 + j * G : U - 1;
+        const int w = w0 + j * G < W ? w0 + j * G : W - 1;
+        layer[j] = NL == 1 ? 0 : w / U;
+        const int unit = w - layer[j] * U;
         const int r = unit / p.H;
         h[j] = unit - r * p.H;
         row0[j] = RAGGED ? ld_l2(p.cu_seqlens + r) : r * p.max_T;
@@ -306,7 +323,8 @@ __device__ __forceinline__ void early_prefetch(const Maps &maps, const Args &p, 
     }
 #pragma unroll
     for (int j = 0; j < 2; ++j) {
-        if (unit0 + j * G >= U) break;
+        if (w0 + j * G >= W) break;
+        const Maps &maps = L.maps[layer[j]];
         const long long row = row0[j] < 0 ? 0 : (row0[j] >= p.n_tok ? p.n_tok - 1 : row0[j]);
         const long long sl = slot[j] < 0 ? 0 : (slot[j] >= p.pool_slots ? p.pool_slots - 1 : slot[j]);
 #pragma unroll
@@ -368,9 +386,9 @@ __device__ __forceinline__ void ld_tile_row(const unsigned char *tile, int warp,
     }
 }
 
-template <int MODE, int NW, bool RAGGED>
+template <int MODE, int NW, bool RAGGED, int NL>
 __global__ void __launch_bounds__(32 * NW, kBlocksPerSM)
-    chunk_kernel(const Args p, const __grid_constant__ Maps maps) {
+    chunk_kernel(const __grid_constant__ Launch<NL> L) {
     using C = Cfg<NW>;
     constexpr int MT = C::MT, CPT = C::CPT, NTH = C::kThreads;
     extern __shared__ unsigned char smem_raw[];
@@ -380,7 +398,9 @@ __global__ void __launch_bounds__(32 * NW, kBlocksPerSM)
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int g = lane >> 2, c = lane & 3;
-    const int U = p.B * p.H;
+    const Args &p = L.a[0];  // the request-level fields every layer shares
+    const int U = p.B * p.H;  // units per layer
+    const int W = NL == 1 ? U : U * L.n;  // units of the launch
     const int G = gridDim.x;
     const size_t row_stride = (size_t)p.H * D;
     const uint32_t tile_bar = smem_u32(&ax.tile_full);
@@ -399,23 +419,25 @@ __global__ void __launch_bounds__(32 * NW, kBlocksPerSM)
         asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
 #pragma unroll
         for (int m = 0; m < 4; ++m)
-            asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&maps.pool + m))
+            asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&L.maps[0].pool + m))
                          : "memory");
     }
     __syncthreads();
-    if (tid == 0) early_prefetch<MODE, RAGGED>(maps, p, blockIdx.x, G, U);
+    if (tid == 0) early_prefetch<MODE, RAGGED, NL>(L, blockIdx.x, G, W, U);
     asm volatile("griddepcontrol.wait;" ::: "memory");
 
     // Plans: `cur` is the unit being computed, `nxt` the next one (its loads are
     // issued during `cur`), `raw` the metadata of the one after.
-    int unit = blockIdx.x;
+    int unit = blockIdx.x;  // launch unit
     UnitPlan cur, nxt;
     RawMeta raw;
     cur.skip = true;
     nxt.skip = true;
-    if (unit < U) cur = plan_unit<MODE>(p, unit, load_unit_meta<MODE, RAGGED>(p, unit, U));
-    if (unit + G < U) nxt = plan_unit<MODE>(p, unit + G, load_unit_meta<MODE, RAGGED>(p, unit + G, U));
-    raw = load_unit_meta<MODE, RAGGED>(p, unit + 2 * G, U);
+    if (unit < W)
+        cur = plan_unit<MODE, NL>(L, unit, U, load_unit_meta<MODE, RAGGED, NL>(p, unit, W, U));
+    if (unit + G < W)
+        nxt = plan_unit<MODE, NL>(L, unit + G, U, load_unit_meta<MODE, RAGGED, NL>(p, unit + G, W, U));
+    raw = load_unit_meta<MODE, RAGGED, NL>(p, unit + 2 * G, W, U);
 
     // Unit k (in the order this block computes them) uses token buffer k & 1.
     // Its token boxes go out when unit k-1 starts (that buffer was last used by
@@ -424,10 +446,10 @@ __global__ void __launch_bounds__(32 * NW, kBlocksPerSM)
     int tok_issued = 0;  // units whose token load was issued
     int processed = 0;   // units computed
     if (tid == 0 && !cur.skip) {
-        issue_tokens<MODE>(maps, cur, sm.tok[0], smem_u32(&ax.tok_full[0]));
-        issue_tile(maps, p, cur, sm.tile, tile_bar);
+        issue_tokens<MODE>(L.maps[cur.layer], cur, sm.tok[0], smem_u32(&ax.tok_full[0]));
+        issue_tile(L.maps[cur.layer], cur, sm.tile, tile_bar);
     }
-    if (tid == 0 && !nxt.skip) prefetch_unit<MODE>(maps, p, nxt);
+    if (tid == 0 && !nxt.skip) prefetch_unit<MODE>(L.maps[nxt.layer], nxt);
     if (!cur.skip) {
         ++issued;
         ++tok_issued;
@@ -435,31 +457,32 @@ __global__ void __launch_bounds__(32 * NW, kBlocksPerSM)
     // Gates of the current unit: thread t < 16 holds alpha_t, beta_t, loaded
     // unconditionally from a clamped (always valid) row; rows t >= T are
     // replaced by alpha = 1, beta = 0 where the values are used.
-    float ga = gate_load(p.alpha, p, cur, tid), gb = gate_load(p.beta, p, cur, tid);
+    float ga = gate_load(L.a[cur.layer].alpha, p, cur, tid);
+    float gb = gate_load(L.a[cur.layer].beta, p, cur, tid);
 
     bool aborted = false;
-    for (; unit < U; unit += G) {
+    for (; unit < W; unit += G) {
         // Advance the metadata pipeline.
         const UnitPlan me = cur;
         cur = nxt;
         nxt.skip = true;
-        if (unit + 2 * G < U) nxt = plan_unit<MODE>(p, unit + 2 * G, raw);
-        raw = load_unit_meta<MODE, RAGGED>(p, unit + 3 * G, U);
+        if (unit + 2 * G < W) nxt = plan_unit<MODE, NL>(L, unit + 2 * G, U, raw);
+        raw = load_unit_meta<MODE, RAGGED, NL>(p, unit + 3 * G, W, U);
         if (me.skip) {
             // Gates of the next unit (consumed one iteration later).
-            ga = gate_load(p.alpha, p, cur, tid);
-            gb = gate_load(p.beta, p, cur, tid);
+            ga = gate_load(L.a[cur.layer].alpha, p, cur, tid);
+            gb = gate_load(L.a[cur.layer].beta, p, cur, tid);
             if (!cur.skip && issued == processed) {
                 // Nothing is in flight: the next unit's loads can all go now.
                 if (tid == 0) {
-                    issue_tokens<MODE>(maps, cur, sm.tok[tok_issued & 1],
+                    issue_tokens<MODE>(L.maps[cur.layer], cur, sm.tok[tok_issued & 1],
                                        smem_u32(&ax.tok_full[tok_issued & 1]));
-                    issue_tile(maps, p, cur, sm.tile, tile_bar);
+                    issue_tile(L.maps[cur.layer], cur, sm.tile, tile_bar);
                 }
                 ++issued;
                 ++tok_issued;
             }
-            if (tid == 0 && !nxt.skip) prefetch_unit<MODE>(maps, p, nxt);
+            if (tid == 0 && !nxt.skip) prefetch_unit<MODE>(L.maps[nxt.layer], nxt);
             continue;
         }
         const int T = me.teff;
@@ -477,7 +500,7 @@ __global__ void __launch_bounds__(32 * NW, kBlocksPerSM)
         // The next unit's token block goes into the other buffer now.
         if (!cur.skip && tok_issued == processed + 1) {
             if (tid == 0)
-                issue_tokens<MODE>(maps, cur, sm.tok[tok_issued & 1],
+                issue_tokens<MODE>(L.maps[cur.layer], cur, sm.tok[tok_issued & 1],
                                    smem_u32(&ax.tok_full[tok_issued & 1]));
             ++tok_issued;
         }
@@ -487,8 +510,8 @@ __global__ void __launch_bounds__(32 * NW, kBlocksPerSM)
         }
         // Gates of the next unit, loaded straight into the registers just freed
         // (consumed one iteration later, so this load is never waited on here).
-        ga = gate_load(p.alpha, p, cur, tid);
-        gb = gate_load(p.beta, p, cur, tid);
+        ga = gate_load(L.a[cur.layer].alpha, p, cur, tid);
+        gb = gate_load(L.a[cur.layer].beta, p, cur, tid);
         if (!wait_parity(smem_u32(&ax.tok_full[buf]), (processed >> 1) & 1)) ax.abort_flag = 1;
         __syncthreads();
         if (ax.abort_flag) {
@@ -633,10 +656,10 @@ __global__ void __launch_bounds__(32 * NW, kBlocksPerSM)
         // and thread 0 sends the next unit's tile.
         __syncthreads();
         if (!keep_tile && !cur.skip) {
-            if (tid == 0) issue_tile(maps, p, cur, sm.tile, tile_bar);
+            if (tid == 0) issue_tile(L.maps[cur.layer], cur, sm.tile, tile_bar);
             ++issued;
         }
-        if (tid == 0 && !nxt.skip) prefetch_unit<MODE>(maps, p, nxt);
+        if (tid == 0 && !nxt.skip) prefetch_unit<MODE>(L.maps[nxt.layer], nxt);
 
         // Token indices of this thread in the fragments: n-tile half ntt, element e:
         //   t = 8 ntt + 2c + (e & 1);   column = col0 + 2m + (e >> 1).
@@ -694,7 +717,7 @@ __global__ void __launch_bounds__(32 * NW, kBlocksPerSM)
                 split2(mr[2 * c], mr[2 * c + 1], bh[nt][0], bl[nt][0]);
                 split2(mr[2 * c + 8], mr[2 * c + 9], bh[nt][1], bl[nt][1]);
             }
-            float *go = p.o + ((size_t)me.u.row0 * p.H + me.h) * D + col0;
+            float *go = L.a[me.layer].o + ((size_t)me.u.row0 * p.H + me.h) * D + col0;
 #pragma unroll
             for (int m = 0; m < MT; ++m) {
                 uint32_t ah[4], al[4];
@@ -786,7 +809,7 @@ __global__ void __launch_bounds__(32 * NW, kBlocksPerSM)
             // The commit has read the tile: the stage is free now.
             __syncthreads();
             if (!cur.skip) {
-                if (tid == 0) issue_tile(maps, p, cur, sm.tile, tile_bar);
+                if (tid == 0) issue_tile(L.maps[cur.layer], cur, sm.tile, tile_bar);
                 ++issued;
             }
         }
@@ -800,7 +823,9 @@ __global__ void __launch_bounds__(32 * NW, kBlocksPerSM)
             ok = wait_parity(smem_u32(&ax.tok_full[k & 1]), (k >> 1) & 1) && ok;
         if (!ok) aborted = true;
     }
-    if (tid == 0 && aborted && p.dev_err) atomicOr(p.dev_err, GDN_DEVERR_TIMEOUT);
+    if (tid == 0 && aborted)
+        for (int l = 0; l < (NL == 1 ? 1 : L.n); ++l)
+            if (L.a[l].dev_err) atomicOr(L.a[l].dev_err, GDN_DEVERR_TIMEOUT);
 }
 
 // ------------------------------------------------------------ host side
@@ -837,21 +862,17 @@ constexpr int kMaxDevices = 64;
 
 struct DeviceInfo {
     int sms = 0;
-    bool smem_set[3][2] = {{false, false}, {false, false}, {false, false}};
+    bool smem_set[3][2][2] = {};  // [mode][ragged][batched]
 };
 
 DeviceInfo g_dev[kMaxDevices];
 std::mutex g_dev_mutex;
 
-// Warps per block for each mode.
-template <int MODE>
-struct ModeWarps {
-    static constexpr int NW = 4;
-};
+constexpr int NW = 4;  // warps per block
+static_assert(sizeof(Launch<kChunkMaxLayers>) <= 32764, "kernel parameter space");
 
-template <int MODE, bool RAGGED>
-cudaError_t launch_mode(const Args &p, const Maps &maps, cudaStream_t stream) {
-    constexpr int NW = ModeWarps<MODE>::NW;
+template <int MODE, bool RAGGED, int NL>
+cudaError_t launch_mode(const Launch<NL> &L, cudaStream_t stream) {
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
@@ -864,17 +885,17 @@ cudaError_t launch_mode(const Args &p, const Maps &maps, cudaStream_t stream) {
             e = cudaDeviceGetAttribute(&info.sms, cudaDevAttrMultiProcessorCount, dev);
             if (e != cudaSuccess) return e;
         }
-        if (!info.smem_set[MODE][RAGGED]) {
-            e = cudaFuncSetAttribute(chunk_kernel<MODE, NW, RAGGED>,
+        if (!info.smem_set[MODE][RAGGED][NL != 1]) {
+            e = cudaFuncSetAttribute(chunk_kernel<MODE, NW, RAGGED, NL>,
                                      cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
             if (e != cudaSuccess) return e;
-            info.smem_set[MODE][RAGGED] = true;
+            info.smem_set[MODE][RAGGED][NL != 1] = true;
         }
         sms = info.sms;
     }
-    const int units = p.B * p.H;
+    const long long units = (long long)L.a[0].B * L.a[0].H * L.n;
     const int slots = kBlocksPerSM * sms;
-    const int grid = units < slots ? units : slots;
+    const int grid = units < slots ? (int)units : slots;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)grid);
     cfg.blockDim = dim3((unsigned)Cfg<NW>::kThreads);
@@ -885,7 +906,53 @@ cudaError_t launch_mode(const Args &p, const Maps &maps, cudaStream_t stream) {
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, chunk_kernel<MODE, NW, RAGGED>, p, maps);
+    return cudaLaunchKernelEx(&cfg, chunk_kernel<MODE, NW, RAGGED, NL>, L);
+}
+
+// The pool and token tensor maps of one layer.
+cudaError_t encode_layer(const Args &p, Maps *maps) {
+    const unsigned long long tiles = (unsigned long long)p.pool_slots * (unsigned long long)p.H;
+    if (tiles == 0 || tiles > (1ull << 31) || p.n_tok < 1 || p.n_tok > (1ll << 31))
+        return cudaErrorInvalidValue;
+    PFN_cuTensorMapEncodeTiled_v12000 encode = encode_fn();
+    if (!encode) return cudaErrorNotSupported;
+    // The pool as a 3-D tensor: value column (contiguous), key row, slot * H + head.
+    const cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)D, (cuuint64_t)tiles};
+    const cuuint64_t strides[2] = {(cuuint64_t)D * 4, (cuuint64_t)D * D * 4};
+    const cuuint32_t box[3] = {32, (cuuint32_t)D, 1};
+    const cuuint32_t elem[3] = {1, 1, 1};
+    if (encode(&maps->pool, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, p.pool, dims, strides, box, elem,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+        return cudaErrorInvalidValue;
+    if (!encode_tokens(encode, &maps->k, p.k, p.H, p.n_tok) ||
+        !encode_tokens(encode, &maps->v, p.v, p.H, p.n_tok) ||
+        !encode_tokens(encode, &maps->q, p.q, p.H, p.n_tok))
+        return cudaErrorInvalidValue;
+    return cudaSuccess;
+}
+
+template <int NL>
+cudaError_t launch_layers(const Args *layers, int n, int mode, cudaStream_t stream) {
+    Launch<NL> L = {};
+    L.n = n;
+    for (int l = 0; l < n; ++l) {
+        L.a[l] = layers[l];
+        const cudaError_t e = encode_layer(layers[l], &L.maps[l]);
+        if (e != cudaSuccess) return e;
+    }
+    const bool ragged = layers[0].cu_seqlens != nullptr;
+    switch (mode) {
+        case kVerify:
+            return ragged ? launch_mode<kVerify, true, NL>(L, stream)
+                          : launch_mode<kVerify, false, NL>(L, stream);
+        case kCommit:
+            return ragged ? launch_mode<kCommit, true, NL>(L, stream)
+                          : launch_mode<kCommit, false, NL>(L, stream);
+        default:
+            return ragged ? launch_mode<kFused, true, NL>(L, stream)
+                          : launch_mode<kFused, false, NL>(L, stream);
+    }
 }
 
 }  // namespace
@@ -896,38 +963,14 @@ bool chunk_supported(bool bf16, int dk, int dv, int max_T) {
 
 bool chunk_preferred(int max_T) { return max_T >= 1; }
 
-cudaError_t launch_chunk(const Args &p, int mode, cudaStream_t stream) {
-    const unsigned long long tiles = (unsigned long long)p.pool_slots * (unsigned long long)p.H;
-    if (tiles == 0 || tiles > (1ull << 31) || p.n_tok < 1 || p.n_tok > (1ll << 31))
-        return cudaErrorInvalidValue;
-    PFN_cuTensorMapEncodeTiled_v12000 encode = encode_fn();
-    if (!encode) return cudaErrorNotSupported;
-    Maps maps;
-    // The pool as a 3-D tensor: value column (contiguous), key row, slot * H + head.
-    const cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)D, (cuuint64_t)tiles};
-    const cuuint64_t strides[2] = {(cuuint64_t)D * 4, (cuuint64_t)D * D * 4};
-    const cuuint32_t box[3] = {32, (cuuint32_t)D, 1};
-    const cuuint32_t elem[3] = {1, 1, 1};
-    if (encode(&maps.pool, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, p.pool, dims, strides, box, elem,
-               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
-        return cudaErrorInvalidValue;
-    if (!encode_tokens(encode, &maps.k, p.k, p.H, p.n_tok) ||
-        !encode_tokens(encode, &maps.v, p.v, p.H, p.n_tok) ||
-        !encode_tokens(encode, &maps.q, p.q, p.H, p.n_tok))
-        return cudaErrorInvalidValue;
-    const bool ragged = p.cu_seqlens != nullptr;
-    switch (mode) {
-        case kVerify:
-            return ragged ? launch_mode<kVerify, true>(p, maps, stream)
-                          : launch_mode<kVerify, false>(p, maps, stream);
-        case kCommit:
-            return ragged ? launch_mode<kCommit, true>(p, maps, stream)
-                          : launch_mode<kCommit, false>(p, maps, stream);
-        default:
-            return ragged ? launch_mode<kFused, true>(p, maps, stream)
-                          : launch_mode<kFused, false>(p, maps, stream);
+cudaError_t launch_chunk(const Args *layers, int n, int mode, cudaStream_t stream) {
+    for (int l0 = 0; l0 < n; l0 += kChunkMaxLayers) {
+        const int m = n - l0 < kChunkMaxLayers ? n - l0 : kChunkMaxLayers;
+        const cudaError_t e = m == 1 ? launch_layers<1>(layers + l0, 1, mode, stream)
+                                     : launch_layers<kChunkMaxLayers>(layers + l0, m, mode, stream);
+        if (e != cudaSuccess) return e;
     }
+    return cudaSuccess;
 }
 
 }  // namespace gdn

@@ -11,9 +11,12 @@ namespace gdn {
 // multiple of 128 up to 256; q/k/v bf16 or fp32; any max_T.
 cudaError_t launch_recurrent(const Args &p, int mode, bool bf16, cudaStream_t stream);
 
-// Chunked tensor-core kernel and its applicability.
+// Chunked tensor-core kernel and its applicability.  One call covers n
+// problems (layers) that share every request-level field; up to
+// kChunkMaxLayers of them run in one launch, more are split into several.
+constexpr int kChunkMaxLayers = 32;
 bool chunk_supported(bool bf16, int dk, int dv, int max_T);
 bool chunk_preferred(int max_T);
-cudaError_t launch_chunk(const Args &p, int mode, cudaStream_t stream);
+cudaError_t launch_chunk(const Args *layers, int n, int mode, cudaStream_t stream);
 
 }  // namespace gdn

@@ -63,10 +63,14 @@ class DeviceProblem:
         place_checkpoints(self.pool, prob)
         self.dev_err = torch.zeros(1, dtype=torch.int32, device=dev) if with_dev_err else None
         self.o = torch.zeros((prob.n_tok, prob.heads, prob.dv), dtype=torch.float32, device=dev)
-        self.c = binding.make_problem(q=self.q, k=self.k, v=self.v, alpha=self.alpha,
-                                      beta=self.beta, pool=self.pool, slot_ids=self.slot_ids,
-                                      max_T=prob.max_T, cu_seqlens=self.cu_seqlens,
-                                      dev_err=self.dev_err, algo=algo)
+        self.algo = algo
+        self.c = self._make_c()
+
+    def _make_c(self) -> binding.Problem:
+        return binding.make_problem(q=self.q, k=self.k, v=self.v, alpha=self.alpha,
+                                    beta=self.beta, pool=self.pool, slot_ids=self.slot_ids,
+                                    max_T=self.host.max_T, cu_seqlens=self.cu_seqlens,
+                                    dev_err=self.dev_err, algo=self.algo)
 
     def verify(self, stream=None):
         binding.gdn_verify(self.c, self.o, stream)
@@ -93,3 +97,36 @@ class DeviceProblem:
             if st != binding.GDN_OK:
                 raise binding.GdnError(st, f"gdn {mode}")
         return call
+
+
+def share_request_arrays(dps) -> None:
+    """Point every layer at the first layer's slot_ids, accepted and cu_seqlens
+    device arrays (one step's requests are the same in every layer), as the
+    layer-batch calls require.  The values must already be equal."""
+    d0 = dps[0]
+    for d in dps[1:]:
+        for name in ("slot_ids", "accepted"):
+            if not torch.equal(getattr(d, name), getattr(d0, name)):
+                raise ValueError(f"layers disagree on {name}")
+        d.slot_ids, d.accepted, d.cu_seqlens = d0.slot_ids, d0.accepted, d0.cu_seqlens
+        d.c = d._make_c()
+
+
+def layers_launcher(dps, mode: str, stream):
+    """A zero-argument callable issuing one layer-batch call (verify, commit or
+    fused) over all of `dps` on `stream`, every argument marshalled in advance."""
+    lib = binding.lib()
+    arr = binding.ProblemArray([d.c for d in dps])
+    o = binding._ptr_array([d.o for d in dps])
+    s = binding._stream(stream)
+    acc = dps[0].accepted.data_ptr()
+    fn = {"verify": lambda: lib.gdn_verify_layers(arr.ref, arr.n, o, s),
+          "commit": lambda: lib.gdn_commit_layers(arr.ref, arr.n, acc, s),
+          "fused": lambda: lib.gdn_verify_commit_fused_layers(arr.ref, arr.n, acc, o, s)}[mode]
+
+    def call():
+        st = fn()
+        if st != binding.GDN_OK:
+            raise binding.GdnError(st, f"gdn {mode} layers")
+    call.keep = (arr, o)
+    return call

@@ -132,7 +132,78 @@ def test_select_algo(lib):
 
 
 def test_status_strings(lib):
-    for s in range(9):
+    for s in range(10):
         assert binding.gdn_status_string(s)
     assert binding.gdn_version().count(".") == 2
     assert binding.gdn_last_error_string() == ""
+
+
+# ---------------------------------------------------------------- layer batches
+
+def fake_layers(n, **over_last):
+    """n problems that share the request-level fields and each own their arrays
+    (disjoint fake addresses); overrides apply to the last one."""
+    arr = (binding.gdn_problem * n)()
+    for l in range(n):
+        c = fake_problem()
+        off = (l + 1) << 36
+        c.q, c.k, c.v, c.alpha, c.beta, c.pool = (x + off for x in (c.q, c.k, c.v, c.alpha,
+                                                                      c.beta, c.pool))
+        arr[l] = c
+    for k, v in over_last.items():
+        setattr(arr[n - 1], k, v)
+    return arr
+
+
+def o_array(n, **set_at):
+    arr = (ctypes.c_void_p * n)(*[O_PTR + ((l + 1) << 36) for l in range(n)])
+    for i, v in set_at.items():
+        arr[int(i[1:])] = v
+    return arr
+
+
+def call_layers(lib, fn, arr, n, o=None, acc=ACC_PTR):
+    o = o_array(max(n, 1)) if o is None else o
+    P = ctypes.cast(arr, ctypes.POINTER(binding.gdn_problem)) if arr is not None else None
+    if fn == "verify":
+        return lib.gdn_verify_layers(P, n, o, None)
+    if fn == "commit":
+        return lib.gdn_commit_layers(P, n, acc, None)
+    return lib.gdn_verify_commit_fused_layers(P, n, acc, o, None)
+
+
+@pytest.mark.parametrize("fn", ["verify", "commit", "fused"])
+def test_layers_empty_and_null(lib, fn):
+    assert call_layers(lib, fn, fake_layers(2), 0) == 0
+    assert call_layers(lib, fn, fake_layers(2), -1) == 2
+    assert call_layers(lib, fn, None, 2) == 1
+    P = ctypes.cast(fake_layers(2), ctypes.POINTER(binding.gdn_problem))
+    if fn == "verify":
+        assert lib.gdn_verify_layers(P, 2, None, None) == 1           # no o array
+    elif fn == "commit":
+        assert lib.gdn_commit_layers(P, 2, None, None) == 1           # no accepted
+    else:
+        assert lib.gdn_verify_commit_fused_layers(P, 2, ACC_PTR, None, None) == 1
+
+
+@pytest.mark.parametrize("fn", ["verify", "commit", "fused"])
+@pytest.mark.parametrize("over,status", [
+    (dict(heads=0), 2),                                  # a single-problem check on layer 2
+    (dict(q=(1 << 40) + 8), 7),
+    (dict(batch=1), 9), (dict(max_T=4), 9), (dict(pool_slots=16), 9),
+    (dict(slot_ids=(1 << 40) + 6 * (1 << 32) + 64), 9), (dict(algo=1), 9),
+    (dict(cu_seqlens=(1 << 40) + 11 * (1 << 32)), 9),
+])
+def test_layers_reject(lib, fn, over, status):
+    assert call_layers(lib, fn, fake_layers(3, **over), 3) == status
+
+
+def test_layers_cross_layer_aliasing(lib):
+    # a layer's output over another layer's input or output
+    arr = fake_layers(2)
+    assert call_layers(lib, "verify", arr, 2, o=o_array(2, o1=arr[0].q)) == 8
+    assert call_layers(lib, "fused", arr, 2, o=o_array(2, o1=arr[0].pool)) == 8
+    assert call_layers(lib, "verify", arr, 2, o=o_array(2, o1=O_PTR + (1 << 36))) == 8
+    # a committed pool over another layer's pool or tokens
+    assert call_layers(lib, "commit", fake_layers(2, pool=fake_layers(1)[0].pool), 2) == 8
+    assert call_layers(lib, "fused", fake_layers(2, pool=fake_layers(1)[0].k), 2) == 8
