@@ -13,7 +13,10 @@ state after a_r tokens; a request with a_r = 0 leaves its slot untouched
 (ReplaySSM keeps the accepted prefix and rolls the rest back, OCRia write-up,
 section "Make speculative verification cheaper").
 
-Parity unpinned: none.  Every function here is pinned by `tests/test_oracle_pins.py`.
+The greedy accept-length rule lives in `accept.py` (pure Python loops).
+
+Parity unpinned: none.  Every function here is pinned by `tests/test_oracle_pins.py`
+and `tests/test_accept_oracle.py`.
 """
 from __future__ import annotations
 
@@ -25,6 +28,8 @@ from concurrent.futures import ThreadPoolExecutor
 from typing import Optional, Sequence
 
 import numpy as np
+
+from .accept import accept_prefix  # noqa: F401  (greedy accept length)
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 _SRC = os.path.join(_HERE, "gdn_oracle.c")
