@@ -44,7 +44,8 @@ METRIC = "us per layer-call (verify+commit) and achieved HBM GB/s vs ~8 TB/s, 1x
 UNIT = "us/layer-call"
 NOMINAL_HBM_GBS = 8000.0
 MODE_NAME = {"v": "verify", "c": "commit", "f": "fused",
-             "C": "commit_layers", "F": "fused_layers"}  # upper case: one launch, all layers
+             "C": "commit_layers", "F": "fused_layers",  # upper case: one launch, all layers
+             "a": "accept"}
 
 
 # ----------------------------------------------------------------- accounting
@@ -268,6 +269,19 @@ def run_ours(args, rank, world, local_rank):
         else:
             order = [(d, m) for d in dps for m in kinds]
         calls = [(m, d.launcher(MODE_NAME[m], stream)) for d, m in order]
+    if args.with_accept:
+        # The step starts with the greedy accepted lengths computed on the device
+        # from token ids (one call for all layers), as an engine would.
+        draft, target = inputs.make_token_ids(p0, seed=5)
+        ids = [torch.from_numpy(x).to(dev) for x in (draft, target)]
+        d0 = dps[0]
+
+        def accept_call():
+            binding.gdn_accept_prefix(ids[0], ids[1], d0.accepted, p0.max_T,
+                                      cu_seqlens=d0.cu_seqlens, dev_err=d0.dev_err, stream=stream)
+        kinds = ["a"] + kinds
+        calls = [("a", accept_call)] + calls
+        bytes_of["a"] = [2 * 4 * p0.n_tok + 4 * p0.batch + (4 * (p0.batch + 1) if p0.ragged else 0)]
     bytes_call = sum(sum(bytes_of[m]) for m in kinds) / L
 
     def step(events=None):
@@ -362,6 +376,8 @@ def run_ours(args, rank, world, local_rank):
                           "all verifies then all commits"),
                 "l2": "inputs larger than L2 (each step touches ~%.1f GB)" % (bytes_call * L / 1e9),
                 "algo": {1: "recurrent", 2: "chunk"}.get(algo_used, str(algo_used)),
+                "accepted": ("greedy prefix match of token ids on the device, every step"
+                             if args.with_accept else "given (device array)"),
             },
             "achieved_gbs": gbs,
             "frac_of_8tbs": gbs / NOMINAL_HBM_GBS,
@@ -452,6 +468,8 @@ def main():
     ap.add_argument("--ref-units", type=int, default=64)
     ap.add_argument("--e2e-steps", type=int, default=20)
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--with-accept", action="store_true",
+                    help="start every step with the on-device greedy accept-length call")
     ap.add_argument("--batch-layers", action="store_true",
                     help="all layers' commits (or fused calls) in one layer-batch launch")
     ap.add_argument("--no-cpu-baseline", action="store_true")

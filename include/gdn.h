@@ -160,6 +160,28 @@ GDN_API gdn_status gdn_verify_commit_fused_layers(const gdn_problem *problems, i
                                                   const int32_t *accepted, float *const *o,
                                                   cudaStream_t stream);
 
+/* Greedy accepted lengths on the device, so that the commit needs no host round
+ * trip: accepted[r] = the largest a in [0, T_r] such that
+ *     draft_ids[c_r + t] == target_ids[c_r + t]   for every t < a,
+ * with c_r, T_r the token rows of request r as for gdn_problem (cu_seqlens, or
+ * r * max_T and max_T when cu_seqlens is NULL).  Speculative decoding keeps the
+ * draft tokens that agree with the target model and rolls back to that prefix
+ * (OCRia write-up, sections "Generate more tokens per target pass: speculative
+ * decoding" and "Make speculative verification cheaper"); this is the greedy
+ * form of that check.  The caller lines up both arrays so that row c_r + t
+ * holds the draft id of the token fed at that row and the target's own choice
+ * for it (a row that is always kept is passed with equal ids).
+ *
+ * draft_ids, target_ids: device int32 [n_tok] (uniform: batch * max_T rows);
+ * accepted: device int32 [batch], written; it must not overlap the other
+ * arrays.  A ragged request whose rows leave [0, n_tok) or whose length
+ * leaves [0, max_T] sets GDN_DEVERR_SEQLEN in *dev_err and its accepted[r] is
+ * not written.  batch = 0 launches nothing.  All pointers 4-byte aligned. */
+GDN_API gdn_status gdn_accept_prefix(int32_t batch, int32_t max_T, const int32_t *cu_seqlens,
+                                     int64_t n_tok, const int32_t *draft_ids,
+                                     const int32_t *target_ids, int32_t *accepted,
+                                     int32_t *dev_err, cudaStream_t stream);
+
 /* Waits for `stream`, copies *p->dev_err to *host_code (0 when dev_err is NULL).
  * Returns GDN_ERR_DEVICE_ARG when the word is non-zero, GDN_OK when it is zero. */
 GDN_API gdn_status gdn_read_device_error(const gdn_problem *p, cudaStream_t stream,

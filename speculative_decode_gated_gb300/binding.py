@@ -28,7 +28,7 @@ GDN_MAX_T = 1024
 EXPORTED = (
     "gdn_verify", "gdn_commit", "gdn_verify_commit_fused",
     "gdn_verify_layers", "gdn_commit_layers", "gdn_verify_commit_fused_layers",
-    "gdn_read_device_error", "gdn_select_algo", "gdn_status_string", "gdn_last_error_string",
+    "gdn_accept_prefix", "gdn_read_device_error", "gdn_select_algo", "gdn_status_string", "gdn_last_error_string",
     "gdn_version",
 )
 
@@ -76,12 +76,13 @@ def lib() -> ctypes.CDLL:
         h.gdn_verify_layers.argtypes = [P, I32, S, S]
         h.gdn_commit_layers.argtypes = [P, I32, S, S]
         h.gdn_verify_commit_fused_layers.argtypes = [P, I32, S, S, S]
+        h.gdn_accept_prefix.argtypes = [I32, I32, S, ctypes.c_int64, S, S, S, S, S]
         h.gdn_read_device_error.argtypes = [P, S, ctypes.POINTER(ctypes.c_int32)]
         h.gdn_select_algo.argtypes = [P]
         h.gdn_status_string.argtypes = [ctypes.c_int]
         for name in ("gdn_verify", "gdn_commit", "gdn_verify_commit_fused",
                      "gdn_verify_layers", "gdn_commit_layers", "gdn_verify_commit_fused_layers",
-                     "gdn_read_device_error", "gdn_select_algo"):
+                     "gdn_accept_prefix", "gdn_read_device_error", "gdn_select_algo"):
             getattr(h, name).restype = ctypes.c_int
         for name in ("gdn_status_string", "gdn_last_error_string", "gdn_version"):
             getattr(h, name).restype = ctypes.c_char_p
@@ -230,6 +231,22 @@ def gdn_verify_commit_fused_layers(probs: ProblemArray, accepted: torch.Tensor, 
     _raise(lib().gdn_verify_commit_fused_layers(probs.ref, probs.n, _ptr(accepted), arr,
                                                 _stream(stream)),
            "gdn_verify_commit_fused_layers")
+
+
+def gdn_accept_prefix(draft_ids: torch.Tensor, target_ids: torch.Tensor, accepted: torch.Tensor,
+                      max_T: int, cu_seqlens: Optional[torch.Tensor] = None,
+                      dev_err: Optional[torch.Tensor] = None, stream=None) -> None:
+    """accepted[r] <- greedy accepted length of request r (int32 tensors on one device;
+    draft_ids/target_ids [N_tok], accepted [B], cu_seqlens [B+1] or None)."""
+    dev = accepted.device
+    for t, n in ((draft_ids, "draft_ids"), (target_ids, "target_ids"), (accepted, "accepted"),
+                 (cu_seqlens, "cu_seqlens"), (dev_err, "dev_err")):
+        _check(t, n, (torch.int32,), dev)
+    batch = accepted.numel()
+    st = lib().gdn_accept_prefix(batch, int(max_T), _ptr(cu_seqlens), draft_ids.numel(),
+                                 _ptr(draft_ids), _ptr(target_ids), _ptr(accepted), _ptr(dev_err),
+                                 _stream(stream))
+    _raise(st, "gdn_accept_prefix")
 
 
 def gdn_read_device_error(prob: Problem, stream=None) -> int:

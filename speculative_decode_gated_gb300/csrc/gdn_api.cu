@@ -269,6 +269,33 @@ gdn_status gdn_verify_commit_fused_layers(const gdn_problem *problems, int32_t n
     return run_layers(problems, n_layers, gdn::kFused, accepted, o, stream);
 }
 
+gdn_status gdn_accept_prefix(int32_t batch, int32_t max_T, const int32_t *cu_seqlens,
+                             int64_t n_tok, const int32_t *draft_ids, const int32_t *target_ids,
+                             int32_t *accepted, int32_t *dev_err, cudaStream_t stream) {
+    if (batch < 0 || max_T < 0 || max_T > GDN_MAX_T) return GDN_ERR_BAD_DIM;
+    if (batch == 0) return GDN_OK;
+    if (cu_seqlens && n_tok < 0) return GDN_ERR_BAD_DIM;
+    if (!accepted) return GDN_ERR_NULL_PTR;
+    const int64_t rows = cu_seqlens ? n_tok : (int64_t)batch * max_T;
+    if (rows > 0 && (!draft_ids || !target_ids)) return GDN_ERR_NULL_PTR;
+    if (!aligned4(cu_seqlens) || !aligned4(draft_ids) || !aligned4(target_ids) ||
+        !aligned4(accepted) || !aligned4(dev_err))
+        return GDN_ERR_ALIGN;
+    const Range ra = range(accepted, (int64_t)batch * 4);
+    const Range ins[] = {range(draft_ids, rows * 4), range(target_ids, rows * 4),
+                         range(cu_seqlens, cu_seqlens ? ((int64_t)batch + 1) * 4 : 0),
+                         range(dev_err, dev_err ? 4 : 0)};
+    for (const Range &x : ins)
+        if (overlap(ra, x)) return GDN_ERR_ALIAS;
+    const cudaError_t e = gdn::launch_accept(batch, max_T, cu_seqlens, n_tok, draft_ids,
+                                             target_ids, accepted, dev_err, stream);
+    if (e != cudaSuccess) {
+        set_cuda_error(e, "kernel launch");
+        return GDN_ERR_CUDA;
+    }
+    return GDN_OK;
+}
+
 gdn_status gdn_read_device_error(const gdn_problem *p, cudaStream_t stream, int32_t *host_code) {
     if (!p || !host_code) return GDN_ERR_NULL_PTR;
     *host_code = 0;

@@ -19,4 +19,9 @@ bool chunk_supported(bool bf16, int dk, int dv, int max_T);
 bool chunk_preferred(int max_T);
 cudaError_t launch_chunk(const Args *layers, int n, int mode, cudaStream_t stream);
 
+// Greedy accepted lengths (arguments already validated on the host).
+cudaError_t launch_accept(int B, int max_T, const int32_t *cu_seqlens, long long n_tok,
+                          const int32_t *draft, const int32_t *target, int32_t *accepted,
+                          int32_t *dev_err, cudaStream_t stream);
+
 }  // namespace gdn

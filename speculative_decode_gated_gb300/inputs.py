@@ -36,6 +36,8 @@ __all__ = [
     "make_problem",
     "make_custom",
     "make_layers",
+    "make_token_ids",
+    "random_token_ids",
     "POOL_SENTINEL_BITS",
 ]
 
@@ -207,3 +209,34 @@ def make_layers(name: str) -> List[Problem]:
     """Every layer of a workload (one element for single-layer workloads)."""
     n = WORKLOADS[name].get("layers", 1)
     return [make_problem(name, layer=l) for l in range(n)]
+
+
+def make_token_ids(prob: Problem, seed: int = 0, vocab: int = 151936):
+    """Draft and target token ids (int32 [N_tok] each) whose greedy prefix match
+    gives back the problem's accepted lengths: in request r the ids agree at
+    rows t < a_r, differ at row a_r (when a_r < T_r) and are drawn
+    independently after it (so they may agree again there)."""
+    rng = np.random.default_rng(np.random.SeedSequence([seed, 77]))
+    n = prob.n_tok
+    draft = rng.integers(0, vocab, size=n).astype(np.int64)
+    target = rng.integers(0, vocab, size=n).astype(np.int64)
+    for r in range(prob.batch):
+        c0, T, a = int(prob.cu_seqlens[r]), int(prob.lengths[r]), int(prob.accepted[r])
+        target[c0:c0 + a] = draft[c0:c0 + a]
+        if a < T:
+            target[c0 + a] = (draft[c0 + a] + 1 + rng.integers(0, vocab - 1)) % vocab
+    return draft.astype(np.int32), target.astype(np.int32)
+
+
+def random_token_ids(lengths: Sequence[int], seed: int, p_differ: float = 0.1, vocab: int = 50):
+    """cu_seqlens and draft/target ids where each row's target differs from the
+    draft with probability p_differ (independently per row)."""
+    rng = np.random.default_rng(np.random.SeedSequence([seed, 78]))
+    lens = np.asarray(lengths, dtype=np.int64)
+    cu = np.zeros(len(lens) + 1, dtype=np.int32)
+    cu[1:] = np.cumsum(lens)
+    n = int(cu[-1])
+    draft = rng.integers(0, vocab, size=n)
+    differ = rng.random(n) < p_differ
+    target = np.where(differ, (draft + 1 + rng.integers(0, vocab - 1, size=n)) % vocab, draft)
+    return cu, draft.astype(np.int32), target.astype(np.int32)

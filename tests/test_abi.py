@@ -207,3 +207,25 @@ def test_layers_cross_layer_aliasing(lib):
     # a committed pool over another layer's pool or tokens
     assert call_layers(lib, "commit", fake_layers(2, pool=fake_layers(1)[0].pool), 2) == 8
     assert call_layers(lib, "fused", fake_layers(2, pool=fake_layers(1)[0].k), 2) == 8
+
+
+# ---------------------------------------------------------------- accept length
+
+def call_accept(lib, batch=4, max_T=8, cu=None, n_tok=32, draft=(1 << 40), target=(1 << 40) + (1 << 32),
+                acc=ACC_PTR, err=None):
+    return lib.gdn_accept_prefix(batch, max_T, cu, n_tok, draft, target, acc, err, None)
+
+
+def test_accept_prefix_validation(lib):
+    assert call_accept(lib, batch=0, acc=None, draft=None, target=None) == 0  # nothing to do
+    assert call_accept(lib, batch=-1) == 2
+    assert call_accept(lib, max_T=1025) == 2
+    assert call_accept(lib, max_T=-1) == 2
+    assert call_accept(lib, cu=(1 << 40) + 11 * (1 << 32), n_tok=-1) == 2
+    assert call_accept(lib, acc=None) == 1
+    assert call_accept(lib, draft=None) == 1
+    assert call_accept(lib, target=None) == 1
+    assert call_accept(lib, acc=ACC_PTR + 2) == 7
+    assert call_accept(lib, draft=(1 << 40) + 1) == 7
+    assert call_accept(lib, acc=(1 << 40) + 16) == 8           # accepted over the draft ids
+    assert call_accept(lib, err=ACC_PTR + 4) == 8              # accepted over the error word
