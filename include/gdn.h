@@ -82,11 +82,13 @@ typedef enum gdn_dtype {
 } gdn_dtype;
 
 /* Which kernel runs.  AUTO: the chunked tensor-core kernel where it applies
- * (bf16 q/k/v, dk = dv = 128, max_T <= 16), else the recurrent kernel. */
+ * (bf16 q/k/v, dk = dv = 128, any max_T: blocks of 16 tokens chained through
+ * the state), else the recurrent kernel. */
 typedef enum gdn_algo {
     GDN_ALGO_AUTO = 0,
     GDN_ALGO_RECURRENT = 1,   /* per-token update on CUDA cores, any supported shape */
-    GDN_ALGO_CHUNK = 2        /* WY/chunk form, bf16 mma.sync for the state products */
+    GDN_ALGO_CHUNK = 2        /* WY/chunk form, bf16 mma.sync for the state products; 16-token
+                                 chunks, the state carried from one chunk to the next */
 } gdn_algo;
 
 /* Bits ORed into *dev_err by the kernels. */

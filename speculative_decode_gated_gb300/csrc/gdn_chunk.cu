@@ -76,12 +76,13 @@ struct TokBuf {  // 1024-byte aligned: three swizzled [16][128] bf16 tiles
 };
 
 struct Aux {
-    float gram[2][2][CT][CT];  // [part][0][t][s] = k_t.k_s, [part][1][t][s] = q_t.k_s (partial sums)
+    float gram[2][CT][CT];  // [0][t][s] = k_t.k_s, [1][t][s] = q_t.k_s
     float A[CT][CT];        // beta_t D[t][s] k_t.k_s for s < t < T, else 0
     float M[CT][CT];        // D[t][s] q_t.k_s for s <= t, else 0
     float Tinv[CT][CT];     // (I + A)^-1, rows t >= T zeroed
     float alpha[CT], beta[CT], gamma[CT];
-    float dcol[CT];         // D[a-1][s] for s < a, else 0
+    float dcol[CT];         // D[a'-1][s] for s < a' (a' = the commit point within the chunk), else 0
+    float dlast[CT];        // D[15][s]: the whole chunk's decay to its end
     unsigned long long tile_full, tok_full[2];
     int abort_flag;
 };
@@ -255,18 +256,19 @@ __device__ __forceinline__ UnitPlan plan_unit(const Launch<NL> &L, int w, int U,
     return pl;
 }
 
-// Thread 0: the token boxes (k, v and, unless committing, q) of one unit.
+// Thread 0: the token boxes (k, v and, unless committing, q) of chunk `ch` of
+// one unit: token rows row0 + 16 ch + [0, 16).
 template <int MODE>
-__device__ __forceinline__ void issue_tokens(const Maps &maps, const UnitPlan &pl, TokBuf &tb,
-                                             uint32_t tok_bar) {
+__device__ __forceinline__ void issue_tokens(const Maps &maps, const UnitPlan &pl, int ch,
+                                             TokBuf &tb, uint32_t tok_bar) {
+    const int row = pl.u.row0 + CT * ch;
     mbar_arrive_expect_tx(tok_bar, (MODE == kCommit ? 2u : 3u) * kTokBytes);
 #pragma unroll
     for (int hb = 0; hb < 2; ++hb) {
-        tma_load_3d(smem_u32(tb.k) + hb * kTokHalfBytes, &maps.k, 64 * hb, pl.h, pl.u.row0, tok_bar);
-        tma_load_3d(smem_u32(tb.v) + hb * kTokHalfBytes, &maps.v, 64 * hb, pl.h, pl.u.row0, tok_bar);
+        tma_load_3d(smem_u32(tb.k) + hb * kTokHalfBytes, &maps.k, 64 * hb, pl.h, row, tok_bar);
+        tma_load_3d(smem_u32(tb.v) + hb * kTokHalfBytes, &maps.v, 64 * hb, pl.h, row, tok_bar);
         if (MODE != kCommit)
-            tma_load_3d(smem_u32(tb.q) + hb * kTokHalfBytes, &maps.q, 64 * hb, pl.h, pl.u.row0,
-                        tok_bar);
+            tma_load_3d(smem_u32(tb.q) + hb * kTokHalfBytes, &maps.q, 64 * hb, pl.h, row, tok_bar);
     }
 }
 
@@ -338,12 +340,14 @@ __device__ __forceinline__ void early_prefetch(const Launch<NL> &L, int w0, int 
     }
 }
 
-// Gate of token min(tid, T - 1) of a unit (any clamped row when the unit is
-// skipped or tid >= T): always a valid address (the chunk kernel runs only
-// with n_tok >= 1), so the load never sits behind a branch.
+// Gate of token 16 ch + min(tid, left - 1) of a unit, left = the unit's tokens
+// from chunk ch on (any clamped row when the unit is skipped or the token is
+// past the end): always a valid address (the chunk kernel runs only with
+// n_tok >= 1), so the load never sits behind a branch.
 __device__ __forceinline__ float gate_load(const float *gate, const Args &p, const UnitPlan &pl,
-                                           int tid) {
-    long long row = (long long)pl.u.row0 + (tid < pl.teff ? tid : pl.teff - 1);
+                                           int ch, int tid) {
+    const int left = pl.teff - CT * ch;
+    long long row = (long long)pl.u.row0 + CT * ch + (tid < left ? tid : left - 1);
     row = row < 0 ? 0 : (row >= p.n_tok ? p.n_tok - 1 : row);
     const int h = pl.h < 0 ? 0 : (pl.h >= p.H ? p.H - 1 : pl.h);
     return ld_early(gate + (size_t)row * p.H + h);
@@ -351,46 +355,95 @@ __device__ __forceinline__ float gate_load(const float *gate, const Args &p, con
 
 // ------------------------------------------------------------ the kernel
 
-// NW warps per block share one unit: warp w owns CW = 128 / NW value columns,
-// MT = CW / 16 m-tiles of 16 columns; lane (g, c) holds CPT = 2 MT adjacent
-// columns CPT g + {0..CPT-1} of the warp's slice (m-tile m: fragment row g is
-// column CPT g + 2m, row g + 8 is CPT g + 2m + 1).
-template <int NW>
-struct Cfg {
-    static constexpr int kThreads = 32 * NW;
-    static constexpr int CW = D / NW;
-    static constexpr int MT = CW / 16;
-    static constexpr int CPT = 2 * MT;
-    static constexpr int kTinvLanes = CT / NW;  // Tinv columns per warp
-};
+// Four warps share one unit: warp w owns the 32 value columns [32w, 32w + 32),
+// two m-tiles of 16 columns; lane (g, c) holds the 4 adjacent columns
+// 32w + 4g + {0..3} (m-tile m: fragment row g is column 4g + 2m, row g + 8 is
+// 4g + 2m + 1).
+constexpr int NW = 4;
+constexpr int kThreads = 32 * NW;
+constexpr int CW = D / NW;       // 32 columns per warp
+constexpr int MT = CW / 16;      // 2 m-tiles
+constexpr int CPT = 2 * MT;      // 4 columns per lane
+constexpr int kTinvLanes = CT / NW;  // Tinv columns per warp
 
-// Columns CPT g + [0, CPT) of warp w's slice, row `row`, from the swizzled tile.
-template <int NW>
-__device__ __forceinline__ void ld_tile_row(const unsigned char *tile, int warp, int g, int row,
-                                            float *out) {
-    using C = Cfg<NW>;
-    const int col = warp * C::CW + C::CPT * g;  // first column, 0..127
+// Columns CPT g + [0, CPT) of warp w's slice, key row `row`, from the swizzled tile.
+__device__ __forceinline__ float4 ld_tile_row(const unsigned char *tile, int warp, int g, int row) {
+    const int col = warp * CW + CPT * g;  // first column, 0..127
     const unsigned char *box = tile + (col >> 5) * kBoxBytes;
     const int chunk = (col & 31) >> 2;
-    const unsigned char *ptr = box + row * 128 + ((chunk ^ (row & 7)) << 4) + (col & 3) * 4;
-    if (C::CPT == 4) {
-        const float4 x = *reinterpret_cast<const float4 *>(ptr);
-        out[0] = x.x;
-        out[1] = x.y;
-        out[2] = x.z;
-        out[3] = x.w;
-    } else {
-        const float2 x = *reinterpret_cast<const float2 *>(ptr);
-        out[0] = x.x;
-        out[1] = x.y;
+    return *reinterpret_cast<const float4 *>(box + row * 128 + ((chunk ^ (row & 7)) << 4));
+}
+
+// Key rows of this lane in iteration kb, element rr of a fragment: 16 kb + 2c + {0, 1, 8, 9}.
+__device__ __forceinline__ int key_row(int kb, int c, int rr) {
+    return 16 * kb + 2 * c + (rr & 1) + 8 * (rr >> 1);
+}
+
+// The state after `dvec`-weighted tokens of the chunk:
+//   H^T <- gam H^T + (dvec . W)^T K       (dvec[s] = 0 for tokens not taken)
+// 16 key rows at a time; the accumulators start from the state in `hr` (the
+// A-fragment layout of H^T is also the accumulator layout of this product).
+// STORE: the result goes to `dst` (this thread's columns of the pool tile,
+// 16-byte stores); else it replaces `hr`.
+template <bool STORE>
+__device__ __forceinline__ void state_update(float (&hr)[8][4][CPT], const float (&wq)[MT][2][4],
+                                             const float *dvec, float gam, uint32_t k_smem,
+                                             int lane, int c, float *dst) {
+    uint32_t ah[MT][4], al[MT][4];
+#pragma unroll
+    for (int ntt = 0; ntt < 2; ++ntt) {
+        const float d0 = dvec[8 * ntt + 2 * c], d1 = dvec[8 * ntt + 2 * c + 1];
+#pragma unroll
+        for (int m = 0; m < MT; ++m) {
+            split2(d0 * wq[m][ntt][0], d1 * wq[m][ntt][1], ah[m][2 * ntt], al[m][2 * ntt]);
+            split2(d0 * wq[m][ntt][2], d1 * wq[m][ntt][3], ah[m][2 * ntt + 1], al[m][2 * ntt + 1]);
+        }
+    }
+    // ldmatrix.trans row address of this lane: matrix lane/8 -> (token half, dk half).
+    const int mi = lane >> 3;
+    const int krow = (lane & 7) + 8 * (mi & 1);
+#pragma unroll
+    for (int kb = 0; kb < 8; ++kb) {
+        float hv[4][CPT];
+#pragma unroll
+        for (int rr = 0; rr < 4; ++rr)
+#pragma unroll
+            for (int e = 0; e < CPT; ++e) hv[rr][e] = gam * hr[kb][rr][e];
+        uint32_t b00, b01, b10, b11;  // (n-tile 2kb: b0, b1), (n-tile 2kb+1: b0, b1)
+        ldsm_x4_trans(b00, b01, b10, b11, k_smem + tok_off(krow, 16 * kb + 8 * (mi >> 1)));
+#pragma unroll
+        for (int m = 0; m < MT; ++m) {
+            mma(hv[0][2 * m], hv[1][2 * m], hv[0][2 * m + 1], hv[1][2 * m + 1], ah[m][0], ah[m][1],
+                ah[m][2], ah[m][3], b00, b01);
+            mma(hv[2][2 * m], hv[3][2 * m], hv[2][2 * m + 1], hv[3][2 * m + 1], ah[m][0], ah[m][1],
+                ah[m][2], ah[m][3], b10, b11);
+        }
+#pragma unroll
+        for (int m = 0; m < MT; ++m) {
+            mma(hv[0][2 * m], hv[1][2 * m], hv[0][2 * m + 1], hv[1][2 * m + 1], al[m][0], al[m][1],
+                al[m][2], al[m][3], b00, b01);
+            mma(hv[2][2 * m], hv[3][2 * m], hv[2][2 * m + 1], hv[3][2 * m + 1], al[m][0], al[m][1],
+                al[m][2], al[m][3], b10, b11);
+        }
+#pragma unroll
+        for (int rr = 0; rr < 4; ++rr) {
+            if (STORE) {
+                *reinterpret_cast<float4 *>(dst + key_row(kb, c, rr) * D) =
+                    make_float4(hv[rr][0], hv[rr][1], hv[rr][2], hv[rr][3]);
+            } else {
+#pragma unroll
+                for (int e = 0; e < CPT; ++e) hr[kb][rr][e] = hv[rr][e];
+            }
+        }
     }
 }
 
-template <int MODE, int NW, bool RAGGED, int NL>
-__global__ void __launch_bounds__(32 * NW, kBlocksPerSM)
+// MULTI: units may have more than 16 tokens (several chunks, the state carried
+// in registers from one to the next); otherwise every unit is one chunk and
+// the verify kernel keeps no state in registers.
+template <int MODE, bool RAGGED, int NL, bool MULTI>
+__global__ void __launch_bounds__(kThreads, kBlocksPerSM)
     chunk_kernel(const __grid_constant__ Launch<NL> L) {
-    using C = Cfg<NW>;
-    constexpr int MT = C::MT, CPT = C::CPT, NTH = C::kThreads;
     extern __shared__ unsigned char smem_raw[];
     const uint32_t raw_addr = smem_u32(smem_raw);
     Smem &sm = *reinterpret_cast<Smem *>(smem_raw + ((1024u - (raw_addr & 1023u)) & 1023u));
@@ -404,7 +457,7 @@ __global__ void __launch_bounds__(32 * NW, kBlocksPerSM)
     const int G = gridDim.x;
     const size_t row_stride = (size_t)p.H * D;
     const uint32_t tile_bar = smem_u32(&ax.tile_full);
-    const int col0 = warp * C::CW + CPT * g;  // this thread's first value column
+    const int col0 = warp * CW + CPT * g;  // this thread's first value column
 
     // Programmatic dependent launch: the next kernel on the stream may be
     // launched right away (its blocks become resident as ours exit and wait in
@@ -439,14 +492,17 @@ __global__ void __launch_bounds__(32 * NW, kBlocksPerSM)
         nxt = plan_unit<MODE, NL>(L, unit + G, U, load_unit_meta<MODE, RAGGED, NL>(p, unit + G, W, U));
     raw = load_unit_meta<MODE, RAGGED, NL>(p, unit + 2 * G, W, U);
 
-    // Unit k (in the order this block computes them) uses token buffer k & 1.
-    // Its token boxes go out when unit k-1 starts (that buffer was last used by
-    // unit k-2), its tile when unit k-1 is done with the tile stage.
+    // A step is one 16-token chunk of one unit.  Step k (in the order this block
+    // computes them) uses token buffer k & 1; its token boxes go out when step
+    // k-1 starts (that buffer was last used by step k-2).  A unit's tile goes
+    // out when the previous unit has read its own tile (right after that unit's
+    // first product); later chunks start from the state held in registers.
     int issued = 0;      // units whose tile load was issued
-    int tok_issued = 0;  // units whose token load was issued
-    int processed = 0;   // units computed
+    int processed = 0;   // units whose tile was consumed
+    int tok_issued = 0;  // steps whose token load was issued
+    int steps = 0;       // steps computed
     if (tid == 0 && !cur.skip) {
-        issue_tokens<MODE>(L.maps[cur.layer], cur, sm.tok[0], smem_u32(&ax.tok_full[0]));
+        issue_tokens<MODE>(L.maps[cur.layer], cur, 0, sm.tok[0], smem_u32(&ax.tok_full[0]));
         issue_tile(L.maps[cur.layer], cur, sm.tile, tile_bar);
     }
     if (tid == 0 && !nxt.skip) prefetch_unit<MODE>(L.maps[nxt.layer], nxt);
@@ -454,11 +510,16 @@ __global__ void __launch_bounds__(32 * NW, kBlocksPerSM)
         ++issued;
         ++tok_issued;
     }
-    // Gates of the current unit: thread t < 16 holds alpha_t, beta_t, loaded
+    // Gates of the next step: thread t < 16 holds alpha_t, beta_t, loaded
     // unconditionally from a clamped (always valid) row; rows t >= T are
     // replaced by alpha = 1, beta = 0 where the values are used.
-    float ga = gate_load(L.a[cur.layer].alpha, p, cur, tid);
-    float gb = gate_load(L.a[cur.layer].beta, p, cur, tid);
+    float ga = gate_load(L.a[cur.layer].alpha, p, cur, 0, tid);
+    float gb = gate_load(L.a[cur.layer].beta, p, cur, 0, tid);
+
+    // The unit's state as H^T in the A-fragment layout: the checkpoint tile,
+    // then the state after each chunk (single-chunk verify needs none).
+    constexpr bool kKeep = MULTI || MODE != kVerify;
+    float hr[kKeep ? 8 : 1][4][CPT];
 
     bool aborted = false;
     for (; unit < W; unit += G) {
@@ -470,12 +531,12 @@ __global__ void __launch_bounds__(32 * NW, kBlocksPerSM)
         raw = load_unit_meta<MODE, RAGGED, NL>(p, unit + 3 * G, W, U);
         if (me.skip) {
             // Gates of the next unit (consumed one iteration later).
-            ga = gate_load(L.a[cur.layer].alpha, p, cur, tid);
-            gb = gate_load(L.a[cur.layer].beta, p, cur, tid);
+            ga = gate_load(L.a[cur.layer].alpha, p, cur, 0, tid);
+            gb = gate_load(L.a[cur.layer].beta, p, cur, 0, tid);
             if (!cur.skip && issued == processed) {
                 // Nothing is in flight: the next unit's loads can all go now.
                 if (tid == 0) {
-                    issue_tokens<MODE>(L.maps[cur.layer], cur, sm.tok[tok_issued & 1],
+                    issue_tokens<MODE>(L.maps[cur.layer], cur, 0, sm.tok[tok_issued & 1],
                                        smem_u32(&ax.tok_full[tok_issued & 1]));
                     issue_tile(L.maps[cur.layer], cur, sm.tile, tile_bar);
                 }
@@ -485,341 +546,312 @@ __global__ void __launch_bounds__(32 * NW, kBlocksPerSM)
             if (tid == 0 && !nxt.skip) prefetch_unit<MODE>(L.maps[nxt.layer], nxt);
             continue;
         }
-        const int T = me.teff;
-        const int buf = processed & 1;
-        const TokBuf &tb = sm.tok[buf];
-        const bool write_state = MODE != kVerify && me.u.a > 0;
-        // With 4 warps the tile also stays in registers for the commit (so the
-        // stage is free right after the first product); with 8 warps (half the
-        // registers) the commit re-reads it and the stage is held until then.
-        constexpr bool kRegTile = NW == 4;
-        const bool keep_tile = write_state && !kRegTile;
+        const int Tu = me.teff;  // tokens of the unit that matter: T_r, or a_r for commit
+        const int nch = MULTI ? (Tu + CT - 1) / CT : 1;
+        // The commit point: chunk `ca` holds token a_r - 1.
+        const int ca = (MODE != kVerify && me.u.a > 0) ? (me.u.a - 1) / CT : -1;
 
-        // 1. Gates into shared memory; token block arrival.
-        __syncthreads();  // the previous unit is done with the small matrices
-        // The next unit's token block goes into the other buffer now.
-        if (!cur.skip && tok_issued == processed + 1) {
-            if (tid == 0)
-                issue_tokens<MODE>(L.maps[cur.layer], cur, sm.tok[tok_issued & 1],
-                                   smem_u32(&ax.tok_full[tok_issued & 1]));
-            ++tok_issued;
-        }
-        if (tid < CT) {
-            ax.alpha[tid] = tid < T ? ga : 1.0f;
-            ax.beta[tid] = tid < T ? gb : 0.0f;
-        }
-        // Gates of the next unit, loaded straight into the registers just freed
-        // (consumed one iteration later, so this load is never waited on here).
-        ga = gate_load(L.a[cur.layer].alpha, p, cur, tid);
-        gb = gate_load(L.a[cur.layer].beta, p, cur, tid);
-        if (!wait_parity(smem_u32(&ax.tok_full[buf]), (processed >> 1) & 1)) ax.abort_flag = 1;
-        __syncthreads();
-        if (ax.abort_flag) {
-            aborted = true;
-            break;
-        }
+        for (int ch = 0; ch < nch; ++ch) {
+            const int T = Tu - CT * ch < CT ? Tu - CT * ch : CT;  // tokens of this chunk
+            const bool more = MULTI && ch + 1 < nch;  // another chunk of this unit follows
+            const TokBuf &tb = sm.tok[steps & 1];
 
-        // 2. Gram blocks k_t.k_s and q_t.k_s: block (matrix (w/2)%2, columns 8 (w%2) + [0, 8)),
-        //    k-steps split over NW/4 warps into partial sums.
-        {
-            const int blk = warp & 3, part = warp >> 2;
-            constexpr int KPW = 8 / (NW / 4);  // k-steps per warp
-            const unsigned char *At = (blk >> 1) ? tb.q : tb.k;
-            const int nt = blk & 1;
-            float a0[4] = {0.f, 0.f, 0.f, 0.f}, a1[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-            for (int kk = 0; kk < KPW; ++kk) {
-                const int kb = part * KPW + kk;
-                const int col = 16 * kb + 2 * c;
-                float *acc = (kk & 1) ? a1 : a0;
-                mma(acc[0], acc[1], acc[2], acc[3], ld_tok32(At, g, col), ld_tok32(At, g + 8, col),
-                    ld_tok32(At, g, col + 8), ld_tok32(At, g + 8, col + 8),
-                    ld_tok32(tb.k, 8 * nt + g, col), ld_tok32(tb.k, 8 * nt + g, col + 8));
-            }
-            float(*Gm)[CT] = ax.gram[part][blk >> 1];
-            Gm[g][8 * nt + 2 * c] = a0[0] + a1[0];
-            Gm[g][8 * nt + 2 * c + 1] = a0[1] + a1[1];
-            Gm[g + 8][8 * nt + 2 * c] = a0[2] + a1[2];
-            Gm[g + 8][8 * nt + 2 * c + 1] = a0[3] + a1[3];
-        }
-        __syncthreads();
-
-        // 3. Decay products and the triangular matrices, 256 / NTH (t, s) pairs per thread.
-        {
-            float al[CT];
-#pragma unroll
-            for (int r4 = 0; r4 < CT; r4 += 4) {
-                const float4 a4 = *reinterpret_cast<const float4 *>(&ax.alpha[r4]);
-                al[r4] = a4.x;
-                al[r4 + 1] = a4.y;
-                al[r4 + 2] = a4.z;
-                al[r4 + 3] = a4.w;
-            }
-#pragma unroll
-            for (int e2 = 0; e2 < CT * CT / NTH; ++e2) {
-                const int e = tid + NTH * e2;
-                const int t = e >> 4, s = e & 15;
-                float d = 1.0f;  // D[t][s] = prod_{s<r<=t} alpha_r
-#pragma unroll
-                for (int r = 1; r < CT; ++r) d *= (r > s && r <= t) ? al[r] : 1.0f;
-                float kk = ax.gram[0][0][t][s], qk = ax.gram[0][1][t][s];
-                if (NW == 8) {
-                    kk += ax.gram[1][0][t][s];
-                    qk += ax.gram[1][1][t][s];
+            // 1. Gates into shared memory; token block arrival.
+            __syncthreads();  // the previous step is done with the small matrices
+            // The next step's token block goes into the other buffer now.
+            if (tok_issued == steps + 1 && (more || !cur.skip)) {
+                if (tid == 0) {
+                    TokBuf &nb = sm.tok[tok_issued & 1];
+                    const uint32_t nbar = smem_u32(&ax.tok_full[tok_issued & 1]);
+                    if (more)
+                        issue_tokens<MODE>(L.maps[me.layer], me, ch + 1, nb, nbar);
+                    else
+                        issue_tokens<MODE>(L.maps[cur.layer], cur, 0, nb, nbar);
                 }
-                ax.A[t][s] = (s < t && t < T) ? ax.beta[t] * d * kk : 0.0f;
-                ax.M[t][s] = (s <= t) ? d * qk : 0.0f;
-                if (s == 0) ax.gamma[t] = d * al[0];
-                if (MODE != kVerify && t == me.u.a - 1) ax.dcol[s] = (s <= t) ? d : 0.0f;
+                ++tok_issued;
             }
-        }
-        __syncthreads();
+            if (tid < CT) {
+                ax.alpha[tid] = tid < T ? ga : 1.0f;
+                ax.beta[tid] = tid < T ? gb : 0.0f;
+            }
+            // Gates of the next step, loaded straight into the registers just
+            // freed (consumed one step later, so this load is never waited on here).
+            if (more) {
+                ga = gate_load(L.a[me.layer].alpha, p, me, ch + 1, tid);
+                gb = gate_load(L.a[me.layer].beta, p, me, ch + 1, tid);
+            } else {
+                ga = gate_load(L.a[cur.layer].alpha, p, cur, 0, tid);
+                gb = gate_load(L.a[cur.layer].beta, p, cur, 0, tid);
+            }
+            if (!wait_parity(smem_u32(&ax.tok_full[steps & 1]), (steps >> 1) & 1))
+                ax.abort_flag = 1;
+            __syncthreads();
+            if (ax.abort_flag) {
+                aborted = true;
+                break;
+            }
 
-        // 4. The checkpoint tile of this unit.
-        if (!wait_parity(tile_bar, processed & 1)) ax.abort_flag = 1;
-        __syncthreads();
-        if (ax.abort_flag) {
-            aborted = true;
-            break;
-        }
-
-        // 5. P = H_0^T Q^T and Z = H_0^T K^T for this warp's columns (N-tiles: Q 0-7,
-        //    Q 8-15, K 0-7, K 8-15; commit needs only Z).
-        constexpr int NT0 = (MODE == kCommit) ? 2 : 0;
-        // Interleaved with the products (it only needs A, finished above):
-        // Tinv = (I + A)^-1 by forward substitution, rows 2kb and 2kb+1 in
-        // iteration kb.  Lane groups compute column j = w + NW (lane % (16/NW));
-        // the first 16/NW lanes store it.  x_t = [t == j, t < T] - sum_{s<t} A[t][s] x_s
-        // gives zeros above the diagonal and in rows t >= T (A is zero there).
-        const int tj = warp + NW * (lane % C::kTinvLanes);
-        float xt[CT];
-        float hr[kRegTile ? 8 : 1][4][CPT];  // the tile in registers (4-warp layout)
-        float y[MT][4][4];
+            // 2. Gram blocks k_t.k_s and q_t.k_s: warp w computes matrix w / 2,
+            //    columns 8 (w % 2) + [0, 8), over all 128 key dims.
+            {
+                const unsigned char *At = (warp >> 1) ? tb.q : tb.k;
+                const int nt = warp & 1;
+                float a0[4] = {0.f, 0.f, 0.f, 0.f}, a1[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-        for (int m = 0; m < MT; ++m)
-#pragma unroll
-            for (int nt = 0; nt < 4; ++nt)
-#pragma unroll
-                for (int e = 0; e < 4; ++e) y[m][nt][e] = 0.0f;
-#pragma unroll
-        for (int kb = 0; kb < 8; ++kb) {
-#pragma unroll
-            for (int t = 2 * kb; t < 2 * kb + 2; ++t) {
-                float acc = (t == tj && t < T) ? 1.0f : 0.0f;
-#pragma unroll
-                for (int s4 = 0; s4 < t; s4 += 4) {
-                    const float4 a4 = *reinterpret_cast<const float4 *>(&ax.A[t][s4]);
-                    acc = fmaf(-a4.x, xt[s4], acc);
-                    if (s4 + 1 < t) acc = fmaf(-a4.y, xt[s4 + 1], acc);
-                    if (s4 + 2 < t) acc = fmaf(-a4.z, xt[s4 + 2], acc);
-                    if (s4 + 3 < t) acc = fmaf(-a4.w, xt[s4 + 3], acc);
+                for (int kb = 0; kb < 8; ++kb) {
+                    const int col = 16 * kb + 2 * c;
+                    float *acc = (kb & 1) ? a1 : a0;
+                    mma(acc[0], acc[1], acc[2], acc[3], ld_tok32(At, g, col),
+                        ld_tok32(At, g + 8, col), ld_tok32(At, g, col + 8),
+                        ld_tok32(At, g + 8, col + 8), ld_tok32(tb.k, 8 * nt + g, col),
+                        ld_tok32(tb.k, 8 * nt + g, col + 8));
                 }
-                xt[t] = acc;
-                if (lane < C::kTinvLanes) ax.Tinv[t][tj] = acc;
+                float(*Gm)[CT] = ax.gram[warp >> 1];
+                Gm[g][8 * nt + 2 * c] = a0[0] + a1[0];
+                Gm[g][8 * nt + 2 * c + 1] = a0[1] + a1[1];
+                Gm[g + 8][8 * nt + 2 * c] = a0[2] + a1[2];
+                Gm[g + 8][8 * nt + 2 * c + 1] = a0[3] + a1[3];
             }
-            float hv[4][CPT];
-#pragma unroll
-            for (int rr = 0; rr < 4; ++rr) {
-                ld_tile_row<NW>(sm.tile, warp, g, 16 * kb + 2 * c + (rr & 1) + 8 * (rr >> 1), hv[rr]);
-                if (kRegTile && MODE != kVerify)
-#pragma unroll
-                    for (int e = 0; e < CPT; ++e) hr[kRegTile ? kb : 0][rr][e] = hv[rr][e];
-            }
-            uint32_t b[4][2];
-#pragma unroll
-            for (int nt = NT0; nt < 4; ++nt) {
-                const unsigned char *Bt = nt < 2 ? tb.q : tb.k;
-                const int tok = 8 * (nt & 1) + g;
-                b[nt][0] = ld_tok32(Bt, tok, 16 * kb + 2 * c);
-                b[nt][1] = ld_tok32(Bt, tok, 16 * kb + 2 * c + 8);
-            }
-#pragma unroll
-            for (int m = 0; m < MT; ++m) {
-                uint32_t ah[4], al[4];
-                split2(hv[0][2 * m], hv[1][2 * m], ah[0], al[0]);
-                split2(hv[0][2 * m + 1], hv[1][2 * m + 1], ah[1], al[1]);
-                split2(hv[2][2 * m], hv[3][2 * m], ah[2], al[2]);
-                split2(hv[2][2 * m + 1], hv[3][2 * m + 1], ah[3], al[3]);
-#pragma unroll
-                for (int nt = NT0; nt < 4; ++nt)
-                    mma(y[m][nt][0], y[m][nt][1], y[m][nt][2], y[m][nt][3], ah[0], ah[1], ah[2],
-                        ah[3], b[nt][0], b[nt][1]);
-#pragma unroll
-                for (int nt = NT0; nt < 4; ++nt)
-                    mma(y[m][nt][0], y[m][nt][1], y[m][nt][2], y[m][nt][3], al[0], al[1], al[2],
-                        al[3], b[nt][0], b[nt][1]);
-            }
-        }
-        ++processed;
+            __syncthreads();
 
-        // Tinv is complete; when the tile is not needed again, the stage is free
-        // and thread 0 sends the next unit's tile.
-        __syncthreads();
-        if (!keep_tile && !cur.skip) {
-            if (tid == 0) issue_tile(L.maps[cur.layer], cur, sm.tile, tile_bar);
-            ++issued;
-        }
-        if (tid == 0 && !nxt.skip) prefetch_unit<MODE>(L.maps[nxt.layer], nxt);
-
-        // Token indices of this thread in the fragments: n-tile half ntt, element e:
-        //   t = 8 ntt + 2c + (e & 1);   column = col0 + 2m + (e >> 1).
-        // 6. R^T = beta_t (v_t - gamma_t Z_t), zero for t >= T.
-        float rr_[MT][2][4];
+            // 3. Decay products and the triangular matrices, 256 / kThreads (t, s) pairs per thread.
+            {
+                float al[CT];
 #pragma unroll
-        for (int m = 0; m < MT; ++m)
-#pragma unroll
-            for (int ntt = 0; ntt < 2; ++ntt)
-#pragma unroll
-                for (int eo = 0; eo < 2; ++eo) {
-                    const int t = 8 * ntt + 2 * c + eo;
-                    const uint32_t vv = *reinterpret_cast<const uint32_t *>(tb.v + tok_off(t, col0 + 2 * m));
-                    const float v0 = __uint_as_float(vv << 16), v1 = __uint_as_float(vv & 0xFFFF0000u);
-                    const float bt = ax.beta[t], gt = ax.gamma[t];
-                    const bool live = t < T;
-                    rr_[m][ntt][eo] = live ? bt * (v0 - gt * y[m][2 + ntt][eo]) : 0.0f;
-                    rr_[m][ntt][2 + eo] = live ? bt * (v1 - gt * y[m][2 + ntt][2 + eo]) : 0.0f;
+                for (int r4 = 0; r4 < CT; r4 += 4) {
+                    const float4 a4 = *reinterpret_cast<const float4 *>(&ax.alpha[r4]);
+                    al[r4] = a4.x;
+                    al[r4 + 1] = a4.y;
+                    al[r4 + 2] = a4.z;
+                    al[r4 + 3] = a4.w;
                 }
-
-        // 7. W^T = R^T Tinv^T: A = R^T (accumulator layout, split), B = Tinv^T (split).
-        float wq[MT][2][4];
-        {
-            uint32_t bh[2][2], bl[2][2];
+                const int tc = ch == ca ? me.u.a - CT * ch - 1 : -1;  // commit row of this chunk
 #pragma unroll
-            for (int nt = 0; nt < 2; ++nt) {
-                const float *tr = ax.Tinv[8 * nt + g];
-                split2(tr[2 * c], tr[2 * c + 1], bh[nt][0], bl[nt][0]);
-                split2(tr[2 * c + 8], tr[2 * c + 9], bh[nt][1], bl[nt][1]);
-            }
+                for (int e2 = 0; e2 < CT * CT / kThreads; ++e2) {
+                    const int e = tid + kThreads * e2;
+                    const int t = e >> 4, s = e & 15;
+                    float d = 1.0f;  // D[t][s] = prod_{s<r<=t} alpha_r
 #pragma unroll
-            for (int m = 0; m < MT; ++m) {
-                uint32_t ah[4], al[4];
-                split2(rr_[m][0][0], rr_[m][0][1], ah[0], al[0]);
-                split2(rr_[m][0][2], rr_[m][0][3], ah[1], al[1]);
-                split2(rr_[m][1][0], rr_[m][1][1], ah[2], al[2]);
-                split2(rr_[m][1][2], rr_[m][1][3], ah[3], al[3]);
-#pragma unroll
-                for (int nt = 0; nt < 2; ++nt) {
-                    float *d = wq[m][nt];
-                    d[0] = d[1] = d[2] = d[3] = 0.0f;
-                    mma(d[0], d[1], d[2], d[3], ah[0], ah[1], ah[2], ah[3], bh[nt][0], bh[nt][1]);
-                    mma(d[0], d[1], d[2], d[3], ah[0], ah[1], ah[2], ah[3], bl[nt][0], bl[nt][1]);
-                    mma(d[0], d[1], d[2], d[3], al[0], al[1], al[2], al[3], bh[nt][0], bh[nt][1]);
+                    for (int r = 1; r < CT; ++r) d *= (r > s && r <= t) ? al[r] : 1.0f;
+                    const float kk = ax.gram[0][t][s], qk = ax.gram[1][t][s];
+                    ax.A[t][s] = (s < t && t < T) ? ax.beta[t] * d * kk : 0.0f;
+                    ax.M[t][s] = (s <= t) ? d * qk : 0.0f;
+                    if (s == 0) ax.gamma[t] = d * al[0];
+                    if (MODE != kVerify && t == tc) ax.dcol[s] = (s <= t) ? d : 0.0f;
+                    if (MULTI && t == CT - 1) ax.dlast[s] = d;
                 }
             }
-        }
+            __syncthreads();
 
-        // 8. O^T = P^T diag(gamma) + W^T M^T, stored as float2 pairs of adjacent columns.
-        if (MODE != kCommit) {
-            uint32_t bh[2][2], bl[2][2];
-#pragma unroll
-            for (int nt = 0; nt < 2; ++nt) {
-                const float *mr = ax.M[8 * nt + g];
-                split2(mr[2 * c], mr[2 * c + 1], bh[nt][0], bl[nt][0]);
-                split2(mr[2 * c + 8], mr[2 * c + 9], bh[nt][1], bl[nt][1]);
-            }
-            float *go = L.a[me.layer].o + ((size_t)me.u.row0 * p.H + me.h) * D + col0;
-#pragma unroll
-            for (int m = 0; m < MT; ++m) {
-                uint32_t ah[4], al[4];
-                split2(wq[m][0][0], wq[m][0][1], ah[0], al[0]);
-                split2(wq[m][0][2], wq[m][0][3], ah[1], al[1]);
-                split2(wq[m][1][0], wq[m][1][1], ah[2], al[2]);
-                split2(wq[m][1][2], wq[m][1][3], ah[3], al[3]);
-#pragma unroll
-                for (int nt = 0; nt < 2; ++nt) {
-                    const int t0 = 8 * nt + 2 * c;
-                    const float g0 = ax.gamma[t0], g1 = ax.gamma[t0 + 1];
-                    float d[4] = {g0 * y[m][nt][0], g1 * y[m][nt][1], g0 * y[m][nt][2],
-                                  g1 * y[m][nt][3]};
-                    mma(d[0], d[1], d[2], d[3], ah[0], ah[1], ah[2], ah[3], bh[nt][0], bh[nt][1]);
-                    mma(d[0], d[1], d[2], d[3], ah[0], ah[1], ah[2], ah[3], bl[nt][0], bl[nt][1]);
-                    mma(d[0], d[1], d[2], d[3], al[0], al[1], al[2], al[3], bh[nt][0], bh[nt][1]);
-                    if (t0 < T)
-                        *reinterpret_cast<float2 *>(go + t0 * row_stride + 2 * m) = make_float2(d[0], d[2]);
-                    if (t0 + 1 < T)
-                        *reinterpret_cast<float2 *>(go + (t0 + 1) * row_stride + 2 * m) =
-                            make_float2(d[1], d[3]);
+            // 4. The checkpoint tile of this unit (first chunk only).
+            if (!MULTI || ch == 0) {
+                if (!wait_parity(tile_bar, processed & 1)) ax.abort_flag = 1;
+                __syncthreads();
+                if (ax.abort_flag) {
+                    aborted = true;
+                    break;
                 }
             }
-        }
 
-        // 9. Commit: H_a^T = gamma_{a-1} H_0^T + (D[a-1][.] w)^T K, 16 key rows at a
-        //    time: accumulators start from the tile (re-read from shared memory).
-        if (write_state) {
-            uint32_t ah[MT][4], al[MT][4];
+            // 5. P = H^T Q^T and Z = H^T K^T for this warp's columns, H the state at
+            //    the chunk's start (N-tiles: Q 0-7, Q 8-15, K 0-7, K 8-15; commit
+            //    needs only Z).  Interleaved with the products (it only needs A,
+            //    finished above): Tinv = (I + A)^-1 by forward substitution, rows
+            //    2kb and 2kb+1 in iteration kb.  Lane groups compute column
+            //    j = w + 4 (lane % 4); the first 4 lanes store it.
+            //    x_t = [t == j, t < T] - sum_{s<t} A[t][s] x_s gives zeros above
+            //    the diagonal and in rows t >= T (A is zero there).
+            constexpr int NT0 = (MODE == kCommit) ? 2 : 0;
+            const int tj = warp + NW * (lane % kTinvLanes);
+            float xt[CT];
+            float y[MT][4][4];
 #pragma unroll
-            for (int ntt = 0; ntt < 2; ++ntt) {
-                const float d0 = ax.dcol[8 * ntt + 2 * c], d1 = ax.dcol[8 * ntt + 2 * c + 1];
+            for (int m = 0; m < MT; ++m)
 #pragma unroll
-                for (int m = 0; m < MT; ++m) {
-                    split2(d0 * wq[m][ntt][0], d1 * wq[m][ntt][1], ah[m][2 * ntt], al[m][2 * ntt]);
-                    split2(d0 * wq[m][ntt][2], d1 * wq[m][ntt][3], ah[m][2 * ntt + 1],
-                           al[m][2 * ntt + 1]);
-                }
-            }
-            const float gam = ax.gamma[me.u.a - 1];
-            // ldmatrix.trans row address of this lane: matrix lane/8 -> (token half, dk half).
-            const int mi = lane >> 3;
-            const int krow = (lane & 7) + 8 * (mi & 1);
-            float *dst = opaque(me.u.tile) + col0;
+                for (int nt = 0; nt < 4; ++nt)
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) y[m][nt][e] = 0.0f;
 #pragma unroll
             for (int kb = 0; kb < 8; ++kb) {
-                float hv[4][CPT];
 #pragma unroll
-                for (int rr = 0; rr < 4; ++rr) {
-                    if (kRegTile) {
+                for (int t = 2 * kb; t < 2 * kb + 2; ++t) {
+                    float acc = (t == tj && t < T) ? 1.0f : 0.0f;
 #pragma unroll
-                        for (int e = 0; e < CPT; ++e) hv[rr][e] = hr[kRegTile ? kb : 0][rr][e];
-                    } else {
-                        ld_tile_row<NW>(sm.tile, warp, g, 16 * kb + 2 * c + (rr & 1) + 8 * (rr >> 1),
-                                        hv[rr]);
+                    for (int s4 = 0; s4 < t; s4 += 4) {
+                        const float4 a4 = *reinterpret_cast<const float4 *>(&ax.A[t][s4]);
+                        acc = fmaf(-a4.x, xt[s4], acc);
+                        if (s4 + 1 < t) acc = fmaf(-a4.y, xt[s4 + 1], acc);
+                        if (s4 + 2 < t) acc = fmaf(-a4.z, xt[s4 + 2], acc);
+                        if (s4 + 3 < t) acc = fmaf(-a4.w, xt[s4 + 3], acc);
                     }
-#pragma unroll
-                    for (int e = 0; e < CPT; ++e) hv[rr][e] *= gam;
+                    xt[t] = acc;
+                    if (lane < kTinvLanes) ax.Tinv[t][tj] = acc;
                 }
-                uint32_t b00, b01, b10, b11;  // (n-tile 2kb: b0, b1), (n-tile 2kb+1: b0, b1)
-                ldsm_x4_trans(b00, b01, b10, b11,
-                              smem_u32(tb.k) + tok_off(krow, 16 * kb + 8 * (mi >> 1)));
+                float hv[4][CPT];
+                if (!MULTI || ch == 0) {
+#pragma unroll
+                    for (int rr = 0; rr < 4; ++rr) {
+                        const float4 x = ld_tile_row(sm.tile, warp, g, key_row(kb, c, rr));
+                        hv[rr][0] = x.x;
+                        hv[rr][1] = x.y;
+                        hv[rr][2] = x.z;
+                        hv[rr][3] = x.w;
+                        if (kKeep)
+#pragma unroll
+                            for (int e = 0; e < CPT; ++e) hr[kKeep ? kb : 0][rr][e] = hv[rr][e];
+                    }
+                } else {
+#pragma unroll
+                    for (int rr = 0; rr < 4; ++rr)
+#pragma unroll
+                        for (int e = 0; e < CPT; ++e) hv[rr][e] = hr[kKeep ? kb : 0][rr][e];
+                }
+                uint32_t b[4][2];
+#pragma unroll
+                for (int nt = NT0; nt < 4; ++nt) {
+                    const unsigned char *Bt = nt < 2 ? tb.q : tb.k;
+                    const int tok = 8 * (nt & 1) + g;
+                    b[nt][0] = ld_tok32(Bt, tok, 16 * kb + 2 * c);
+                    b[nt][1] = ld_tok32(Bt, tok, 16 * kb + 2 * c + 8);
+                }
 #pragma unroll
                 for (int m = 0; m < MT; ++m) {
-                    mma(hv[0][2 * m], hv[1][2 * m], hv[0][2 * m + 1], hv[1][2 * m + 1], ah[m][0],
-                        ah[m][1], ah[m][2], ah[m][3], b00, b01);
-                    mma(hv[2][2 * m], hv[3][2 * m], hv[2][2 * m + 1], hv[3][2 * m + 1], ah[m][0],
-                        ah[m][1], ah[m][2], ah[m][3], b10, b11);
-                }
+                    uint32_t ah[4], al[4];
+                    split2(hv[0][2 * m], hv[1][2 * m], ah[0], al[0]);
+                    split2(hv[0][2 * m + 1], hv[1][2 * m + 1], ah[1], al[1]);
+                    split2(hv[2][2 * m], hv[3][2 * m], ah[2], al[2]);
+                    split2(hv[2][2 * m + 1], hv[3][2 * m + 1], ah[3], al[3]);
 #pragma unroll
-                for (int m = 0; m < MT; ++m) {
-                    mma(hv[0][2 * m], hv[1][2 * m], hv[0][2 * m + 1], hv[1][2 * m + 1], al[m][0],
-                        al[m][1], al[m][2], al[m][3], b00, b01);
-                    mma(hv[2][2 * m], hv[3][2 * m], hv[2][2 * m + 1], hv[3][2 * m + 1], al[m][0],
-                        al[m][1], al[m][2], al[m][3], b10, b11);
-                }
+                    for (int nt = NT0; nt < 4; ++nt)
+                        mma(y[m][nt][0], y[m][nt][1], y[m][nt][2], y[m][nt][3], ah[0], ah[1], ah[2],
+                            ah[3], b[nt][0], b[nt][1]);
 #pragma unroll
-                for (int rr = 0; rr < 4; ++rr) {
-                    float *rowp = dst + (16 * kb + 2 * c + (rr & 1) + 8 * (rr >> 1)) * D;
-                    if (CPT == 4)
-                        *reinterpret_cast<float4 *>(rowp) =
-                            make_float4(hv[rr][0], hv[rr][1], hv[rr][2], hv[rr][3]);
-                    else
-                        *reinterpret_cast<float2 *>(rowp) = make_float2(hv[rr][0], hv[rr][1]);
+                    for (int nt = NT0; nt < 4; ++nt)
+                        mma(y[m][nt][0], y[m][nt][1], y[m][nt][2], y[m][nt][3], al[0], al[1], al[2],
+                            al[3], b[nt][0], b[nt][1]);
                 }
             }
-        }
-        if (keep_tile) {
-            // The commit has read the tile: the stage is free now.
+
+            // Tinv is complete.  After the first chunk the tile is in registers:
+            // the stage is free and thread 0 sends the next unit's tile.
             __syncthreads();
-            if (!cur.skip) {
-                if (tid == 0) issue_tile(L.maps[cur.layer], cur, sm.tile, tile_bar);
-                ++issued;
+            if (!MULTI || ch == 0) {
+                ++processed;
+                if (!cur.skip) {
+                    if (tid == 0) issue_tile(L.maps[cur.layer], cur, sm.tile, tile_bar);
+                    ++issued;
+                }
+                if (tid == 0 && !nxt.skip) prefetch_unit<MODE>(L.maps[nxt.layer], nxt);
             }
+
+            // Token indices of this thread in the fragments: n-tile half ntt, element e:
+            //   t = 8 ntt + 2c + (e & 1);   column = col0 + 2m + (e >> 1).
+            // 6. R^T = beta_t (v_t - gamma_t Z_t), zero for t >= T.
+            float rr_[MT][2][4];
+#pragma unroll
+            for (int m = 0; m < MT; ++m)
+#pragma unroll
+                for (int ntt = 0; ntt < 2; ++ntt)
+#pragma unroll
+                    for (int eo = 0; eo < 2; ++eo) {
+                        const int t = 8 * ntt + 2 * c + eo;
+                        const uint32_t vv =
+                            *reinterpret_cast<const uint32_t *>(tb.v + tok_off(t, col0 + 2 * m));
+                        const float v0 = __uint_as_float(vv << 16);
+                        const float v1 = __uint_as_float(vv & 0xFFFF0000u);
+                        const float bt = ax.beta[t], gt = ax.gamma[t];
+                        const bool live = t < T;
+                        rr_[m][ntt][eo] = live ? bt * (v0 - gt * y[m][2 + ntt][eo]) : 0.0f;
+                        rr_[m][ntt][2 + eo] = live ? bt * (v1 - gt * y[m][2 + ntt][2 + eo]) : 0.0f;
+                    }
+
+            // 7. W^T = R^T Tinv^T: A = R^T (accumulator layout, split), B = Tinv^T (split).
+            float wq[MT][2][4];
+            {
+                uint32_t bh[2][2], bl[2][2];
+#pragma unroll
+                for (int nt = 0; nt < 2; ++nt) {
+                    const float *tr = ax.Tinv[8 * nt + g];
+                    split2(tr[2 * c], tr[2 * c + 1], bh[nt][0], bl[nt][0]);
+                    split2(tr[2 * c + 8], tr[2 * c + 9], bh[nt][1], bl[nt][1]);
+                }
+#pragma unroll
+                for (int m = 0; m < MT; ++m) {
+                    uint32_t ah[4], al[4];
+                    split2(rr_[m][0][0], rr_[m][0][1], ah[0], al[0]);
+                    split2(rr_[m][0][2], rr_[m][0][3], ah[1], al[1]);
+                    split2(rr_[m][1][0], rr_[m][1][1], ah[2], al[2]);
+                    split2(rr_[m][1][2], rr_[m][1][3], ah[3], al[3]);
+#pragma unroll
+                    for (int nt = 0; nt < 2; ++nt) {
+                        float *d = wq[m][nt];
+                        d[0] = d[1] = d[2] = d[3] = 0.0f;
+                        mma(d[0], d[1], d[2], d[3], ah[0], ah[1], ah[2], ah[3], bh[nt][0], bh[nt][1]);
+                        mma(d[0], d[1], d[2], d[3], ah[0], ah[1], ah[2], ah[3], bl[nt][0], bl[nt][1]);
+                        mma(d[0], d[1], d[2], d[3], al[0], al[1], al[2], al[3], bh[nt][0], bh[nt][1]);
+                    }
+                }
+            }
+
+            // 8. O^T = P^T diag(gamma) + W^T M^T, stored as float2 pairs of adjacent columns.
+            if (MODE != kCommit) {
+                uint32_t bh[2][2], bl[2][2];
+#pragma unroll
+                for (int nt = 0; nt < 2; ++nt) {
+                    const float *mr = ax.M[8 * nt + g];
+                    split2(mr[2 * c], mr[2 * c + 1], bh[nt][0], bl[nt][0]);
+                    split2(mr[2 * c + 8], mr[2 * c + 9], bh[nt][1], bl[nt][1]);
+                }
+                float *go = L.a[me.layer].o +
+                            ((size_t)(me.u.row0 + CT * ch) * p.H + me.h) * D + col0;
+#pragma unroll
+                for (int m = 0; m < MT; ++m) {
+                    uint32_t ah[4], al[4];
+                    split2(wq[m][0][0], wq[m][0][1], ah[0], al[0]);
+                    split2(wq[m][0][2], wq[m][0][3], ah[1], al[1]);
+                    split2(wq[m][1][0], wq[m][1][1], ah[2], al[2]);
+                    split2(wq[m][1][2], wq[m][1][3], ah[3], al[3]);
+#pragma unroll
+                    for (int nt = 0; nt < 2; ++nt) {
+                        const int t0 = 8 * nt + 2 * c;
+                        const float g0 = ax.gamma[t0], g1 = ax.gamma[t0 + 1];
+                        float d[4] = {g0 * y[m][nt][0], g1 * y[m][nt][1], g0 * y[m][nt][2],
+                                      g1 * y[m][nt][3]};
+                        mma(d[0], d[1], d[2], d[3], ah[0], ah[1], ah[2], ah[3], bh[nt][0], bh[nt][1]);
+                        mma(d[0], d[1], d[2], d[3], ah[0], ah[1], ah[2], ah[3], bl[nt][0], bl[nt][1]);
+                        mma(d[0], d[1], d[2], d[3], al[0], al[1], al[2], al[3], bh[nt][0], bh[nt][1]);
+                        if (t0 < T)
+                            *reinterpret_cast<float2 *>(go + t0 * row_stride + 2 * m) =
+                                make_float2(d[0], d[2]);
+                        if (t0 + 1 < T)
+                            *reinterpret_cast<float2 *>(go + (t0 + 1) * row_stride + 2 * m) =
+                                make_float2(d[1], d[3]);
+                    }
+                }
+            }
+
+            // 9. The committed state (its chunk only), then the state after the
+            //    whole chunk when another chunk follows.  A commit covers exactly
+            //    the chunks up to the commit point, so there the two never meet.
+            const bool commit_here = MODE == kCommit ? !more : (MODE == kFused && ch == ca);
+            if constexpr (kKeep) {
+                if (commit_here)
+                    state_update<true>(hr, wq, ax.dcol, ax.gamma[me.u.a - CT * ch - 1],
+                                       smem_u32(tb.k), lane, c, opaque(me.u.tile) + col0);
+                if (more)
+                    state_update<false>(hr, wq, ax.dlast, ax.gamma[CT - 1], smem_u32(tb.k), lane,
+                                        c, nullptr);
+            }
+            ++steps;
         }
+        if (aborted) break;
     }
 
     // Copies still in flight must land before the block exits.
     if (tid == 0) {
         bool ok = true;
         if (issued > processed) ok = wait_parity(tile_bar, processed & 1) && ok;
-        for (int k = processed; k < tok_issued; ++k)
+        for (int k = steps; k < tok_issued; ++k)
             ok = wait_parity(smem_u32(&ax.tok_full[k & 1]), (k >> 1) & 1) && ok;
         if (!ok) aborted = true;
     }
@@ -862,16 +894,15 @@ constexpr int kMaxDevices = 64;
 
 struct DeviceInfo {
     int sms = 0;
-    bool smem_set[3][2][2] = {};  // [mode][ragged][batched]
+    bool smem_set[3][2][2][2] = {};  // [mode][ragged][batched][multi]
 };
 
 DeviceInfo g_dev[kMaxDevices];
 std::mutex g_dev_mutex;
 
-constexpr int NW = 4;  // warps per block
 static_assert(sizeof(Launch<kChunkMaxLayers>) <= 32764, "kernel parameter space");
 
-template <int MODE, bool RAGGED, int NL>
+template <int MODE, bool RAGGED, int NL, bool MULTI>
 cudaError_t launch_mode(const Launch<NL> &L, cudaStream_t stream) {
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
@@ -885,11 +916,11 @@ cudaError_t launch_mode(const Launch<NL> &L, cudaStream_t stream) {
             e = cudaDeviceGetAttribute(&info.sms, cudaDevAttrMultiProcessorCount, dev);
             if (e != cudaSuccess) return e;
         }
-        if (!info.smem_set[MODE][RAGGED][NL != 1]) {
-            e = cudaFuncSetAttribute(chunk_kernel<MODE, NW, RAGGED, NL>,
+        if (!info.smem_set[MODE][RAGGED][NL != 1][MULTI]) {
+            e = cudaFuncSetAttribute(chunk_kernel<MODE, RAGGED, NL, MULTI>,
                                      cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
             if (e != cudaSuccess) return e;
-            info.smem_set[MODE][RAGGED][NL != 1] = true;
+            info.smem_set[MODE][RAGGED][NL != 1][MULTI] = true;
         }
         sms = info.sms;
     }
@@ -898,7 +929,7 @@ cudaError_t launch_mode(const Launch<NL> &L, cudaStream_t stream) {
     const int grid = units < slots ? (int)units : slots;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)grid);
-    cfg.blockDim = dim3((unsigned)Cfg<NW>::kThreads);
+    cfg.blockDim = dim3((unsigned)kThreads);
     cfg.dynamicSmemBytes = kSmemBytes;
     cfg.stream = stream;
     cudaLaunchAttribute attr[1];
@@ -906,7 +937,7 @@ cudaError_t launch_mode(const Launch<NL> &L, cudaStream_t stream) {
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, chunk_kernel<MODE, NW, RAGGED, NL>, L);
+    return cudaLaunchKernelEx(&cfg, chunk_kernel<MODE, RAGGED, NL, MULTI>, L);
 }
 
 // The pool and token tensor maps of one layer.
@@ -932,6 +963,21 @@ cudaError_t encode_layer(const Args &p, Maps *maps) {
     return cudaSuccess;
 }
 
+template <int NL, bool MULTI>
+cudaError_t dispatch(const Launch<NL> &L, int mode, bool ragged, cudaStream_t stream) {
+    switch (mode) {
+        case kVerify:
+            return ragged ? launch_mode<kVerify, true, NL, MULTI>(L, stream)
+                          : launch_mode<kVerify, false, NL, MULTI>(L, stream);
+        case kCommit:
+            return ragged ? launch_mode<kCommit, true, NL, MULTI>(L, stream)
+                          : launch_mode<kCommit, false, NL, MULTI>(L, stream);
+        default:
+            return ragged ? launch_mode<kFused, true, NL, MULTI>(L, stream)
+                          : launch_mode<kFused, false, NL, MULTI>(L, stream);
+    }
+}
+
 template <int NL>
 cudaError_t launch_layers(const Args *layers, int n, int mode, cudaStream_t stream) {
     Launch<NL> L = {};
@@ -942,23 +988,14 @@ cudaError_t launch_layers(const Args *layers, int n, int mode, cudaStream_t stre
         if (e != cudaSuccess) return e;
     }
     const bool ragged = layers[0].cu_seqlens != nullptr;
-    switch (mode) {
-        case kVerify:
-            return ragged ? launch_mode<kVerify, true, NL>(L, stream)
-                          : launch_mode<kVerify, false, NL>(L, stream);
-        case kCommit:
-            return ragged ? launch_mode<kCommit, true, NL>(L, stream)
-                          : launch_mode<kCommit, false, NL>(L, stream);
-        default:
-            return ragged ? launch_mode<kFused, true, NL>(L, stream)
-                          : launch_mode<kFused, false, NL>(L, stream);
-    }
+    if (layers[0].max_T > CT) return dispatch<NL, true>(L, mode, ragged, stream);
+    return dispatch<NL, false>(L, mode, ragged, stream);
 }
 
 }  // namespace
 
 bool chunk_supported(bool bf16, int dk, int dv, int max_T) {
-    return bf16 && dk == D && dv == D && max_T >= 1 && max_T <= CT;
+    return bf16 && dk == D && dv == D && max_T >= 1;
 }
 
 bool chunk_preferred(int max_T) { return max_T >= 1; }

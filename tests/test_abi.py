@@ -95,7 +95,7 @@ def call(lib, fn, c, o=O_PTR, acc=ACC_PTR):
     (dict(cu_seqlens=(1 << 40) + 11 * (1 << 32), n_tok=-1), 2),
     (dict(qkv_dtype=5), 3),
     (dict(dk=48), 4), (dict(dk=256), 4), (dict(dv=48), 4), (dict(dv=160), 4), (dict(algo=9), 4),
-    (dict(algo=2, qkv_dtype=0), 4), (dict(algo=2, max_T=17), 4),
+    (dict(algo=2, qkv_dtype=0), 4), (dict(algo=2, dk=64, dv=64), 4),
     (dict(pool=None), 1), (dict(slot_ids=None), 1), (dict(q=None), 1), (dict(beta=None), 1),
     (dict(q=(1 << 40) + 8), 7), (dict(pool=(1 << 40) + 5 * (1 << 32) + 4), 7),
     (dict(alpha=(1 << 40) + 3 * (1 << 32) + 2), 7),
@@ -126,7 +126,8 @@ def test_select_algo(lib):
     assert lib.gdn_select_algo(ctypes.byref(fake_problem(algo=1))) == 1
     assert lib.gdn_select_algo(ctypes.byref(fake_problem(qkv_dtype=0))) == 1
     assert lib.gdn_select_algo(ctypes.byref(fake_problem(dk=64))) == 1
-    assert lib.gdn_select_algo(ctypes.byref(fake_problem(max_T=17))) == 1
+    assert lib.gdn_select_algo(ctypes.byref(fake_problem(max_T=17))) == binding.GDN_ALGO_CHUNK
+    assert lib.gdn_select_algo(ctypes.byref(fake_problem(max_T=1024))) == binding.GDN_ALGO_CHUNK
     assert lib.gdn_select_algo(ctypes.byref(fake_problem(dk=48))) == -1
     assert lib.gdn_select_algo(ctypes.byref(fake_problem(max_T=4096))) == -1
 

@@ -54,6 +54,15 @@ SMALL = {
                                       dv=128, T=16, pool_slots=8, accept="zero", seed=20),
     "accept_full_b4_d128_t16": custom("accept_full_b4_d128_t16", batch=4, heads=2, dk=128,
                                       dv=128, T=16, pool_slots=8, accept="full", seed=21),
+    # several 16-token chunks per unit: lengths across chunk boundaries, commit
+    # points in every chunk and on a boundary
+    "ragged_multichunk_b7_d128": custom("ragged_multichunk_b7_d128", batch=7, heads=2, dk=128,
+                                        dv=128, lengths=[1, 16, 17, 33, 48, 31, 64],
+                                        pool_slots=9, seed=22),
+    "b3_h2_d128_t64_full": custom("b3_h2_d128_t64_full", batch=3, heads=2, dk=128, dv=128,
+                                  T=64, pool_slots=3, accept="full", seed=23),
+    "b2_h2_d128_t200": custom("b2_h2_d128_t200", batch=2, heads=2, dk=128, dv=128, T=200,
+                              pool_slots=2, seed=24),
 }
 
 _cache = {}
