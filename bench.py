@@ -236,7 +236,7 @@ def run_ours(args, rank, world, local_rank):
     n_layers = inputs.WORKLOADS[name].get("layers", 1)
     if args.layers:
         n_layers = min(n_layers, args.layers)
-    layers = [inputs.make_problem(name, layer=l) for l in range(n_layers)]
+    layers = [inputs.make_problem(name, layer=l, draft=args.draft) for l in range(n_layers)]
     L = len(layers)
     p0 = layers[0]
     multi = "layers" in inputs.WORKLOADS[name]
@@ -468,6 +468,9 @@ def main():
     ap.add_argument("--ref-units", type=int, default=64)
     ap.add_argument("--e2e-steps", type=int, default=20)
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--draft", type=int, default=None,
+                    help="replace the draft length of a uniform workload (longer drafts run as "
+                         "several 16-token chunks)")
     ap.add_argument("--with-accept", action="store_true",
                     help="start every step with the on-device greedy accept-length call")
     ap.add_argument("--batch-layers", action="store_true",

@@ -13,10 +13,12 @@ state after a_r tokens; a request with a_r = 0 leaves its slot untouched
 (ReplaySSM keeps the accepted prefix and rolls the rest back, OCRia write-up,
 section "Make speculative verification cheaper").
 
-The greedy accept-length rule lives in `accept.py` (pure Python loops).
+The greedy accept-length rule lives in `accept.py` (pure Python loops); the
+ReplaySSM buffer (checkpoint plus buffered rows, periodic flush) in `replay.py`,
+which runs this recurrence over the replayed rows.
 
 Parity unpinned: none.  Every function here is pinned by `tests/test_oracle_pins.py`
-and `tests/test_accept_oracle.py`.
+and `tests/test_accept_oracle.py` and `tests/test_replay_oracle.py`.
 """
 from __future__ import annotations
 
@@ -30,6 +32,7 @@ from typing import Optional, Sequence
 import numpy as np
 
 from .accept import accept_prefix  # noqa: F401  (greedy accept length)
+from .replay import replay_commit, replay_verify  # noqa: F401  (ReplaySSM buffer)
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 _SRC = os.path.join(_HERE, "gdn_oracle.c")

@@ -37,6 +37,7 @@ __all__ = [
     "make_custom",
     "make_layers",
     "make_token_ids",
+    "make_replay",
     "random_token_ids",
     "POOL_SENTINEL_BITS",
 ]
@@ -200,9 +201,16 @@ def _recipe_kwargs(name: str) -> dict:
     return spec
 
 
-def make_problem(name: str, layer: int = 0) -> Problem:
-    """The named workload (one layer of it for the multi-layer one)."""
-    return make_custom(name=name, layer=layer, **_recipe_kwargs(name))
+def make_problem(name: str, layer: int = 0, draft: Optional[int] = None) -> Problem:
+    """The named workload (one layer of it for the multi-layer one).  `draft`
+    replaces the draft length of a uniform workload (accepted lengths keep
+    their distribution, over the new length)."""
+    kw = _recipe_kwargs(name)
+    if draft is not None:
+        if "T" not in kw:
+            raise ValueError(f"{name} has ragged drafts")
+        kw["T"] = int(draft)
+    return make_custom(name=name, layer=layer, **kw)
 
 
 def make_layers(name: str) -> List[Problem]:
@@ -240,3 +248,36 @@ def random_token_ids(lengths: Sequence[int], seed: int, p_differ: float = 0.1, v
     differ = rng.random(n) < p_differ
     target = np.where(differ, (draft + 1 + rng.integers(0, vocab - 1, size=n)) % vocab, draft)
     return cu, draft.astype(np.int32), target.astype(np.int32)
+
+
+def make_replay(prob: Problem, capacity: int, seed: int = 0,
+                len_in: Optional[np.ndarray] = None) -> dict:
+    """A ReplaySSM buffer for `prob`: `capacity` rows per pool slot in the token
+    layout (k [slots*C][H][dk], v [slots*C][H][dv], alpha/beta [slots*C][H]),
+    and len_in[slot], the rows already buffered.  For a named slot len_in is
+    uniform on [0, C - T_r] (room for the drafts) unless given; its rows are
+    drawn like the workload's tokens, and request r's drafts are copied to
+    rows slot*C + len_in + [0, T_r).  Rows of unnamed slots are zero (alpha 1)."""
+    C = int(capacity)
+    if prob.batch and C < prob.max_T:
+        raise ValueError("capacity below the draft length")
+    rng = np.random.default_rng(np.random.SeedSequence([seed, 90]))
+    S, H = prob.pool_slots, prob.heads
+    k = np.zeros((S * C, H, prob.dk), np.float32)
+    v = np.zeros((S * C, H, prob.dv), np.float32)
+    alpha = np.ones((S * C, H), np.float32)
+    beta = np.zeros((S * C, H), np.float32)
+    lens = np.zeros(S, np.int32) if len_in is None else np.array(len_in, np.int32, copy=True)
+    for r in range(prob.batch):
+        s, T, c0 = int(prob.slot_ids[r]), int(prob.lengths[r]), int(prob.cu_seqlens[r])
+        if len_in is None:
+            lens[s] = rng.integers(0, C - T + 1)
+        _, ks, vs, al, be = _draw_tokens(rng, C, H, prob.dk, prob.dv, prob.qkv_dtype)
+        n = int(lens[s])
+        if n + T > C:
+            raise ValueError("buffered rows plus drafts exceed the capacity")
+        ks[n:n + T], vs[n:n + T] = prob.k[c0:c0 + T], prob.v[c0:c0 + T]
+        al[n:n + T], be[n:n + T] = prob.alpha[c0:c0 + T], prob.beta[c0:c0 + T]
+        k[s * C:(s + 1) * C], v[s * C:(s + 1) * C] = ks, vs
+        alpha[s * C:(s + 1) * C], beta[s * C:(s + 1) * C] = al, be
+    return dict(capacity=C, k=k, v=v, alpha=alpha, beta=beta, len_in=lens)
