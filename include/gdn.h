@@ -96,6 +96,7 @@ typedef enum gdn_algo {
 #define GDN_DEVERR_ACCEPTED 2   /* accepted[r] outside [0, T_r]        */
 #define GDN_DEVERR_SEQLEN   4   /* cu[r+1] - cu[r] outside [0, max_T], or rows outside [0, n_tok) */
 #define GDN_DEVERR_TIMEOUT  8   /* an internal pipeline wait gave up (about 2 s); results incomplete */
+#define GDN_DEVERR_REPLAY  16   /* replay buffer: len_in[slot] < 0, or buffered plus new rows > capacity */
 
 /* Limits checked on the host. */
 #define GDN_MAX_T 1024          /* draft tokens per request */
@@ -183,6 +184,52 @@ GDN_API gdn_status gdn_accept_prefix(int32_t batch, int32_t max_T, const int32_t
                                      int64_t n_tok, const int32_t *draft_ids,
                                      const int32_t *target_ids, int32_t *accepted,
                                      int32_t *dev_err, cudaStream_t stream);
+
+/* ReplaySSM buffer (multi-step speculation).  ReplaySSM keeps a checkpoint of
+ * the state next to a small buffer of recent inputs, computes outputs from
+ * both, writes the full checkpoint only at periodic flushes, and rolls a
+ * rejection back by moving the buffer pointer (OCRia write-up, section "Make
+ * speculative verification cheaper").  Here pool[slot] is the checkpoint as
+ * of the slot's last flush, and the slot's buffer holds the rows accepted
+ * since then: rows slot * capacity + [0, len_in[slot]) of k, v, alpha, beta
+ * (the layout of the token arrays, with pool_slots * capacity rows).
+ *
+ * A step, for request r in slot s with n = len_in[s]:
+ *   1. the caller writes the step's draft rows of k, v, alpha, beta at buffer
+ *      rows s * capacity + n + [0, T_r) (n + T_r <= capacity), and q as usual
+ *      at rows cu[r] + [0, T_r) of p->q;
+ *   2. gdn_replay_verify: o for the draft rows (rows cu[r] + t of o), from
+ *      pool[s] and buffer rows [0, n + T_r); writes neither pool nor buffer;
+ *   3. gdn_replay_commit with accepted[r] = a_r: keep = n + a_r.  If
+ *      keep + max_T > capacity (a full next draft would not fit) the slot is
+ *      flushed: pool[s][h] <- the state after buffer rows [0, keep) and
+ *      len_out[s] = 0; otherwise the pool is not touched and len_out[s] = keep
+ *      (rejected rows are overwritten by the next step's drafts);
+ *   4. the caller swaps len_in and len_out for the next step.
+ * Only the chunked kernel runs these calls (bf16 q/k/v, dk = dv = 128);
+ * other shapes return GDN_ERR_UNSUPPORTED.  p->k, p->v, p->alpha and p->beta
+ * are not used (the buffer holds those rows); every other field of p means
+ * what it means for gdn_verify and gdn_commit.  A unit whose buffer does not
+ * hold its rows (n < 0, n + T_r > capacity in verify, keep > capacity in
+ * commit) sets GDN_DEVERR_REPLAY and is skipped; len_out[s] is then not
+ * written.  len_out[s] is written for every named slot, by one thread;
+ * entries of other slots are left as they are. */
+typedef struct gdn_replay {
+    int32_t capacity;            /* buffer rows per slot, >= max_T */
+    int32_t reserved;            /* must be 0 */
+    const void *k;               /* device [pool_slots * capacity][heads][dk], qkv_dtype, 16-byte aligned */
+    const void *v;               /* device [pool_slots * capacity][heads][dv], 16-byte aligned */
+    const float *alpha;          /* device [pool_slots * capacity][heads] */
+    const float *beta;           /* device [pool_slots * capacity][heads] */
+    const int32_t *len_in;       /* device [pool_slots]: rows buffered in each slot */
+    int32_t *len_out;            /* device [pool_slots]: written by gdn_replay_commit; must not
+                                    overlap len_in or any other array */
+} gdn_replay;
+
+GDN_API gdn_status gdn_replay_verify(const gdn_problem *p, const gdn_replay *rb, float *o,
+                                     cudaStream_t stream);
+GDN_API gdn_status gdn_replay_commit(const gdn_problem *p, const gdn_replay *rb,
+                                     const int32_t *accepted, cudaStream_t stream);
 
 /* Waits for `stream`, copies *p->dev_err to *host_code (0 when dev_err is NULL).
  * Returns GDN_ERR_DEVICE_ARG when the word is non-zero, GDN_OK when it is zero. */

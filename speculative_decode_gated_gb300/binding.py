@@ -22,14 +22,15 @@ GDN_ERR_ALIAS, GDN_ERR_LAYER_MISMATCH = 8, 9
 GDN_FP32, GDN_BF16 = 0, 1
 GDN_ALGO_AUTO, GDN_ALGO_RECURRENT, GDN_ALGO_CHUNK = 0, 1, 2
 GDN_DEVERR_SLOT, GDN_DEVERR_ACCEPTED, GDN_DEVERR_SEQLEN = 1, 2, 4
+GDN_DEVERR_TIMEOUT, GDN_DEVERR_REPLAY = 8, 16
 GDN_MAX_T = 1024
 
 # Every symbol include/gdn.h declares.
 EXPORTED = (
     "gdn_verify", "gdn_commit", "gdn_verify_commit_fused",
     "gdn_verify_layers", "gdn_commit_layers", "gdn_verify_commit_fused_layers",
-    "gdn_accept_prefix", "gdn_read_device_error", "gdn_select_algo", "gdn_status_string", "gdn_last_error_string",
-    "gdn_version",
+    "gdn_accept_prefix", "gdn_replay_verify", "gdn_replay_commit", "gdn_read_device_error",
+    "gdn_select_algo", "gdn_status_string", "gdn_last_error_string", "gdn_version",
 )
 
 
@@ -56,6 +57,16 @@ class gdn_problem(ctypes.Structure):
     ]
 
 
+class gdn_replay(ctypes.Structure):
+    """Mirror of the C struct gdn_replay (include/gdn.h), field for field."""
+
+    _fields_ = [
+        ("capacity", ctypes.c_int32), ("reserved", ctypes.c_int32),
+        ("k", ctypes.c_void_p), ("v", ctypes.c_void_p), ("alpha", ctypes.c_void_p),
+        ("beta", ctypes.c_void_p), ("len_in", ctypes.c_void_p), ("len_out", ctypes.c_void_p),
+    ]
+
+
 _lib_handle: Optional[ctypes.CDLL] = None
 
 
@@ -77,12 +88,16 @@ def lib() -> ctypes.CDLL:
         h.gdn_commit_layers.argtypes = [P, I32, S, S]
         h.gdn_verify_commit_fused_layers.argtypes = [P, I32, S, S, S]
         h.gdn_accept_prefix.argtypes = [I32, I32, S, ctypes.c_int64, S, S, S, S, S]
+        R = ctypes.POINTER(gdn_replay)
+        h.gdn_replay_verify.argtypes = [P, R, S, S]
+        h.gdn_replay_commit.argtypes = [P, R, S, S]
         h.gdn_read_device_error.argtypes = [P, S, ctypes.POINTER(ctypes.c_int32)]
         h.gdn_select_algo.argtypes = [P]
         h.gdn_status_string.argtypes = [ctypes.c_int]
         for name in ("gdn_verify", "gdn_commit", "gdn_verify_commit_fused",
                      "gdn_verify_layers", "gdn_commit_layers", "gdn_verify_commit_fused_layers",
-                     "gdn_accept_prefix", "gdn_read_device_error", "gdn_select_algo"):
+                     "gdn_accept_prefix", "gdn_replay_verify", "gdn_replay_commit",
+                     "gdn_read_device_error", "gdn_select_algo"):
             getattr(h, name).restype = ctypes.c_int
         for name in ("gdn_status_string", "gdn_last_error_string", "gdn_version"):
             getattr(h, name).restype = ctypes.c_char_p
@@ -247,6 +262,52 @@ def gdn_accept_prefix(draft_ids: torch.Tensor, target_ids: torch.Tensor, accepte
                                  _ptr(draft_ids), _ptr(target_ids), _ptr(accepted), _ptr(dev_err),
                                  _stream(stream))
     _raise(st, "gdn_accept_prefix")
+
+
+class Replay:
+    """A gdn_replay plus references to the tensors it points into."""
+
+    def __init__(self, c: gdn_replay, refs: tuple):
+        self.c = c
+        self.refs = refs
+
+    @property
+    def ref(self):
+        return ctypes.byref(self.c)
+
+    def swap_lengths(self) -> None:
+        """len_in <-> len_out, for the next step."""
+        self.c.len_in, self.c.len_out = self.c.len_out, self.c.len_in
+        self.refs = self.refs[:4] + (self.refs[5], self.refs[4])
+
+
+def make_replay(*, capacity: int, k: torch.Tensor, v: torch.Tensor, alpha: torch.Tensor,
+                beta: torch.Tensor, len_in: torch.Tensor, len_out: torch.Tensor) -> Replay:
+    """k: [slots*capacity, H, dk], v: [slots*capacity, H, dv] (the q/k/v dtype);
+    alpha, beta: [slots*capacity, H] fp32; len_in, len_out: [slots] int32."""
+    dev = len_in.device
+    _check(k, "k", (torch.bfloat16, torch.float32), dev)
+    _check(v, "v", (k.dtype,), dev)
+    for t, n in ((alpha, "alpha"), (beta, "beta")):
+        _check(t, n, (torch.float32,), dev)
+    for t, n in ((len_in, "len_in"), (len_out, "len_out")):
+        _check(t, n, (torch.int32,), dev)
+    c = gdn_replay()
+    c.capacity, c.reserved = int(capacity), 0
+    c.k, c.v, c.alpha, c.beta = _ptr(k), _ptr(v), _ptr(alpha), _ptr(beta)
+    c.len_in, c.len_out = _ptr(len_in), _ptr(len_out)
+    return Replay(c, (k, v, alpha, beta, len_in, len_out))
+
+
+def gdn_replay_verify(prob: Problem, rb: Replay, o: torch.Tensor, stream=None) -> None:
+    _check(o, "o", (torch.float32,), None)
+    _raise(lib().gdn_replay_verify(prob.ref, rb.ref, _ptr(o), _stream(stream)), "gdn_replay_verify")
+
+
+def gdn_replay_commit(prob: Problem, rb: Replay, accepted: torch.Tensor, stream=None) -> None:
+    _check(accepted, "accepted", (torch.int32,), None)
+    _raise(lib().gdn_replay_commit(prob.ref, rb.ref, _ptr(accepted), _stream(stream)),
+           "gdn_replay_commit")
 
 
 def gdn_read_device_error(prob: Problem, stream=None) -> int:

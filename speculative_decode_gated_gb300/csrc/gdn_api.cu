@@ -44,16 +44,18 @@ struct LayerRanges {
     Range q, k, v, alpha, beta, pool;
 };
 
-LayerRanges layer_ranges(const gdn_problem *p) {
+// kv_rows: rows of k, v, alpha and beta (-1: the token rows).
+LayerRanges layer_ranges(const gdn_problem *p, int64_t kv_rows = -1) {
     const int64_t H = p->heads;
     const int64_t n_tok = token_rows(p);
+    const int64_t nkv = kv_rows < 0 ? n_tok : kv_rows;
     const int64_t esz = p->qkv_dtype == GDN_BF16 ? 2 : 4;
     LayerRanges r;
     r.q = range(p->q, n_tok * H * p->dk * esz);
-    r.k = range(p->k, n_tok * H * p->dk * esz);
-    r.v = range(p->v, n_tok * H * p->dv * esz);
-    r.alpha = range(p->alpha, n_tok * H * 4);
-    r.beta = range(p->beta, n_tok * H * 4);
+    r.k = range(p->k, nkv * H * p->dk * esz);
+    r.v = range(p->v, nkv * H * p->dv * esz);
+    r.alpha = range(p->alpha, nkv * H * 4);
+    r.beta = range(p->beta, nkv * H * 4);
     r.pool = range(p->pool, p->pool_slots * H * p->dk * p->dv * 4);
     return r;
 }
@@ -87,7 +89,7 @@ int resolve_algo(const gdn_problem *p) {
 // Host validation shared by all entry points.  On success *algo is the kernel
 // to run and *empty tells whether there is nothing to launch.
 gdn_status validate(const gdn_problem *p, bool with_o, const float *o, bool with_acc,
-                    const int32_t *accepted, int *algo, bool *empty) {
+                    const int32_t *accepted, int *algo, bool *empty, int64_t kv_rows = -1) {
     if (!p) return GDN_ERR_NULL_PTR;
     if (p->reserved != 0 || !shape_ok(p)) return GDN_ERR_BAD_DIM;
     if (p->qkv_dtype != GDN_FP32 && p->qkv_dtype != GDN_BF16) return GDN_ERR_BAD_DTYPE;
@@ -110,7 +112,7 @@ gdn_status validate(const gdn_problem *p, bool with_o, const float *o, bool with
         return GDN_ERR_ALIGN;
 
     // Aliasing: o must not overlap any input; the pool must not overlap q/k/v/gates/metadata.
-    const LayerRanges lr = layer_ranges(p);
+    const LayerRanges lr = layer_ranges(p, kv_rows);
     const Range rq = lr.q, rk = lr.k, rv = lr.v, ra = lr.alpha, rb = lr.beta, rp = lr.pool;
     const Range rs = range(p->slot_ids, (int64_t)p->batch * 4);
     const Range rc = range(p->cu_seqlens, p->cu_seqlens ? ((int64_t)p->batch + 1) * 4 : 0);
@@ -148,6 +150,7 @@ gdn::Args make_args(const gdn_problem *p, const int32_t *accepted, float *o) {
     a.accepted = accepted;
     a.o = o;
     a.dev_err = p->dev_err;
+    a.kv_rows = a.n_tok;
     return a;
 }
 
@@ -236,6 +239,53 @@ gdn_status run_layers(const gdn_problem *ps, int32_t n, int mode, const int32_t 
     return GDN_OK;
 }
 
+gdn_status run_replay(const gdn_problem *p, const gdn_replay *rb, int mode,
+                      const int32_t *accepted, float *o, cudaStream_t stream) {
+    if (!p || !rb) return GDN_ERR_NULL_PTR;
+    if (rb->reserved != 0 || rb->capacity < 1) return GDN_ERR_BAD_DIM;
+    // The problem as the kernel sees it: k, v and the gates come from the buffer.
+    gdn_problem pp = *p;
+    pp.k = rb->k;
+    pp.v = rb->v;
+    pp.alpha = rb->alpha;
+    pp.beta = rb->beta;
+    const int64_t kv_rows = p->pool_slots * (int64_t)rb->capacity;
+    const bool with_o = mode == gdn::kVerify;
+    const bool with_acc = mode == gdn::kCommit;
+    int algo = 0;
+    bool empty = false;
+    gdn_status st = validate(&pp, with_o, o, with_acc, accepted, &algo, &empty, kv_rows);
+    if (st != GDN_OK) return st;
+    if (algo != GDN_ALGO_CHUNK) return GDN_ERR_UNSUPPORTED;
+    if (empty) return GDN_OK;
+    if (rb->capacity < p->max_T || kv_rows > (1ll << 31)) return GDN_ERR_BAD_DIM;
+    if (!rb->len_in || (with_acc && !rb->len_out)) return GDN_ERR_NULL_PTR;
+    if (!aligned4(rb->len_in) || !aligned4(rb->len_out)) return GDN_ERR_ALIGN;
+    if (with_acc) {
+        const Range rl = range(rb->len_out, p->pool_slots * 4);
+        const LayerRanges lr = layer_ranges(&pp, kv_rows);
+        const Range others[] = {lr.q, lr.k, lr.v, lr.alpha, lr.beta, lr.pool,
+                                range(rb->len_in, p->pool_slots * 4),
+                                range(p->slot_ids, (int64_t)p->batch * 4),
+                                range(p->cu_seqlens, p->cu_seqlens ? ((int64_t)p->batch + 1) * 4 : 0),
+                                range(accepted, (int64_t)p->batch * 4),
+                                range(p->dev_err, p->dev_err ? 4 : 0)};
+        for (const Range &x : others)
+            if (overlap(rl, x)) return GDN_ERR_ALIAS;
+    }
+    gdn::Args a = make_args(&pp, with_acc ? accepted : nullptr, with_o ? o : nullptr);
+    a.cap = rb->capacity;
+    a.kv_rows = kv_rows;
+    a.len_in = rb->len_in;
+    a.len_out = rb->len_out;
+    const cudaError_t e = gdn::launch_chunk(&a, 1, mode, stream);
+    if (e != cudaSuccess) {
+        set_cuda_error(e, "kernel launch");
+        return GDN_ERR_CUDA;
+    }
+    return GDN_OK;
+}
+
 }  // namespace
 
 extern "C" {
@@ -267,6 +317,16 @@ gdn_status gdn_verify_commit_fused_layers(const gdn_problem *problems, int32_t n
                                           const int32_t *accepted, float *const *o,
                                           cudaStream_t stream) {
     return run_layers(problems, n_layers, gdn::kFused, accepted, o, stream);
+}
+
+gdn_status gdn_replay_verify(const gdn_problem *p, const gdn_replay *rb, float *o,
+                             cudaStream_t stream) {
+    return run_replay(p, rb, gdn::kVerify, nullptr, o, stream);
+}
+
+gdn_status gdn_replay_commit(const gdn_problem *p, const gdn_replay *rb, const int32_t *accepted,
+                             cudaStream_t stream) {
+    return run_replay(p, rb, gdn::kCommit, accepted, nullptr, stream);
 }
 
 gdn_status gdn_accept_prefix(int32_t batch, int32_t max_T, const int32_t *cu_seqlens,

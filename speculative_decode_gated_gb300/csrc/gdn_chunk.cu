@@ -200,11 +200,15 @@ __device__ __forceinline__ uint32_t ld_tok32(const unsigned char *tile, int t, i
 // ------------------------------------------------------------ per-unit plan
 
 struct UnitPlan {
-    Unit u = {0, 0, -1, nullptr};
+    Unit u = {0, 0, -1, nullptr};  // u.row0: first row of k, v and the gates
     int h = 0;
     int layer = 0;  // which problem of the launch
     int tile = 0;   // slot * H + h: the tile's index in its layer's pool
-    int teff = 0;   // tokens that matter: T_r, or a_r for commit
+    int teff = 0;   // rows that matter: T_r, or a_r for commit (replay: buffered rows too)
+    int qrow0 = 0;  // row of q and o that goes with row u.row0
+    int nskip = 0;  // rows before this one have no output (replay: the buffered rows)
+    int slot = 0;
+    int n = 0;      // replay: rows buffered in the slot (loaded with the plan)
     bool skip = true;
 };
 
@@ -242,7 +246,7 @@ __device__ __forceinline__ RawMeta load_unit_meta(const Args &p, int w, int W, i
     return m;
 }
 
-template <int MODE, int NL>
+template <int MODE, int NL, bool REPLAY>
 __device__ __forceinline__ UnitPlan plan_unit(const Launch<NL> &L, int w, int U, const RawMeta &m) {
     UnitPlan pl;
     pl.layer = NL == 1 ? 0 : w / U;
@@ -251,9 +255,48 @@ __device__ __forceinline__ UnitPlan plan_unit(const Launch<NL> &L, int w, int U,
     pl.h = unit - (unit / p.H) * p.H;
     const bool ok = check_meta(p, m, pl.h, MODE, pl.u);
     pl.tile = ok ? m.slot * p.H + pl.h : 0;
+    pl.slot = ok ? m.slot : 0;
+    pl.qrow0 = pl.u.row0;
+    if (REPLAY) {
+        // The buffered length is only loaded here; finalize_replay uses it one
+        // iteration later, when this plan becomes the next unit.
+        pl.n = ok ? ld_early(p.len_in + m.slot) : 0;
+        pl.u.row0 = pl.slot * p.cap;
+        pl.skip = !ok;
+        return pl;
+    }
     pl.teff = ok ? ((MODE == kCommit) ? pl.u.a : pl.u.T) : 0;
     pl.skip = !ok || pl.teff == 0;
     return pl;
+}
+
+// Replay calls: the rows of a unit are its slot's buffer rows [0, n + T_r)
+// (verify: outputs for rows n.., at q/o rows cu[r] + row - n) or [0, keep)
+// with keep = n + a_r (commit: only when the slot is flushed, keep + max_T >
+// cap).  The commit also records the slot's new buffered length (once, by the
+// unit of head 0).  A unit whose rows leave the buffer reports
+// GDN_DEVERR_REPLAY and is skipped.
+template <int MODE>
+__device__ __forceinline__ void finalize_replay(const Args &p, UnitPlan &pl, int tid) {
+    if (pl.skip) return;  // its metadata was rejected (and reported) already
+    const int n = pl.n;
+    bool bad;
+    if (MODE == kVerify) {
+        bad = n < 0 || n + pl.u.T > p.cap;
+        pl.teff = n + pl.u.T;
+        pl.nskip = n;
+        pl.qrow0 -= n;  // q and o rows of the drafts start at cu[r]
+        pl.skip = bad || pl.u.T == 0;
+    } else {
+        const int keep = n + pl.u.a;
+        bad = n < 0 || keep > p.cap;
+        const bool flush = keep + p.max_T > p.cap;
+        if (!bad && pl.h == 0 && tid == 0) p.len_out[pl.slot] = flush ? 0 : keep;
+        pl.u.a = keep;
+        pl.teff = flush ? keep : 0;
+        pl.skip = bad || !flush || keep == 0;
+    }
+    if (bad && tid == 0 && p.dev_err) atomicOr(p.dev_err, GDN_DEVERR_REPLAY);
 }
 
 // Thread 0: the token boxes (k, v and, unless committing, q) of chunk `ch` of
@@ -262,13 +305,14 @@ template <int MODE>
 __device__ __forceinline__ void issue_tokens(const Maps &maps, const UnitPlan &pl, int ch,
                                              TokBuf &tb, uint32_t tok_bar) {
     const int row = pl.u.row0 + CT * ch;
+    const int qrow = pl.qrow0 + CT * ch;  // may be negative (replay): those rows read as zero
     mbar_arrive_expect_tx(tok_bar, (MODE == kCommit ? 2u : 3u) * kTokBytes);
 #pragma unroll
     for (int hb = 0; hb < 2; ++hb) {
         tma_load_3d(smem_u32(tb.k) + hb * kTokHalfBytes, &maps.k, 64 * hb, pl.h, row, tok_bar);
         tma_load_3d(smem_u32(tb.v) + hb * kTokHalfBytes, &maps.v, 64 * hb, pl.h, row, tok_bar);
         if (MODE != kCommit)
-            tma_load_3d(smem_u32(tb.q) + hb * kTokHalfBytes, &maps.q, 64 * hb, pl.h, row, tok_bar);
+            tma_load_3d(smem_u32(tb.q) + hb * kTokHalfBytes, &maps.q, 64 * hb, pl.h, qrow, tok_bar);
     }
 }
 
@@ -289,7 +333,7 @@ __device__ __forceinline__ void prefetch_unit(const Maps &maps, const UnitPlan &
     for (int hb = 0; hb < 2; ++hb) {
         tma_prefetch_3d(&maps.k, 64 * hb, pl.h, pl.u.row0);
         tma_prefetch_3d(&maps.v, 64 * hb, pl.h, pl.u.row0);
-        if (MODE != kCommit) tma_prefetch_3d(&maps.q, 64 * hb, pl.h, pl.u.row0);
+        if (MODE != kCommit) tma_prefetch_3d(&maps.q, 64 * hb, pl.h, pl.qrow0 > 0 ? pl.qrow0 : 0);
     }
 #pragma unroll
     for (int b = 0; b < 4; ++b) tma_prefetch_3d(&maps.pool, 32 * b, 0, pl.tile);
@@ -309,7 +353,7 @@ __device__ __forceinline__ int ld_l2(const int32_t *ptr) {
 // and read the current data from L2).  The metadata read here may be stale for
 // the same reason; it only picks addresses, clamped into the arrays, and is
 // read again after the wait.
-template <int MODE, bool RAGGED, int NL>
+template <int MODE, bool RAGGED, int NL, bool REPLAY>
 __device__ __forceinline__ void early_prefetch(const Launch<NL> &L, int w0, int G, int W, int U) {
     const Args &p = L.a[0];
     int h[2], row0[2], slot[2], layer[2];
@@ -331,6 +375,7 @@ __device__ __forceinline__ void early_prefetch(const Launch<NL> &L, int w0, int 
         const long long sl = slot[j] < 0 ? 0 : (slot[j] >= p.pool_slots ? p.pool_slots - 1 : slot[j]);
 #pragma unroll
         for (int hb = 0; hb < 2; ++hb) {
+            if (REPLAY) break;  // the buffered length is not known yet: the tile only
             tma_prefetch_3d(&maps.k, 64 * hb, h[j], (int)row);
             tma_prefetch_3d(&maps.v, 64 * hb, h[j], (int)row);
             if (MODE != kCommit) tma_prefetch_3d(&maps.q, 64 * hb, h[j], (int)row);
@@ -348,7 +393,7 @@ __device__ __forceinline__ float gate_load(const float *gate, const Args &p, con
                                            int ch, int tid) {
     const int left = pl.teff - CT * ch;
     long long row = (long long)pl.u.row0 + CT * ch + (tid < left ? tid : left - 1);
-    row = row < 0 ? 0 : (row >= p.n_tok ? p.n_tok - 1 : row);
+    row = row < 0 ? 0 : (row >= p.kv_rows ? p.kv_rows - 1 : row);
     const int h = pl.h < 0 ? 0 : (pl.h >= p.H ? p.H - 1 : pl.h);
     return ld_early(gate + (size_t)row * p.H + h);
 }
@@ -441,7 +486,7 @@ __device__ __forceinline__ void state_update(float (&hr)[8][4][CPT], const float
 // MULTI: units may have more than 16 tokens (several chunks, the state carried
 // in registers from one to the next); otherwise every unit is one chunk and
 // the verify kernel keeps no state in registers.
-template <int MODE, bool RAGGED, int NL, bool MULTI>
+template <int MODE, bool RAGGED, int NL, bool MULTI, bool REPLAY>
 __global__ void __launch_bounds__(kThreads, kBlocksPerSM)
     chunk_kernel(const __grid_constant__ Launch<NL> L) {
     extern __shared__ unsigned char smem_raw[];
@@ -476,7 +521,7 @@ __global__ void __launch_bounds__(kThreads, kBlocksPerSM)
                          : "memory");
     }
     __syncthreads();
-    if (tid == 0) early_prefetch<MODE, RAGGED, NL>(L, blockIdx.x, G, W, U);
+    if (tid == 0) early_prefetch<MODE, RAGGED, NL, REPLAY>(L, blockIdx.x, G, W, U);
     asm volatile("griddepcontrol.wait;" ::: "memory");
 
     // Plans: `cur` is the unit being computed, `nxt` the next one (its loads are
@@ -486,10 +531,13 @@ __global__ void __launch_bounds__(kThreads, kBlocksPerSM)
     RawMeta raw;
     cur.skip = true;
     nxt.skip = true;
-    if (unit < W)
-        cur = plan_unit<MODE, NL>(L, unit, U, load_unit_meta<MODE, RAGGED, NL>(p, unit, W, U));
+    if (unit < W) {
+        cur = plan_unit<MODE, NL, REPLAY>(L, unit, U, load_unit_meta<MODE, RAGGED, NL>(p, unit, W, U));
+        if (REPLAY) finalize_replay<MODE>(L.a[cur.layer], cur, tid);
+    }
     if (unit + G < W)
-        nxt = plan_unit<MODE, NL>(L, unit + G, U, load_unit_meta<MODE, RAGGED, NL>(p, unit + G, W, U));
+        nxt = plan_unit<MODE, NL, REPLAY>(L, unit + G, U,
+                                          load_unit_meta<MODE, RAGGED, NL>(p, unit + G, W, U));
     raw = load_unit_meta<MODE, RAGGED, NL>(p, unit + 2 * G, W, U);
 
     // A step is one 16-token chunk of one unit.  Step k (in the order this block
@@ -526,8 +574,9 @@ __global__ void __launch_bounds__(kThreads, kBlocksPerSM)
         // Advance the metadata pipeline.
         const UnitPlan me = cur;
         cur = nxt;
+        if (REPLAY) finalize_replay<MODE>(L.a[cur.layer], cur, tid);
         nxt.skip = true;
-        if (unit + 2 * G < W) nxt = plan_unit<MODE, NL>(L, unit + 2 * G, U, raw);
+        if (unit + 2 * G < W) nxt = plan_unit<MODE, NL, REPLAY>(L, unit + 2 * G, U, raw);
         raw = load_unit_meta<MODE, RAGGED, NL>(p, unit + 3 * G, W, U);
         if (me.skip) {
             // Gates of the next unit (consumed one iteration later).
@@ -662,6 +711,8 @@ __global__ void __launch_bounds__(kThreads, kBlocksPerSM)
             //    x_t = [t == j, t < T] - sum_{s<t} A[t][s] x_s gives zeros above
             //    the diagonal and in rows t >= T (A is zero there).
             constexpr int NT0 = (MODE == kCommit) ? 2 : 0;
+            // Replay: a chunk of buffered rows only has no outputs (no P, no O).
+            const bool outs = MODE != kCommit && (!REPLAY || CT * ch + T > me.nskip);
             const int tj = warp + NW * (lane % kTinvLanes);
             float xt[CT];
             float y[MT][4][4];
@@ -722,13 +773,17 @@ __global__ void __launch_bounds__(kThreads, kBlocksPerSM)
                     split2(hv[2][2 * m], hv[3][2 * m], ah[2], al[2]);
                     split2(hv[2][2 * m + 1], hv[3][2 * m + 1], ah[3], al[3]);
 #pragma unroll
-                    for (int nt = NT0; nt < 4; ++nt)
+                    for (int nt = NT0; nt < 4; ++nt) {
+                        if (nt < 2 && !outs) continue;
                         mma(y[m][nt][0], y[m][nt][1], y[m][nt][2], y[m][nt][3], ah[0], ah[1], ah[2],
                             ah[3], b[nt][0], b[nt][1]);
+                    }
 #pragma unroll
-                    for (int nt = NT0; nt < 4; ++nt)
+                    for (int nt = NT0; nt < 4; ++nt) {
+                        if (nt < 2 && !outs) continue;
                         mma(y[m][nt][0], y[m][nt][1], y[m][nt][2], y[m][nt][3], al[0], al[1], al[2],
                             al[3], b[nt][0], b[nt][1]);
+                    }
                 }
             }
 
@@ -794,7 +849,7 @@ __global__ void __launch_bounds__(kThreads, kBlocksPerSM)
             }
 
             // 8. O^T = P^T diag(gamma) + W^T M^T, stored as float2 pairs of adjacent columns.
-            if (MODE != kCommit) {
+            if (MODE != kCommit && outs) {
                 uint32_t bh[2][2], bl[2][2];
 #pragma unroll
                 for (int nt = 0; nt < 2; ++nt) {
@@ -802,8 +857,10 @@ __global__ void __launch_bounds__(kThreads, kBlocksPerSM)
                     split2(mr[2 * c], mr[2 * c + 1], bh[nt][0], bl[nt][0]);
                     split2(mr[2 * c + 8], mr[2 * c + 9], bh[nt][1], bl[nt][1]);
                 }
-                float *go = L.a[me.layer].o +
-                            ((size_t)(me.u.row0 + CT * ch) * p.H + me.h) * D + col0;
+                // Row t of this chunk is output row qrow0 + 16 ch + t; rows before
+                // nskip (replay: buffered rows) have none.
+                const long long orow = (long long)me.qrow0 + CT * ch;
+                float *go = L.a[me.layer].o + me.h * D + col0;
 #pragma unroll
                 for (int m = 0; m < MT; ++m) {
                     uint32_t ah[4], al[4];
@@ -820,11 +877,11 @@ __global__ void __launch_bounds__(kThreads, kBlocksPerSM)
                         mma(d[0], d[1], d[2], d[3], ah[0], ah[1], ah[2], ah[3], bh[nt][0], bh[nt][1]);
                         mma(d[0], d[1], d[2], d[3], ah[0], ah[1], ah[2], ah[3], bl[nt][0], bl[nt][1]);
                         mma(d[0], d[1], d[2], d[3], al[0], al[1], al[2], al[3], bh[nt][0], bh[nt][1]);
-                        if (t0 < T)
-                            *reinterpret_cast<float2 *>(go + t0 * row_stride + 2 * m) =
+                        if (t0 < T && CT * ch + t0 >= me.nskip)
+                            *reinterpret_cast<float2 *>(go + (orow + t0) * row_stride + 2 * m) =
                                 make_float2(d[0], d[2]);
-                        if (t0 + 1 < T)
-                            *reinterpret_cast<float2 *>(go + (t0 + 1) * row_stride + 2 * m) =
+                        if (t0 + 1 < T && CT * ch + t0 + 1 >= me.nskip)
+                            *reinterpret_cast<float2 *>(go + (orow + t0 + 1) * row_stride + 2 * m) =
                                 make_float2(d[1], d[3]);
                     }
                 }
@@ -894,7 +951,7 @@ constexpr int kMaxDevices = 64;
 
 struct DeviceInfo {
     int sms = 0;
-    bool smem_set[3][2][2][2] = {};  // [mode][ragged][batched][multi]
+    bool smem_set[3][2][2][2][2] = {};  // [mode][ragged][batched][multi][replay]
 };
 
 DeviceInfo g_dev[kMaxDevices];
@@ -902,7 +959,7 @@ std::mutex g_dev_mutex;
 
 static_assert(sizeof(Launch<kChunkMaxLayers>) <= 32764, "kernel parameter space");
 
-template <int MODE, bool RAGGED, int NL, bool MULTI>
+template <int MODE, bool RAGGED, int NL, bool MULTI, bool REPLAY = false>
 cudaError_t launch_mode(const Launch<NL> &L, cudaStream_t stream) {
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
@@ -916,11 +973,11 @@ cudaError_t launch_mode(const Launch<NL> &L, cudaStream_t stream) {
             e = cudaDeviceGetAttribute(&info.sms, cudaDevAttrMultiProcessorCount, dev);
             if (e != cudaSuccess) return e;
         }
-        if (!info.smem_set[MODE][RAGGED][NL != 1][MULTI]) {
-            e = cudaFuncSetAttribute(chunk_kernel<MODE, RAGGED, NL, MULTI>,
+        if (!info.smem_set[MODE][RAGGED][NL != 1][MULTI][REPLAY]) {
+            e = cudaFuncSetAttribute(chunk_kernel<MODE, RAGGED, NL, MULTI, REPLAY>,
                                      cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
             if (e != cudaSuccess) return e;
-            info.smem_set[MODE][RAGGED][NL != 1][MULTI] = true;
+            info.smem_set[MODE][RAGGED][NL != 1][MULTI][REPLAY] = true;
         }
         sms = info.sms;
     }
@@ -937,13 +994,14 @@ cudaError_t launch_mode(const Launch<NL> &L, cudaStream_t stream) {
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, chunk_kernel<MODE, RAGGED, NL, MULTI>, L);
+    return cudaLaunchKernelEx(&cfg, chunk_kernel<MODE, RAGGED, NL, MULTI, REPLAY>, L);
 }
 
 // The pool and token tensor maps of one layer.
 cudaError_t encode_layer(const Args &p, Maps *maps) {
     const unsigned long long tiles = (unsigned long long)p.pool_slots * (unsigned long long)p.H;
-    if (tiles == 0 || tiles > (1ull << 31) || p.n_tok < 1 || p.n_tok > (1ll << 31))
+    if (tiles == 0 || tiles > (1ull << 31) || p.n_tok < 1 || p.n_tok > (1ll << 31) ||
+        p.kv_rows < 1 || p.kv_rows > (1ll << 31))
         return cudaErrorInvalidValue;
     PFN_cuTensorMapEncodeTiled_v12000 encode = encode_fn();
     if (!encode) return cudaErrorNotSupported;
@@ -956,8 +1014,8 @@ cudaError_t encode_layer(const Args &p, Maps *maps) {
                CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
         return cudaErrorInvalidValue;
-    if (!encode_tokens(encode, &maps->k, p.k, p.H, p.n_tok) ||
-        !encode_tokens(encode, &maps->v, p.v, p.H, p.n_tok) ||
+    if (!encode_tokens(encode, &maps->k, p.k, p.H, p.kv_rows) ||
+        !encode_tokens(encode, &maps->v, p.v, p.H, p.kv_rows) ||
         !encode_tokens(encode, &maps->q, p.q, p.H, p.n_tok))
         return cudaErrorInvalidValue;
     return cudaSuccess;
@@ -988,6 +1046,16 @@ cudaError_t launch_layers(const Args *layers, int n, int mode, cudaStream_t stre
         if (e != cudaSuccess) return e;
     }
     const bool ragged = layers[0].cu_seqlens != nullptr;
+    if (layers[0].cap > 0) {  // replay buffer (single problems): verify or commit
+        if constexpr (NL == 1) {
+            if (mode == kVerify)
+                return ragged ? launch_mode<kVerify, true, NL, true, true>(L, stream)
+                              : launch_mode<kVerify, false, NL, true, true>(L, stream);
+            return ragged ? launch_mode<kCommit, true, NL, true, true>(L, stream)
+                          : launch_mode<kCommit, false, NL, true, true>(L, stream);
+        }
+        return cudaErrorNotSupported;
+    }
     if (layers[0].max_T > CT) return dispatch<NL, true>(L, mode, ragged, stream);
     return dispatch<NL, false>(L, mode, ragged, stream);
 }

@@ -27,6 +27,12 @@ struct Args {
     const int32_t *accepted;  // NULL for verify
     float *o;                 // NULL for commit
     int32_t *dev_err;
+    // ReplaySSM buffer (replay calls only; k, v, alpha, beta then point into
+    // the buffer, whose rows are slot * cap + row).
+    int cap = 0;              // rows per slot, 0 when there is no buffer
+    long long kv_rows = 0;    // rows of k, v, alpha, beta: n_tok, or pool_slots * cap
+    const int32_t *len_in = nullptr;
+    int32_t *len_out = nullptr;
 };
 
 // Token range, accepted length and state tile of one (request r, head h).

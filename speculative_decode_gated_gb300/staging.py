@@ -45,7 +45,7 @@ class DeviceProblem:
 
     def __init__(self, prob: Problem, device="cuda", pool: Optional[torch.Tensor] = None,
                  pool_fill: str = "sentinel", algo: int = binding.GDN_ALGO_AUTO,
-                 with_dev_err: bool = True):
+                 with_dev_err: bool = True, place_s0: bool = True):
         self.host = prob
         dev = torch.device(device)
         self.q = qkv_tensor(prob.q, prob.qkv_dtype, dev)
@@ -60,7 +60,8 @@ class DeviceProblem:
         if pool is None:
             pool = new_pool(prob.pool_slots, prob.heads, prob.dk, prob.dv, dev, pool_fill)
         self.pool = pool
-        place_checkpoints(self.pool, prob)
+        if place_s0:  # else the pool already holds the states (a later step)
+            place_checkpoints(self.pool, prob)
         self.dev_err = torch.zeros(1, dtype=torch.int32, device=dev) if with_dev_err else None
         self.o = torch.zeros((prob.n_tok, prob.heads, prob.dv), dtype=torch.float32, device=dev)
         self.algo = algo
@@ -130,3 +131,46 @@ def layers_launcher(dps, mode: str, stream):
             raise binding.GdnError(st, f"gdn {mode} layers")
     call.keep = (arr, o)
     return call
+
+
+class DeviceReplay:
+    """Device copies of a ReplaySSM buffer (inputs.make_replay) and its C struct.
+    len_out starts as a copy of len_in."""
+
+    def __init__(self, buf: dict, qkv_dtype: str, device="cuda"):
+        dev = torch.device(device)
+        self.capacity = int(buf["capacity"])
+        self.k = qkv_tensor(buf["k"], qkv_dtype, dev)
+        self.v = qkv_tensor(buf["v"], qkv_dtype, dev)
+        self.alpha = torch.from_numpy(np.ascontiguousarray(buf["alpha"], np.float32)).to(dev)
+        self.beta = torch.from_numpy(np.ascontiguousarray(buf["beta"], np.float32)).to(dev)
+        self.len_in = torch.from_numpy(np.ascontiguousarray(buf["len_in"], np.int32)).to(dev)
+        self.len_out = self.len_in.clone()
+        self.c = binding.make_replay(capacity=self.capacity, k=self.k, v=self.v, alpha=self.alpha,
+                                     beta=self.beta, len_in=self.len_in, len_out=self.len_out)
+
+    def swap(self) -> None:
+        """The lengths written by the last commit become the next step's input."""
+        self.len_in, self.len_out = self.len_out, self.len_in
+        self.c.swap_lengths()
+
+    def place_drafts(self, d: "DeviceProblem") -> None:
+        """Copy the step's draft rows (k, v, alpha, beta of `d`) to buffer rows
+        slot * C + len_in[slot] + [0, T_r): what an engine's projection
+        kernels would write there."""
+        prob = d.host
+        lens = torch.from_numpy(prob.lengths.astype(np.int64)).to(self.k.device)
+        cu = torch.from_numpy(prob.cu_seqlens[:-1].astype(np.int64)).to(self.k.device)
+        slots = d.slot_ids.long()
+        req = torch.repeat_interleave(torch.arange(prob.batch, device=self.k.device), lens)
+        t = torch.arange(int(lens.sum()), device=self.k.device) - cu[req]
+        dst = slots[req] * self.capacity + self.len_in.long()[slots[req]] + t
+        src = cu[req] + t
+        for buf, x in ((self.k, d.k), (self.v, d.v), (self.alpha, d.alpha), (self.beta, d.beta)):
+            buf[dst] = x[src]
+
+    def host(self) -> dict:
+        """The buffer as inputs.make_replay lays it out (float32 numpy)."""
+        return dict(capacity=self.capacity, k=self.k.float().cpu().numpy(),
+                    v=self.v.float().cpu().numpy(), alpha=self.alpha.cpu().numpy(),
+                    beta=self.beta.cpu().numpy(), len_in=self.len_in.cpu().numpy())

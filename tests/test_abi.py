@@ -40,20 +40,22 @@ def test_library_exports_every_declared_symbol(lib):
         assert hasattr(lib, name)
 
 
-def test_struct_layout_matches_c(tmp_path):
-    fields = [f[0] for f in binding.gdn_problem._fields_]
+@pytest.mark.parametrize("cls,cname", [(binding.gdn_problem, "gdn_problem"),
+                                       (binding.gdn_replay, "gdn_replay")])
+def test_struct_layout_matches_c(tmp_path, cls, cname):
+    fields = [f[0] for f in cls._fields_]
     prog = tmp_path / "layout.c"
-    body = "\n".join(f'printf("%zu ", offsetof(gdn_problem, {f}));' for f in fields)
+    body = "\n".join(f'printf("%zu ", offsetof({cname}, {f}));' for f in fields)
     prog.write_text(f'#include <stdio.h>\n#include <stddef.h>\n#include "gdn.h"\n'
-                    f'int main(void) {{ {body} printf("%zu\\n", sizeof(gdn_problem)); return 0; }}\n')
+                    f'int main(void) {{ {body} printf("%zu\\n", sizeof({cname})); return 0; }}\n')
     exe = tmp_path / "layout"
     cuda_inc = os.path.join(os.environ.get("CUDA_HOME", "/usr/local/cuda"), "include")
     subprocess.run(["gcc", "-I", os.path.join(ROOT, "include"), "-I", cuda_inc, str(prog),
                     "-o", str(exe)], check=True)
     c_vals = [int(x) for x in subprocess.run([str(exe)], capture_output=True, text=True,
                                              check=True).stdout.split()]
-    py_vals = [getattr(binding.gdn_problem, f).offset for f in fields]
-    py_vals.append(ctypes.sizeof(binding.gdn_problem))
+    py_vals = [getattr(cls, f).offset for f in fields]
+    py_vals.append(ctypes.sizeof(cls))
     assert c_vals == py_vals
 
 
@@ -230,3 +232,49 @@ def test_accept_prefix_validation(lib):
     assert call_accept(lib, draft=(1 << 40) + 1) == 7
     assert call_accept(lib, acc=(1 << 40) + 16) == 8           # accepted over the draft ids
     assert call_accept(lib, err=ACC_PTR + 4) == 8              # accepted over the error word
+
+
+
+# ---------------------------------------------------------------- replay buffer
+
+def fake_replay(**over):
+    rb = binding.gdn_replay()
+    base = (1 << 40) + 20 * (1 << 32)
+    step = 1 << 32
+    rb.capacity, rb.reserved = 32, 0
+    rb.k, rb.v, rb.alpha, rb.beta = base, base + step, base + 2 * step, base + 3 * step
+    rb.len_in, rb.len_out = base + 4 * step, base + 5 * step
+    for k, v in over.items():
+        setattr(rb, k, v)
+    return rb
+
+
+def call_replay(lib, fn, c=None, rb=None):
+    c = fake_problem() if c is None else c
+    rbp = None if rb is False else ctypes.byref(fake_replay() if rb is None else rb)
+    if fn == "verify":
+        return lib.gdn_replay_verify(ctypes.byref(c), rbp, O_PTR, None)
+    return lib.gdn_replay_commit(ctypes.byref(c), rbp, ACC_PTR, None)
+
+
+@pytest.mark.parametrize("fn", ["verify", "commit"])
+def test_replay_validation(lib, fn):
+    assert call_replay(lib, fn, rb=False) == 1
+    assert call_replay(lib, fn, rb=fake_replay(reserved=1)) == 2
+    assert call_replay(lib, fn, rb=fake_replay(capacity=0)) == 2
+    assert call_replay(lib, fn, rb=fake_replay(capacity=7)) == 2       # below max_T = 8
+    assert call_replay(lib, fn, rb=fake_replay(len_in=None)) == 1
+    assert call_replay(lib, fn, rb=fake_replay(k=None)) == 1
+    assert call_replay(lib, fn, rb=fake_replay(k=fake_replay().k + 8)) == 7
+    assert call_replay(lib, fn, rb=fake_replay(len_in=fake_replay().len_in + 2)) == 7
+    assert call_replay(lib, fn, c=fake_problem(dk=64, dv=64)) == 4      # chunked kernel only
+    assert call_replay(lib, fn, c=fake_problem(algo=1)) == 4
+    assert call_replay(lib, fn, c=fake_problem(qkv_dtype=0)) == 4
+    assert call_replay(lib, fn, rb=fake_replay(k=fake_problem().pool)) == 8   # buffer over pool
+    assert call_replay(lib, fn, c=fake_problem(batch=0, q=None, pool=None)) == 0
+
+
+def test_replay_commit_output_checks(lib):
+    assert call_replay(lib, "commit", rb=fake_replay(len_out=None)) == 1
+    assert call_replay(lib, "commit", rb=fake_replay(len_out=fake_replay().len_in)) == 8
+    assert call_replay(lib, "commit", rb=fake_replay(len_out=fake_problem().slot_ids)) == 8
