@@ -45,7 +45,7 @@ UNIT = "us/layer-call"
 NOMINAL_HBM_GBS = 8000.0
 MODE_NAME = {"v": "verify", "c": "commit", "f": "fused",
              "C": "commit_layers", "F": "fused_layers",  # upper case: one launch, all layers
-             "a": "accept"}
+             "a": "accept", "rv": "replay_verify", "rc": "replay_commit"}
 
 
 # ----------------------------------------------------------------- accounting
@@ -72,6 +72,28 @@ def alg_bytes(prob, mode: str) -> int:
     else:
         per_r = tile + (acc > 0) * tile + lens * (2 * q_k + v_ + 8 + o_)
     return int(H * per_r.sum() + meta)
+
+
+def replay_bytes(prob, buf, mode: str) -> int:
+    """Minimum bytes of one ReplaySSM call, per unit, with n = the slot's buffered rows:
+    verify = state read + (n + T) buffered rows (k, v, alpha, beta) + T (q, o)
+    commit = for a flushed slot (keep + max_T > C, keep = n + a): state read +
+             state write + keep buffered rows; nothing else moves (pointer move)
+    plus per-request metadata (slot id, buffered length, accepted length, new length)."""
+    esz = 2 if prob.qkv_dtype == "bf16" else 4
+    tile = prob.dk * prob.dv * 4
+    row = prob.dk * esz + prob.dv * esz + 8  # one buffered row: k, v, alpha, beta
+    lens = prob.lengths.astype(np.int64)
+    n = np.array([int(buf["len_in"][int(s)]) for s in prob.slot_ids], dtype=np.int64)
+    if mode == "verify":
+        per_r = tile + (n + lens) * row + lens * (prob.dk * esz + prob.dv * 4)
+        meta = prob.batch * 8
+    else:
+        keep = n + prob.accepted.astype(np.int64)
+        flush = keep + int(prob.max_T) > int(buf["capacity"])
+        per_r = flush * (2 * tile + keep * row)
+        meta = prob.batch * 16
+    return int(prob.heads * per_r.sum() + meta)
 
 
 # ----------------------------------------------------------------- clocks
@@ -255,7 +277,21 @@ def run_ours(args, rank, world, local_rank):
     per_layer = {m: [alg_bytes(pr, MODE_NAME[m]) for pr in layers] for m in ("v", "c", "f")}
     # bytes_of[kind]: algorithmic bytes of each launch of that kind in one step
     bytes_of = dict(per_layer, C=[sum(per_layer["c"])], F=[sum(per_layer["f"])])
-    if batched and fused:
+    replay_bufs = None
+    if args.replay:
+        if fused or batched or args.order != "interleaved":
+            raise SystemExit("--replay times verify then commit per layer")
+        replay_bufs = [inputs.make_replay(pr, args.replay, seed=l, dense=False)
+                       for l, pr in enumerate(layers)]
+        reps = [staging.DeviceReplay(b, pr.qkv_dtype, dev) for b, pr in zip(replay_bufs, layers)]
+        bytes_of["rv"] = [replay_bytes(pr, b, "verify") for pr, b in zip(layers, replay_bufs)]
+        bytes_of["rc"] = [replay_bytes(pr, b, "commit") for pr, b in zip(layers, replay_bufs)]
+        kinds = ["rv", "rc"]
+        calls = []
+        for d, r in zip(dps, reps):
+            calls.append(("rv", staging.replay_launcher(d, r, "verify", stream)))
+            calls.append(("rc", staging.replay_launcher(d, r, "commit", stream)))
+    elif batched and fused:
         kinds = ["F"]
         calls = [("F", staging.layers_launcher(dps, "fused", stream))]
     elif batched:
@@ -347,10 +383,11 @@ def run_ours(args, rank, world, local_rank):
             + "_" + MODE_NAME[dominant])
     traffic = profile_traffic(ktag, name)
 
-    e2e = run_e2e(args, dps, stream, dev, fused) if not (args.no_e2e or batched) else None
+    e2e = (run_e2e(args, dps, stream, dev, fused)
+           if not (args.no_e2e or batched or args.replay) else None)
 
     cpu = None
-    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+    if rank == 0 and world == 1 and not args.no_cpu_baseline and not args.replay:
         threads = os.cpu_count() or 1
         dt, us, n = cpu_oracle_time(p0, args.cpu_units, threads)
         cpu = {"value": us, "unit": UNIT, "cores": threads, "kind": "oracle",
@@ -369,7 +406,10 @@ def run_ours(args, rank, world, local_rank):
                 "description": (f"batch {p0.batch}, heads {p0.heads}, dk {p0.dk}, dv {p0.dv}, "
                                 f"draft {p0.max_T}, {L} layer(s), pool {p0.pool_slots} slots/layer, "
                                 f"q/k/v {p0.qkv_dtype}, gates/state/o fp32"),
-                "order": ("fused, all layers in one launch" if fused and batched else
+                "order": (f"ReplaySSM buffer of {args.replay} rows per slot: replay verify then "
+                          "replay commit per layer; buffered lengths uniform on [0, C - T] "
+                          "(a steady-state sample, not carried between steps)" if args.replay else
+                          "fused, all layers in one launch" if fused and batched else
                           "fused per layer" if fused else
                           "all verifies, then all layers' commits in one launch" if batched else
                           "verify then commit per layer" if args.order == "interleaved" else
@@ -468,6 +508,8 @@ def main():
     ap.add_argument("--ref-units", type=int, default=64)
     ap.add_argument("--e2e-steps", type=int, default=20)
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--replay", type=int, default=0, metavar="C",
+                    help="time the ReplaySSM buffer calls with C buffer rows per slot")
     ap.add_argument("--draft", type=int, default=None,
                     help="replace the draft length of a uniform workload (longer drafts run as "
                          "several 16-token chunks)")

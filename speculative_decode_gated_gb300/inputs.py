@@ -251,22 +251,27 @@ def random_token_ids(lengths: Sequence[int], seed: int, p_differ: float = 0.1, v
 
 
 def make_replay(prob: Problem, capacity: int, seed: int = 0,
-                len_in: Optional[np.ndarray] = None) -> dict:
+                len_in: Optional[np.ndarray] = None, dense: bool = True) -> dict:
     """A ReplaySSM buffer for `prob`: `capacity` rows per pool slot in the token
     layout (k [slots*C][H][dk], v [slots*C][H][dv], alpha/beta [slots*C][H]),
     and len_in[slot], the rows already buffered.  For a named slot len_in is
     uniform on [0, C - T_r] (room for the drafts) unless given; its rows are
     drawn like the workload's tokens, and request r's drafts are copied to
-    rows slot*C + len_in + [0, T_r).  Rows of unnamed slots are zero (alpha 1)."""
+    rows slot*C + len_in + [0, T_r).  Rows of unnamed slots are zero (alpha 1).
+    dense=False returns only the named slots' rows ("slots": their ids in
+    order, k/v/alpha/beta with len(slots) * C rows), for large pools."""
     C = int(capacity)
     if prob.batch and C < prob.max_T:
         raise ValueError("capacity below the draft length")
     rng = np.random.default_rng(np.random.SeedSequence([seed, 90]))
     S, H = prob.pool_slots, prob.heads
-    k = np.zeros((S * C, H, prob.dk), np.float32)
-    v = np.zeros((S * C, H, prob.dv), np.float32)
-    alpha = np.ones((S * C, H), np.float32)
-    beta = np.zeros((S * C, H), np.float32)
+    named = [int(s) for s in prob.slot_ids]
+    where = {s: i for i, s in enumerate(named)}
+    R = S if dense else len(named)
+    k = np.zeros((R * C, H, prob.dk), np.float32)
+    v = np.zeros((R * C, H, prob.dv), np.float32)
+    alpha = np.ones((R * C, H), np.float32)
+    beta = np.zeros((R * C, H), np.float32)
     lens = np.zeros(S, np.int32) if len_in is None else np.array(len_in, np.int32, copy=True)
     for r in range(prob.batch):
         s, T, c0 = int(prob.slot_ids[r]), int(prob.lengths[r]), int(prob.cu_seqlens[r])
@@ -278,6 +283,11 @@ def make_replay(prob: Problem, capacity: int, seed: int = 0,
             raise ValueError("buffered rows plus drafts exceed the capacity")
         ks[n:n + T], vs[n:n + T] = prob.k[c0:c0 + T], prob.v[c0:c0 + T]
         al[n:n + T], be[n:n + T] = prob.alpha[c0:c0 + T], prob.beta[c0:c0 + T]
-        k[s * C:(s + 1) * C], v[s * C:(s + 1) * C] = ks, vs
-        alpha[s * C:(s + 1) * C], beta[s * C:(s + 1) * C] = al, be
-    return dict(capacity=C, k=k, v=v, alpha=alpha, beta=beta, len_in=lens)
+        i = s if dense else where[s]
+        k[i * C:(i + 1) * C], v[i * C:(i + 1) * C] = ks, vs
+        alpha[i * C:(i + 1) * C], beta[i * C:(i + 1) * C] = al, be
+    out = dict(capacity=C, k=k, v=v, alpha=alpha, beta=beta, len_in=lens)
+    if not dense:
+        out["slots"] = np.array(named, np.int64)
+        out["pool_slots"] = S
+    return out

@@ -139,11 +139,22 @@ class DeviceReplay:
 
     def __init__(self, buf: dict, qkv_dtype: str, device="cuda"):
         dev = torch.device(device)
-        self.capacity = int(buf["capacity"])
-        self.k = qkv_tensor(buf["k"], qkv_dtype, dev)
-        self.v = qkv_tensor(buf["v"], qkv_dtype, dev)
-        self.alpha = torch.from_numpy(np.ascontiguousarray(buf["alpha"], np.float32)).to(dev)
-        self.beta = torch.from_numpy(np.ascontiguousarray(buf["beta"], np.float32)).to(dev)
+        self.capacity = C = int(buf["capacity"])
+        k = qkv_tensor(buf["k"], qkv_dtype, dev)
+        v = qkv_tensor(buf["v"], qkv_dtype, dev)
+        alpha = torch.from_numpy(np.ascontiguousarray(buf["alpha"], np.float32)).to(dev)
+        beta = torch.from_numpy(np.ascontiguousarray(buf["beta"], np.float32)).to(dev)
+        if "slots" in buf:  # compact: only the named slots' rows; scatter into the full buffer
+            S = int(buf["pool_slots"])
+            rows = (torch.from_numpy(buf["slots"]).to(dev)[:, None] * C
+                    + torch.arange(C, device=dev)[None, :]).reshape(-1)
+            full = []
+            for x, fill in ((k, 0.0), (v, 0.0), (alpha, 1.0), (beta, 0.0)):
+                f = torch.full((S * C,) + tuple(x.shape[1:]), fill, dtype=x.dtype, device=dev)
+                f[rows] = x
+                full.append(f)
+            k, v, alpha, beta = full
+        self.k, self.v, self.alpha, self.beta = k, v, alpha, beta
         self.len_in = torch.from_numpy(np.ascontiguousarray(buf["len_in"], np.int32)).to(dev)
         self.len_out = self.len_in.clone()
         self.c = binding.make_replay(capacity=self.capacity, k=self.k, v=self.v, alpha=self.alpha,
@@ -174,3 +185,20 @@ class DeviceReplay:
         return dict(capacity=self.capacity, k=self.k.float().cpu().numpy(),
                     v=self.v.float().cpu().numpy(), alpha=self.alpha.cpu().numpy(),
                     beta=self.beta.cpu().numpy(), len_in=self.len_in.cpu().numpy())
+
+
+def replay_launcher(d: DeviceProblem, r: DeviceReplay, mode: str, stream):
+    """A zero-argument callable issuing one ReplaySSM call on `stream`, every
+    argument marshalled in advance."""
+    lib = binding.lib()
+    s = binding._stream(stream)
+    o, acc = d.o.data_ptr(), d.accepted.data_ptr()
+    pref, rref = d.c.ref, r.c.ref
+    fn = {"verify": lambda: lib.gdn_replay_verify(pref, rref, o, s),
+          "commit": lambda: lib.gdn_replay_commit(pref, rref, acc, s)}[mode]
+
+    def call():
+        st = fn()
+        if st != binding.GDN_OK:
+            raise binding.GdnError(st, f"gdn replay {mode}")
+    return call
