@@ -23,8 +23,9 @@
  *               (qkv_dtype); token rows of request r are [cu[r], cu[r+1]) with
  *               cu = cu_seqlens, or [r*max_T, (r+1)*max_T) when cu_seqlens is NULL.
  *   alpha, beta float32 [N_tok][heads] (alpha is the decay gate, beta the write
- *               strength; both given directly, no log-space or activation applied).
- *   o           float32 [N_tok][heads][dv].
+ *               strength; both given directly, no activation applied; with
+ *               GDN_FLAG_LOG_GATE alpha holds g and the decay is expf(g)).
+ *   o           float32 [N_tok][heads][dv] (bfloat16 with GDN_FLAG_O_BF16).
  *   accepted    int32 [batch], a_r in [0, T_r].
  *
  * Calls.  All compute calls are asynchronous on `stream`; they validate their
@@ -66,7 +67,7 @@ extern "C" {
 typedef enum gdn_status {
     GDN_OK = 0,
     GDN_ERR_NULL_PTR = 1,     /* a required pointer is NULL */
-    GDN_ERR_BAD_DIM = 2,      /* batch/heads/max_T/pool_slots/n_tok out of range */
+    GDN_ERR_BAD_DIM = 2,      /* batch/heads/max_T/pool_slots/n_tok out of range, or unknown flags */
     GDN_ERR_BAD_DTYPE = 3,    /* qkv_dtype is not a gdn_dtype */
     GDN_ERR_UNSUPPORTED = 4,  /* dk/dv (or a forced algo) not supported */
     GDN_ERR_DEVICE_ARG = 5,   /* reported by gdn_read_device_error only */
@@ -98,23 +99,29 @@ typedef enum gdn_algo {
 #define GDN_DEVERR_TIMEOUT  8   /* an internal pipeline wait gave up (about 2 s); results incomplete */
 #define GDN_DEVERR_REPLAY  16   /* replay buffer: len_in[slot] < 0, or buffered plus new rows > capacity */
 
+/* Variant bits of gdn_problem.flags (the same in every problem of a layer batch). */
+#define GDN_FLAG_O_BF16    1    /* o is bfloat16 [N_tok][heads][dv], round to nearest even of the
+                                   float32 result; otherwise o is float32 */
+#define GDN_FLAG_LOG_GATE  2    /* alpha holds the log-space gate g; the kernels use alpha =
+                                   expf(g) (CUDA's expf) */
+
 /* Limits checked on the host. */
 #define GDN_MAX_T 1024          /* draft tokens per request */
 
 typedef struct gdn_problem {
     int32_t batch;               /* B >= 0 requests (B = 0: calls return GDN_OK, no launch) */
     int32_t heads;               /* H >= 1 */
-    int32_t dk;                  /* key dim: 32, 64 or 128 */
+    int32_t dk;                  /* key dim: 32, 64, 128 or 256 */
     int32_t dv;                  /* value dim: a multiple of 32, <= 128 or 256 */
     int32_t max_T;               /* uniform draft length (cu_seqlens NULL) or the ragged maximum, 0..GDN_MAX_T */
     int32_t qkv_dtype;           /* gdn_dtype of q, k, v */
     int32_t algo;                /* gdn_algo */
-    int32_t reserved;            /* must be 0 */
+    int32_t flags;               /* GDN_FLAG_* bits; all other bits must be 0 */
     const int32_t *cu_seqlens;   /* device [batch+1] token-row offsets, or NULL (uniform) */
     const void *q;               /* device [N_tok][heads][dk], 16-byte aligned */
     const void *k;               /* device [N_tok][heads][dk], 16-byte aligned */
     const void *v;               /* device [N_tok][heads][dv], 16-byte aligned */
-    const float *alpha;          /* device [N_tok][heads] */
+    const float *alpha;          /* device [N_tok][heads]: alpha, or g = log(alpha) with GDN_FLAG_LOG_GATE */
     const float *beta;           /* device [N_tok][heads] */
     float *pool;                 /* device [pool_slots][heads][dk][dv], 16-byte aligned */
     int64_t pool_slots;          /* >= batch */
@@ -126,9 +133,10 @@ typedef struct gdn_problem {
                                     [cu[r], cu[r+1]) do not lie in [0, n_tok) */
 } gdn_problem;
 
-/* o_t for every draft token of every unit.  o: device float32 [N_tok][heads][dv],
+/* o_t for every draft token of every unit.  o: device float32 (or, with
+ * GDN_FLAG_O_BF16, bfloat16) [N_tok][heads][dv],
  * 16-byte aligned, must not overlap any input.  Reads the pool, never writes it. */
-GDN_API gdn_status gdn_verify(const gdn_problem *p, float *o, cudaStream_t stream);
+GDN_API gdn_status gdn_verify(const gdn_problem *p, void *o, cudaStream_t stream);
 
 /* For every request r with accepted[r] > 0: pool[slot_ids[r]][h] <- state after
  * accepted[r] tokens, replayed from the checkpoint in that same slot (in place).
@@ -138,7 +146,7 @@ GDN_API gdn_status gdn_commit(const gdn_problem *p, const int32_t *accepted, cud
 /* gdn_verify and then gdn_commit with the same inputs, in one pass: each
  * checkpoint is read once, o is written for every token, the state once. */
 GDN_API gdn_status gdn_verify_commit_fused(const gdn_problem *p, const int32_t *accepted,
-                                           float *o, cudaStream_t stream);
+                                           void *o, cudaStream_t stream);
 
 /* Layer batches: the same calls for the n_layers problems of one step (one per
  * model layer), in as few launches as possible (the chunked kernel takes up to
@@ -156,11 +164,11 @@ GDN_API gdn_status gdn_verify_commit_fused(const gdn_problem *p, const int32_t *
  * arrays (GDN_ERR_ALIAS).  The results equal those of the single-problem call
  * made once per layer.  n_layers = 0 launches nothing. */
 GDN_API gdn_status gdn_verify_layers(const gdn_problem *problems, int32_t n_layers,
-                                     float *const *o, cudaStream_t stream);
+                                     void *const *o, cudaStream_t stream);
 GDN_API gdn_status gdn_commit_layers(const gdn_problem *problems, int32_t n_layers,
                                      const int32_t *accepted, cudaStream_t stream);
 GDN_API gdn_status gdn_verify_commit_fused_layers(const gdn_problem *problems, int32_t n_layers,
-                                                  const int32_t *accepted, float *const *o,
+                                                  const int32_t *accepted, void *const *o,
                                                   cudaStream_t stream);
 
 /* Greedy accepted lengths on the device, so that the commit needs no host round
@@ -226,7 +234,7 @@ typedef struct gdn_replay {
                                     overlap len_in or any other array */
 } gdn_replay;
 
-GDN_API gdn_status gdn_replay_verify(const gdn_problem *p, const gdn_replay *rb, float *o,
+GDN_API gdn_status gdn_replay_verify(const gdn_problem *p, const gdn_replay *rb, void *o,
                                      cudaStream_t stream);
 GDN_API gdn_status gdn_replay_commit(const gdn_problem *p, const gdn_replay *rb,
                                      const int32_t *accepted, cudaStream_t stream);

@@ -106,6 +106,9 @@ def run_units(prob, unit_ids: Optional[Sequence[int]] = None, *, s0: Optional[np
     cu = np.ascontiguousarray(prob.cu_seqlens, dtype=np.int64)
     q, k, v = _f64(prob.q), _f64(prob.k), _f64(prob.v)
     al, be = _f64(prob.alpha), _f64(prob.beta)
+    if getattr(prob, "gate", "alpha") == "log":
+        # The log-space gate variant: the input is g and the decay is alpha = exp(g).
+        al = np.exp(al)
     o = np.zeros((n, T, dv)) if want_o else None
     s_acc = np.zeros((n, dk, dv)) if want_state else None
 

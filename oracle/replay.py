@@ -36,6 +36,7 @@ class _Seq:
 
     def __init__(self, prob, ks, vs, als, bes, qs, accepted, s0):
         self.heads, self.dk, self.dv = prob.heads, prob.dk, prob.dv
+        self.gate = getattr(prob, "gate", "alpha")
         self.batch = len(ks)
         lens = np.array([len(x) for x in ks], dtype=np.int64)
         self.cu_seqlens = np.concatenate([[0], np.cumsum(lens)]).astype(np.int64)

@@ -20,6 +20,7 @@ GDN_OK = 0
 GDN_ERR_DEVICE_ARG = 5
 GDN_ERR_ALIAS, GDN_ERR_LAYER_MISMATCH = 8, 9
 GDN_FP32, GDN_BF16 = 0, 1
+GDN_FLAG_O_BF16, GDN_FLAG_LOG_GATE = 1, 2
 GDN_ALGO_AUTO, GDN_ALGO_RECURRENT, GDN_ALGO_CHUNK = 0, 1, 2
 GDN_DEVERR_SLOT, GDN_DEVERR_ACCEPTED, GDN_DEVERR_SEQLEN = 1, 2, 4
 GDN_DEVERR_TIMEOUT, GDN_DEVERR_REPLAY = 8, 16
@@ -49,7 +50,7 @@ class gdn_problem(ctypes.Structure):
     _fields_ = [
         ("batch", ctypes.c_int32), ("heads", ctypes.c_int32), ("dk", ctypes.c_int32),
         ("dv", ctypes.c_int32), ("max_T", ctypes.c_int32), ("qkv_dtype", ctypes.c_int32),
-        ("algo", ctypes.c_int32), ("reserved", ctypes.c_int32),
+        ("algo", ctypes.c_int32), ("flags", ctypes.c_int32),
         ("cu_seqlens", ctypes.c_void_p), ("q", ctypes.c_void_p), ("k", ctypes.c_void_p),
         ("v", ctypes.c_void_p), ("alpha", ctypes.c_void_p), ("beta", ctypes.c_void_p),
         ("pool", ctypes.c_void_p), ("pool_slots", ctypes.c_int64),
@@ -135,12 +136,14 @@ def _check(t: Optional[torch.Tensor], name: str, dtypes, device) -> None:
 def make_problem(*, q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, alpha: torch.Tensor,
                  beta: torch.Tensor, pool: torch.Tensor, slot_ids: torch.Tensor,
                  max_T: int, cu_seqlens: Optional[torch.Tensor] = None,
-                 dev_err: Optional[torch.Tensor] = None, algo: int = GDN_ALGO_AUTO) -> Problem:
+                 dev_err: Optional[torch.Tensor] = None, algo: int = GDN_ALGO_AUTO,
+                 flags: int = 0) -> Problem:
     """Builds the C problem from device tensors (shapes as in include/gdn.h).
 
     q, k: [N_tok, H, dk]; v: [N_tok, H, dv] (bf16 or fp32, same dtype);
     alpha, beta: [N_tok, H] fp32; pool: [slots, H, dk, dv] fp32; slot_ids: [B] int32;
     cu_seqlens: [B+1] int32 or None (uniform length max_T); dev_err: [1] int32 or None.
+    flags: GDN_FLAG_* bits (bf16 o, log-space alpha).
     """
     dev = pool.device
     if q.dtype not in (torch.bfloat16, torch.float32) or k.dtype != q.dtype or v.dtype != q.dtype:
@@ -162,7 +165,7 @@ def make_problem(*, q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, alpha: to
     c.max_T = int(max_T)
     c.qkv_dtype = GDN_BF16 if q.dtype == torch.bfloat16 else GDN_FP32
     c.algo = int(algo)
-    c.reserved = 0
+    c.flags = int(flags)
     c.cu_seqlens = _ptr(cu_seqlens)
     c.q, c.k, c.v = _ptr(q), _ptr(k), _ptr(v)
     c.alpha, c.beta = _ptr(alpha), _ptr(beta)
@@ -185,8 +188,12 @@ def _raise(status: int, where: str) -> None:
         raise GdnError(status, where)
 
 
+def _o_dtype(prob: Problem):
+    return torch.bfloat16 if prob.c.flags & GDN_FLAG_O_BF16 else torch.float32
+
+
 def gdn_verify(prob: Problem, o: torch.Tensor, stream=None) -> None:
-    _check(o, "o", (torch.float32,), None)
+    _check(o, "o", (_o_dtype(prob),), None)
     _raise(lib().gdn_verify(prob.ref, _ptr(o), _stream(stream)), "gdn_verify")
 
 
@@ -198,7 +205,7 @@ def gdn_commit(prob: Problem, accepted: torch.Tensor, stream=None) -> None:
 def gdn_verify_commit_fused(prob: Problem, accepted: torch.Tensor, o: torch.Tensor,
                             stream=None) -> None:
     _check(accepted, "accepted", (torch.int32,), None)
-    _check(o, "o", (torch.float32,), None)
+    _check(o, "o", (_o_dtype(prob),), None)
     _raise(lib().gdn_verify_commit_fused(prob.ref, _ptr(accepted), _ptr(o), _stream(stream)),
            "gdn_verify_commit_fused")
 
@@ -222,7 +229,7 @@ class ProblemArray:
 def _ptr_array(tensors) -> ctypes.Array:
     arr = (ctypes.c_void_p * max(len(tensors), 1))()
     for i, t in enumerate(tensors):
-        _check(t, f"o[{i}]", (torch.float32,), None)
+        _check(t, f"o[{i}]", (torch.float32, torch.bfloat16), None)
         arr[i] = _ptr(t)
     return arr
 
@@ -300,7 +307,7 @@ def make_replay(*, capacity: int, k: torch.Tensor, v: torch.Tensor, alpha: torch
 
 
 def gdn_replay_verify(prob: Problem, rb: Replay, o: torch.Tensor, stream=None) -> None:
-    _check(o, "o", (torch.float32,), None)
+    _check(o, "o", (_o_dtype(prob),), None)
     _raise(lib().gdn_replay_verify(prob.ref, rb.ref, _ptr(o), _stream(stream)), "gdn_replay_verify")
 
 

@@ -60,12 +60,15 @@ LayerRanges layer_ranges(const gdn_problem *p, int64_t kv_rows = -1) {
     return r;
 }
 
-Range o_range(const gdn_problem *p, const float *o) {
-    return range(o, token_rows(p) * p->heads * p->dv * 4);
+Range o_range(const gdn_problem *p, const void *o) {
+    const int64_t esz = (p->flags & GDN_FLAG_O_BF16) ? 2 : 4;
+    return range(o, token_rows(p) * p->heads * p->dv * esz);
 }
 
+constexpr int32_t kKnownFlags = GDN_FLAG_O_BF16 | GDN_FLAG_LOG_GATE;
+
 bool dims_supported(int dk, int dv) {
-    const bool dk_ok = dk == 32 || dk == 64 || dk == 128;
+    const bool dk_ok = dk == 32 || dk == 64 || dk == 128 || dk == 256;
     const bool dv_ok = dv >= 32 && dv <= 256 && dv % 32 == 0 && (dv <= 128 || dv % 128 == 0);
     return dk_ok && dv_ok;
 }
@@ -88,10 +91,10 @@ int resolve_algo(const gdn_problem *p) {
 
 // Host validation shared by all entry points.  On success *algo is the kernel
 // to run and *empty tells whether there is nothing to launch.
-gdn_status validate(const gdn_problem *p, bool with_o, const float *o, bool with_acc,
+gdn_status validate(const gdn_problem *p, bool with_o, const void *o, bool with_acc,
                     const int32_t *accepted, int *algo, bool *empty, int64_t kv_rows = -1) {
     if (!p) return GDN_ERR_NULL_PTR;
-    if (p->reserved != 0 || !shape_ok(p)) return GDN_ERR_BAD_DIM;
+    if ((p->flags & ~kKnownFlags) != 0 || !shape_ok(p)) return GDN_ERR_BAD_DIM;
     if (p->qkv_dtype != GDN_FP32 && p->qkv_dtype != GDN_BF16) return GDN_ERR_BAD_DTYPE;
     if (!dims_supported(p->dk, p->dv)) return GDN_ERR_UNSUPPORTED;
     if (p->algo < GDN_ALGO_AUTO || p->algo > GDN_ALGO_CHUNK) return GDN_ERR_UNSUPPORTED;
@@ -130,7 +133,7 @@ gdn_status validate(const gdn_problem *p, bool with_o, const float *o, bool with
     return GDN_OK;
 }
 
-gdn::Args make_args(const gdn_problem *p, const int32_t *accepted, float *o) {
+gdn::Args make_args(const gdn_problem *p, const int32_t *accepted, void *o) {
     gdn::Args a;
     a.B = p->batch;
     a.H = p->heads;
@@ -151,10 +154,11 @@ gdn::Args make_args(const gdn_problem *p, const int32_t *accepted, float *o) {
     a.o = o;
     a.dev_err = p->dev_err;
     a.kv_rows = a.n_tok;
+    a.flags = p->flags;
     return a;
 }
 
-gdn_status run(const gdn_problem *p, int mode, const int32_t *accepted, float *o,
+gdn_status run(const gdn_problem *p, int mode, const int32_t *accepted, void *o,
                cudaStream_t stream) {
     int algo = 0;
     bool empty = false;
@@ -177,6 +181,7 @@ gdn_status run(const gdn_problem *p, int mode, const int32_t *accepted, float *o
 bool same_requests(const gdn_problem *a, const gdn_problem *b) {
     return a->batch == b->batch && a->heads == b->heads && a->dk == b->dk && a->dv == b->dv &&
            a->max_T == b->max_T && a->qkv_dtype == b->qkv_dtype && a->algo == b->algo &&
+           a->flags == b->flags &&
            a->cu_seqlens == b->cu_seqlens && a->slot_ids == b->slot_ids &&
            a->pool_slots == b->pool_slots && (!a->cu_seqlens || a->n_tok == b->n_tok);
 }
@@ -187,7 +192,7 @@ bool same_requests(const gdn_problem *a, const gdn_problem *b) {
 // layers go into each launch of the chunked kernel; the recurrent kernel runs
 // once per layer.
 gdn_status run_layers(const gdn_problem *ps, int32_t n, int mode, const int32_t *accepted,
-                      float *const *o, cudaStream_t stream) {
+                      void *const *o, cudaStream_t stream) {
     if (n < 0) return GDN_ERR_BAD_DIM;
     if (n == 0) return GDN_OK;
     if (!ps) return GDN_ERR_NULL_PTR;
@@ -240,7 +245,7 @@ gdn_status run_layers(const gdn_problem *ps, int32_t n, int mode, const int32_t 
 }
 
 gdn_status run_replay(const gdn_problem *p, const gdn_replay *rb, int mode,
-                      const int32_t *accepted, float *o, cudaStream_t stream) {
+                      const int32_t *accepted, void *o, cudaStream_t stream) {
     if (!p || !rb) return GDN_ERR_NULL_PTR;
     if (rb->reserved != 0 || rb->capacity < 1) return GDN_ERR_BAD_DIM;
     // The problem as the kernel sees it: k, v and the gates come from the buffer.
@@ -290,7 +295,7 @@ gdn_status run_replay(const gdn_problem *p, const gdn_replay *rb, int mode,
 
 extern "C" {
 
-gdn_status gdn_verify(const gdn_problem *p, float *o, cudaStream_t stream) {
+gdn_status gdn_verify(const gdn_problem *p, void *o, cudaStream_t stream) {
     return run(p, gdn::kVerify, nullptr, o, stream);
 }
 
@@ -298,12 +303,12 @@ gdn_status gdn_commit(const gdn_problem *p, const int32_t *accepted, cudaStream_
     return run(p, gdn::kCommit, accepted, nullptr, stream);
 }
 
-gdn_status gdn_verify_commit_fused(const gdn_problem *p, const int32_t *accepted, float *o,
+gdn_status gdn_verify_commit_fused(const gdn_problem *p, const int32_t *accepted, void *o,
                                    cudaStream_t stream) {
     return run(p, gdn::kFused, accepted, o, stream);
 }
 
-gdn_status gdn_verify_layers(const gdn_problem *problems, int32_t n_layers, float *const *o,
+gdn_status gdn_verify_layers(const gdn_problem *problems, int32_t n_layers, void *const *o,
                              cudaStream_t stream) {
     return run_layers(problems, n_layers, gdn::kVerify, nullptr, o, stream);
 }
@@ -314,12 +319,12 @@ gdn_status gdn_commit_layers(const gdn_problem *problems, int32_t n_layers,
 }
 
 gdn_status gdn_verify_commit_fused_layers(const gdn_problem *problems, int32_t n_layers,
-                                          const int32_t *accepted, float *const *o,
+                                          const int32_t *accepted, void *const *o,
                                           cudaStream_t stream) {
     return run_layers(problems, n_layers, gdn::kFused, accepted, o, stream);
 }
 
-gdn_status gdn_replay_verify(const gdn_problem *p, const gdn_replay *rb, float *o,
+gdn_status gdn_replay_verify(const gdn_problem *p, const gdn_replay *rb, void *o,
                              cudaStream_t stream) {
     return run_replay(p, rb, gdn::kVerify, nullptr, o, stream);
 }

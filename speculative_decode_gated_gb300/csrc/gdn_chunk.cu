@@ -485,8 +485,10 @@ __device__ __forceinline__ void state_update(float (&hr)[8][4][CPT], const float
 
 // MULTI: units may have more than 16 tokens (several chunks, the state carried
 // in registers from one to the next); otherwise every unit is one chunk and
-// the verify kernel keeps no state in registers.
-template <int MODE, bool RAGGED, int NL, bool MULTI, bool REPLAY>
+// the verify kernel keeps no state in registers.  VAR: the call's flags (bf16
+// o, log-space gates) are read at run time; otherwise they are 0 at compile
+// time, so the default calls carry no code for the variants.
+template <int MODE, bool RAGGED, int NL, bool MULTI, bool REPLAY, bool VAR>
 __global__ void __launch_bounds__(kThreads, kBlocksPerSM)
     chunk_kernel(const __grid_constant__ Launch<NL> L) {
     extern __shared__ unsigned char smem_raw[];
@@ -497,6 +499,7 @@ __global__ void __launch_bounds__(kThreads, kBlocksPerSM)
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int g = lane >> 2, c = lane & 3;
     const Args &p = L.a[0];  // the request-level fields every layer shares
+    const int flags = VAR ? p.flags : 0;
     const int U = p.B * p.H;  // units per layer
     const int W = NL == 1 ? U : U * L.n;  // units of the launch
     const int G = gridDim.x;
@@ -620,7 +623,9 @@ __global__ void __launch_bounds__(kThreads, kBlocksPerSM)
                 ++tok_issued;
             }
             if (tid < CT) {
-                ax.alpha[tid] = tid < T ? ga : 1.0f;
+                // A log-space gate becomes alpha = expf(g) here, once per token.
+                const float at = (flags & GDN_FLAG_LOG_GATE) ? expf(ga) : ga;
+                ax.alpha[tid] = tid < T ? at : 1.0f;
                 ax.beta[tid] = tid < T ? gb : 0.0f;
             }
             // Gates of the next step, loaded straight into the registers just
@@ -860,7 +865,9 @@ __global__ void __launch_bounds__(kThreads, kBlocksPerSM)
                 // Row t of this chunk is output row qrow0 + 16 ch + t; rows before
                 // nskip (replay: buffered rows) have none.
                 const long long orow = (long long)me.qrow0 + CT * ch;
-                float *go = L.a[me.layer].o + me.h * D + col0;
+                const bool o_bf16 = flags & GDN_FLAG_O_BF16;
+                float *go = static_cast<float *>(L.a[me.layer].o) + me.h * D + col0;
+                __nv_bfloat16 *gob = static_cast<__nv_bfloat16 *>(L.a[me.layer].o) + me.h * D + col0;
 #pragma unroll
                 for (int m = 0; m < MT; ++m) {
                     uint32_t ah[4], al[4];
@@ -877,12 +884,22 @@ __global__ void __launch_bounds__(kThreads, kBlocksPerSM)
                         mma(d[0], d[1], d[2], d[3], ah[0], ah[1], ah[2], ah[3], bh[nt][0], bh[nt][1]);
                         mma(d[0], d[1], d[2], d[3], ah[0], ah[1], ah[2], ah[3], bl[nt][0], bl[nt][1]);
                         mma(d[0], d[1], d[2], d[3], al[0], al[1], al[2], al[3], bh[nt][0], bh[nt][1]);
-                        if (t0 < T && CT * ch + t0 >= me.nskip)
-                            *reinterpret_cast<float2 *>(go + (orow + t0) * row_stride + 2 * m) =
-                                make_float2(d[0], d[2]);
-                        if (t0 + 1 < T && CT * ch + t0 + 1 >= me.nskip)
-                            *reinterpret_cast<float2 *>(go + (orow + t0 + 1) * row_stride + 2 * m) =
-                                make_float2(d[1], d[3]);
+                        if (t0 < T && CT * ch + t0 >= me.nskip) {
+                            const size_t i = (orow + t0) * row_stride + 2 * m;
+                            if (o_bf16)
+                                *reinterpret_cast<__nv_bfloat162 *>(gob + i) =
+                                    __floats2bfloat162_rn(d[0], d[2]);
+                            else
+                                *reinterpret_cast<float2 *>(go + i) = make_float2(d[0], d[2]);
+                        }
+                        if (t0 + 1 < T && CT * ch + t0 + 1 >= me.nskip) {
+                            const size_t i = (orow + t0 + 1) * row_stride + 2 * m;
+                            if (o_bf16)
+                                *reinterpret_cast<__nv_bfloat162 *>(gob + i) =
+                                    __floats2bfloat162_rn(d[1], d[3]);
+                            else
+                                *reinterpret_cast<float2 *>(go + i) = make_float2(d[1], d[3]);
+                        }
                     }
                 }
             }
@@ -951,7 +968,7 @@ constexpr int kMaxDevices = 64;
 
 struct DeviceInfo {
     int sms = 0;
-    bool smem_set[3][2][2][2][2] = {};  // [mode][ragged][batched][multi][replay]
+    bool smem_set[3][2][2][2][2][2] = {};  // [mode][ragged][batched][multi][replay][var]
 };
 
 DeviceInfo g_dev[kMaxDevices];
@@ -959,7 +976,7 @@ std::mutex g_dev_mutex;
 
 static_assert(sizeof(Launch<kChunkMaxLayers>) <= 32764, "kernel parameter space");
 
-template <int MODE, bool RAGGED, int NL, bool MULTI, bool REPLAY = false>
+template <int MODE, bool RAGGED, int NL, bool MULTI, bool REPLAY = false, bool VAR = false>
 cudaError_t launch_mode(const Launch<NL> &L, cudaStream_t stream) {
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
@@ -973,11 +990,11 @@ cudaError_t launch_mode(const Launch<NL> &L, cudaStream_t stream) {
             e = cudaDeviceGetAttribute(&info.sms, cudaDevAttrMultiProcessorCount, dev);
             if (e != cudaSuccess) return e;
         }
-        if (!info.smem_set[MODE][RAGGED][NL != 1][MULTI][REPLAY]) {
-            e = cudaFuncSetAttribute(chunk_kernel<MODE, RAGGED, NL, MULTI, REPLAY>,
+        if (!info.smem_set[MODE][RAGGED][NL != 1][MULTI][REPLAY][VAR]) {
+            e = cudaFuncSetAttribute(chunk_kernel<MODE, RAGGED, NL, MULTI, REPLAY, VAR>,
                                      cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
             if (e != cudaSuccess) return e;
-            info.smem_set[MODE][RAGGED][NL != 1][MULTI][REPLAY] = true;
+            info.smem_set[MODE][RAGGED][NL != 1][MULTI][REPLAY][VAR] = true;
         }
         sms = info.sms;
     }
@@ -994,7 +1011,7 @@ cudaError_t launch_mode(const Launch<NL> &L, cudaStream_t stream) {
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, chunk_kernel<MODE, RAGGED, NL, MULTI, REPLAY>, L);
+    return cudaLaunchKernelEx(&cfg, chunk_kernel<MODE, RAGGED, NL, MULTI, REPLAY, VAR>, L);
 }
 
 // The pool and token tensor maps of one layer.
@@ -1046,15 +1063,29 @@ cudaError_t launch_layers(const Args *layers, int n, int mode, cudaStream_t stre
         if (e != cudaSuccess) return e;
     }
     const bool ragged = layers[0].cu_seqlens != nullptr;
-    if (layers[0].cap > 0) {  // replay buffer (single problems): verify or commit
-        if constexpr (NL == 1) {
+    if constexpr (NL == 1) {
+        if (layers[0].cap > 0) {  // replay buffer (single problems): verify or commit
             if (mode == kVerify)
-                return ragged ? launch_mode<kVerify, true, NL, true, true>(L, stream)
-                              : launch_mode<kVerify, false, NL, true, true>(L, stream);
-            return ragged ? launch_mode<kCommit, true, NL, true, true>(L, stream)
-                          : launch_mode<kCommit, false, NL, true, true>(L, stream);
+                return ragged ? launch_mode<kVerify, true, NL, true, true, true>(L, stream)
+                              : launch_mode<kVerify, false, NL, true, true, true>(L, stream);
+            return ragged ? launch_mode<kCommit, true, NL, true, true, true>(L, stream)
+                          : launch_mode<kCommit, false, NL, true, true, true>(L, stream);
         }
-        return cudaErrorNotSupported;
+        if (layers[0].flags != 0) {  // variants: one multi-chunk instantiation for any length
+            switch (mode) {
+                case kVerify:
+                    return ragged ? launch_mode<kVerify, true, NL, true, false, true>(L, stream)
+                                  : launch_mode<kVerify, false, NL, true, false, true>(L, stream);
+                case kCommit:
+                    return ragged ? launch_mode<kCommit, true, NL, true, false, true>(L, stream)
+                                  : launch_mode<kCommit, false, NL, true, false, true>(L, stream);
+                default:
+                    return ragged ? launch_mode<kFused, true, NL, true, false, true>(L, stream)
+                                  : launch_mode<kFused, false, NL, true, false, true>(L, stream);
+            }
+        }
+    } else {
+        if (layers[0].cap > 0 || layers[0].flags != 0) return cudaErrorNotSupported;
     }
     if (layers[0].max_T > CT) return dispatch<NL, true>(L, mode, ragged, stream);
     return dispatch<NL, false>(L, mode, ragged, stream);
@@ -1069,6 +1100,14 @@ bool chunk_supported(bool bf16, int dk, int dv, int max_T) {
 bool chunk_preferred(int max_T) { return max_T >= 1; }
 
 cudaError_t launch_chunk(const Args *layers, int n, int mode, cudaStream_t stream) {
+    if (n > 0 && (layers[0].flags != 0 || layers[0].cap > 0)) {
+        // Variants and replay buffers run one problem per launch.
+        for (int l = 0; l < n; ++l) {
+            const cudaError_t e = launch_layers<1>(layers + l, 1, mode, stream);
+            if (e != cudaSuccess) return e;
+        }
+        return cudaSuccess;
+    }
     for (int l0 = 0; l0 < n; l0 += kChunkMaxLayers) {
         const int m = n - l0 < kChunkMaxLayers ? n - l0 : kChunkMaxLayers;
         const cudaError_t e = m == 1 ? launch_layers<1>(layers + l0, 1, mode, stream)

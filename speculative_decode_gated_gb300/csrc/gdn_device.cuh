@@ -25,8 +25,9 @@ struct Args {
     long long pool_slots;
     const int32_t *slot_ids;
     const int32_t *accepted;  // NULL for verify
-    float *o;                 // NULL for commit
+    void *o;                  // NULL for commit; float, or bf16 with GDN_FLAG_O_BF16
     int32_t *dev_err;
+    int flags = 0;            // GDN_FLAG_* bits
     // ReplaySSM buffer (replay calls only; k, v, alpha, beta then point into
     // the buffer, whose rows are slot * cap + row).
     int cap = 0;              // rows per slot, 0 when there is no buffer

@@ -7,7 +7,7 @@
 
 namespace gdn {
 
-// Recurrent kernel: dk in {32, 64, 128}; dv a multiple of 32, <= 128 or a
+// Recurrent kernel: dk in {32, 64, 128, 256}; dv a multiple of 32, <= 128 or a
 // multiple of 128 up to 256; q/k/v bf16 or fp32; any max_T.
 cudaError_t launch_recurrent(const Args &p, int mode, bool bf16, cudaStream_t stream);
 

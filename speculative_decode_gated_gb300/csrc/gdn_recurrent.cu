@@ -27,7 +27,7 @@ constexpr int kThreads = 128;  // threads per block at most
 
 template <int DK>
 struct RecShape {
-    static constexpr int RS = DK >= 128 ? 2 : 1;  // threads per column
+    static constexpr int RS = DK >= 256 ? 4 : (DK >= 128 ? 2 : 1);  // threads per column
     static constexpr int R = DK / RS;             // rows per thread
     static constexpr int CPW = 32 / RS;           // columns per warp
 };
@@ -104,7 +104,8 @@ __global__ void __launch_bounds__(kThreads) rec_kernel(const Args p) {
         }
         if (tid < n) {
             const size_t x = (size_t)(u.row0 + t0 + tid) * p.H + h;
-            sa[tid] = p.alpha[x];
+            const float a = p.alpha[x];
+            sa[tid] = (p.flags & GDN_FLAG_LOG_GATE) ? expf(a) : a;  // log-space gate: expf(g)
             sb[tid] = p.beta[x];
         }
         __syncthreads();
@@ -167,7 +168,12 @@ __global__ void __launch_bounds__(kThreads) rec_kernel(const Args p) {
             }
             s = s_new;
             if (MODE != kCommit && part == 0) {
-                p.o[((size_t)(u.row0 + t) * p.H + h) * p.dv + j] = fmaf(a_t, p_j, w_j * skq[tt]);
+                const size_t oi = ((size_t)(u.row0 + t) * p.H + h) * p.dv + j;
+                const float ov = fmaf(a_t, p_j, w_j * skq[tt]);
+                if (p.flags & GDN_FLAG_O_BF16)
+                    static_cast<__nv_bfloat16 *>(p.o)[oi] = __float2bfloat16_rn(ov);
+                else
+                    static_cast<float *>(p.o)[oi] = ov;
             }
             if (MODE == kFused && t + 1 == u.a) {
                 float *dst = opaque(col);
@@ -203,13 +209,14 @@ cudaError_t launch_bf(const Args &p, int mode, cudaStream_t stream) {
     switch (p.dk) {
         case 32: return launch_dk<32, BF16>(p, mode, stream);
         case 64: return launch_dk<64, BF16>(p, mode, stream);
-        default: return launch_dk<128, BF16>(p, mode, stream);
+        case 128: return launch_dk<128, BF16>(p, mode, stream);
+        default: return launch_dk<256, BF16>(p, mode, stream);
     }
 }
 
 }  // namespace
 
-// Host launcher.  The caller has validated: dk in {32, 64, 128}, dv a multiple
+// Host launcher.  The caller has validated: dk in {32, 64, 128, 256}, dv a multiple
 // of 32 (and of 128 when above 128), B * H >= 1.
 cudaError_t launch_recurrent(const Args &p, int mode, bool bf16, cudaStream_t stream) {
     return bf16 ? launch_bf<true>(p, mode, stream) : launch_bf<false>(p, mode, stream);

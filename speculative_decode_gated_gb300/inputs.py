@@ -10,7 +10,9 @@ Value recipe (every workload):
             rounded to bfloat16 (round to nearest even) unless the workload keeps
             float32.  The rounded values are the inputs; nothing renormalises them.
   * v     ~ N(0, 1), rounded the same way.
-  * alpha = exp(-softplus(x)) = 1 / (1 + exp(x)),  x ~ N(0, 1), float32.
+  * alpha = exp(-softplus(x)) = 1 / (1 + exp(x)),  x ~ N(0, 1), float32; with
+            gate="log" the same draw is given in log space, g = -softplus(x),
+            float32 (the kernel and the oracle then take alpha = exp(g)).
   * beta  = sigmoid(y) = 1 / (1 + exp(-y)),        y ~ N(0, 1), float32.
   * S0    = 0.1 * N(0, 1) per element, float32 (the standard deviation is 0.1).
   * slot ids: the first B entries of a random permutation of the pool slots
@@ -85,6 +87,7 @@ class Problem:
     slot_ids: np.ndarray  # int32 [B]
     accepted: np.ndarray  # int32 [B]
     s0: np.ndarray  # float32 [B][H][dk][dv], the state held in slot slot_ids[r]
+    gate: str = "alpha"  # what `alpha` holds: the decay alpha, or "log": g = log(alpha)
 
     @property
     def n_tok(self) -> int:
@@ -100,7 +103,7 @@ class Problem:
 
 
 def _draw_tokens(rng: np.random.Generator, n_tok: int, heads: int, dk: int, dv: int,
-                 qkv_dtype: str):
+                 qkv_dtype: str, gate: str = "alpha"):
     def unit_rows(d):
         x = rng.standard_normal((n_tok, heads, d), dtype=np.float32)
         nrm = np.sqrt(np.sum(x * x, axis=-1, keepdims=True, dtype=np.float32))
@@ -115,7 +118,12 @@ def _draw_tokens(rng: np.random.Generator, n_tok: int, heads: int, dk: int, dv: 
         raise ValueError(qkv_dtype)
     x = rng.standard_normal((n_tok, heads), dtype=np.float32).astype(np.float64)
     y = rng.standard_normal((n_tok, heads), dtype=np.float32).astype(np.float64)
-    alpha = (1.0 / (1.0 + np.exp(x))).astype(np.float32)
+    if gate == "log":  # the same decay drawn in log space: g = -softplus(x)
+        alpha = (-np.log1p(np.exp(x))).astype(np.float32)
+    elif gate == "alpha":
+        alpha = (1.0 / (1.0 + np.exp(x))).astype(np.float32)
+    else:
+        raise ValueError(gate)
     beta = (1.0 / (1.0 + np.exp(-y))).astype(np.float32)
     return q, k, v, alpha, beta
 
@@ -139,7 +147,7 @@ def make_custom(*, batch: int, heads: int, dk: int, dv: int,
                 accept: str = "uniform", seed: int = 0, layer: int = 0,
                 slot_ids: Optional[np.ndarray] = None,
                 accepted: Optional[np.ndarray] = None,
-                name: str = "custom") -> Problem:
+                name: str = "custom", gate: str = "alpha") -> Problem:
     """Draw one problem.  Give either a uniform draft length T or per-request lengths.
 
     Slot ids and accepted lengths come from a stream that does not depend on
@@ -161,14 +169,14 @@ def make_custom(*, batch: int, heads: int, dk: int, dv: int,
         slot_ids = meta.permutation(pool_slots)[:batch].astype(np.int32)
     if accepted is None:
         accepted = _draw_accepted(meta, lens, accept)
-    q, k, v, alpha, beta = _draw_tokens(data, int(cu[-1]), heads, dk, dv, qkv_dtype)
+    q, k, v, alpha, beta = _draw_tokens(data, int(cu[-1]), heads, dk, dv, qkv_dtype, gate)
     s0 = (np.float32(0.1) * data.standard_normal((batch, heads, dk, dv), dtype=np.float32))
     return Problem(name=name, batch=batch, heads=heads, dk=dk, dv=dv,
                    max_T=int(lens.max()) if batch else 0, ragged=ragged,
                    qkv_dtype=qkv_dtype, cu_seqlens=cu, q=q, k=k, v=v, alpha=alpha,
                    beta=beta, pool_slots=pool_slots,
                    slot_ids=np.asarray(slot_ids, np.int32),
-                   accepted=np.asarray(accepted, np.int32), s0=s0.astype(np.float32))
+                   accepted=np.asarray(accepted, np.int32), s0=s0.astype(np.float32), gate=gate)
 
 
 # The five workloads: (name, recipe).  Seeds are 1000 + workload index.
@@ -270,14 +278,14 @@ def make_replay(prob: Problem, capacity: int, seed: int = 0,
     R = S if dense else len(named)
     k = np.zeros((R * C, H, prob.dk), np.float32)
     v = np.zeros((R * C, H, prob.dv), np.float32)
-    alpha = np.ones((R * C, H), np.float32)
+    alpha = np.full((R * C, H), 0.0 if prob.gate == "log" else 1.0, np.float32)  # decay 1
     beta = np.zeros((R * C, H), np.float32)
     lens = np.zeros(S, np.int32) if len_in is None else np.array(len_in, np.int32, copy=True)
     for r in range(prob.batch):
         s, T, c0 = int(prob.slot_ids[r]), int(prob.lengths[r]), int(prob.cu_seqlens[r])
         if len_in is None:
             lens[s] = rng.integers(0, C - T + 1)
-        _, ks, vs, al, be = _draw_tokens(rng, C, H, prob.dk, prob.dv, prob.qkv_dtype)
+        _, ks, vs, al, be = _draw_tokens(rng, C, H, prob.dk, prob.dv, prob.qkv_dtype, prob.gate)
         n = int(lens[s])
         if n + T > C:
             raise ValueError("buffered rows plus drafts exceed the capacity")

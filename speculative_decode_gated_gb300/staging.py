@@ -45,7 +45,7 @@ class DeviceProblem:
 
     def __init__(self, prob: Problem, device="cuda", pool: Optional[torch.Tensor] = None,
                  pool_fill: str = "sentinel", algo: int = binding.GDN_ALGO_AUTO,
-                 with_dev_err: bool = True, place_s0: bool = True):
+                 with_dev_err: bool = True, place_s0: bool = True, o_bf16: bool = False):
         self.host = prob
         dev = torch.device(device)
         self.q = qkv_tensor(prob.q, prob.qkv_dtype, dev)
@@ -63,15 +63,19 @@ class DeviceProblem:
         if place_s0:  # else the pool already holds the states (a later step)
             place_checkpoints(self.pool, prob)
         self.dev_err = torch.zeros(1, dtype=torch.int32, device=dev) if with_dev_err else None
-        self.o = torch.zeros((prob.n_tok, prob.heads, prob.dv), dtype=torch.float32, device=dev)
+        self.o = torch.zeros((prob.n_tok, prob.heads, prob.dv),
+                             dtype=torch.bfloat16 if o_bf16 else torch.float32, device=dev)
         self.algo = algo
+        # alpha holds g = log(alpha) for a log-space problem: the kernels apply expf
+        self.flags = ((binding.GDN_FLAG_O_BF16 if o_bf16 else 0)
+                      | (binding.GDN_FLAG_LOG_GATE if prob.gate == "log" else 0))
         self.c = self._make_c()
 
     def _make_c(self) -> binding.Problem:
         return binding.make_problem(q=self.q, k=self.k, v=self.v, alpha=self.alpha,
                                     beta=self.beta, pool=self.pool, slot_ids=self.slot_ids,
                                     max_T=self.host.max_T, cu_seqlens=self.cu_seqlens,
-                                    dev_err=self.dev_err, algo=self.algo)
+                                    dev_err=self.dev_err, algo=self.algo, flags=self.flags)
 
     def verify(self, stream=None):
         binding.gdn_verify(self.c, self.o, stream)

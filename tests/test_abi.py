@@ -63,7 +63,7 @@ def fake_problem(**over):
     """A problem with plausible, aligned fake device addresses (never dereferenced)."""
     c = binding.gdn_problem()
     c.batch, c.heads, c.dk, c.dv, c.max_T = 2, 4, 128, 128, 8
-    c.qkv_dtype, c.algo, c.reserved = binding.GDN_BF16, 0, 0
+    c.qkv_dtype, c.algo, c.flags = binding.GDN_BF16, 0, 0
     base = 1 << 40
     step = 1 << 32
     c.q, c.k, c.v = base, base + step, base + 2 * step
@@ -93,10 +93,10 @@ def call(lib, fn, c, o=O_PTR, acc=ACC_PTR):
 @pytest.mark.parametrize("fn", ["verify", "commit", "fused"])
 @pytest.mark.parametrize("over,status", [
     (dict(heads=0), 2), (dict(batch=-1), 2), (dict(max_T=-1), 2), (dict(max_T=1025), 2),
-    (dict(reserved=1), 2), (dict(pool_slots=1), 2),
+    (dict(flags=4), 2), (dict(flags=-1), 2), (dict(pool_slots=1), 2),
     (dict(cu_seqlens=(1 << 40) + 11 * (1 << 32), n_tok=-1), 2),
     (dict(qkv_dtype=5), 3),
-    (dict(dk=48), 4), (dict(dk=256), 4), (dict(dv=48), 4), (dict(dv=160), 4), (dict(algo=9), 4),
+    (dict(dk=48), 4), (dict(dk=512), 4), (dict(dv=48), 4), (dict(dv=160), 4), (dict(algo=9), 4),
     (dict(algo=2, qkv_dtype=0), 4), (dict(algo=2, dk=64, dv=64), 4),
     (dict(pool=None), 1), (dict(slot_ids=None), 1), (dict(q=None), 1), (dict(beta=None), 1),
     (dict(q=(1 << 40) + 8), 7), (dict(pool=(1 << 40) + 5 * (1 << 32) + 4), 7),

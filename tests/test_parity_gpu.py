@@ -63,6 +63,11 @@ SMALL = {
                                   T=64, pool_slots=3, accept="full", seed=23),
     "b2_h2_d128_t200": custom("b2_h2_d128_t200", batch=2, heads=2, dk=128, dv=128, T=200,
                               pool_slots=2, seed=24),
+    # dk = 256 (recurrent kernel, four threads per value column)
+    "b2_h2_dk256_dv64_t6": custom("b2_h2_dk256_dv64_t6", batch=2, heads=2, dk=256, dv=64, T=6,
+                                  pool_slots=3, seed=25),
+    "fp32_b2_h2_dk256_dv256_t5": custom("fp32_b2_h2_dk256_dv256_t5", batch=2, heads=2, dk=256,
+                                        dv=256, T=5, qkv_dtype="fp32", pool_slots=2, seed=26),
 }
 
 _cache = {}
