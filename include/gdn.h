@@ -88,8 +88,14 @@ typedef enum gdn_dtype {
 typedef enum gdn_algo {
     GDN_ALGO_AUTO = 0,
     GDN_ALGO_RECURRENT = 1,   /* per-token update on CUDA cores, any supported shape */
-    GDN_ALGO_CHUNK = 2        /* WY/chunk form, bf16 mma.sync for the state products; 16-token
+    GDN_ALGO_CHUNK = 2,       /* WY/chunk form, bf16 mma.sync for the state products; 16-token
                                  chunks, the state carried from one chunk to the next */
+    GDN_ALGO_CHUNK_TC = 3     /* the same chunk form with the two state-sized products on
+                                 tcgen05.mma (A = H^T staged in tensor memory, accumulators in
+                                 tensor memory) and the small solves on CUDA cores; same shapes
+                                 as GDN_ALGO_CHUNK, results within the same tolerance; opt-in
+                                 (slower than GDN_ALGO_CHUNK on 16-token chunks); no replay
+                                 buffer calls; layer batches run one launch per layer */
 } gdn_algo;
 
 /* Bits ORed into *dev_err by the kernels. */

@@ -21,7 +21,7 @@ GDN_ERR_DEVICE_ARG = 5
 GDN_ERR_ALIAS, GDN_ERR_LAYER_MISMATCH = 8, 9
 GDN_FP32, GDN_BF16 = 0, 1
 GDN_FLAG_O_BF16, GDN_FLAG_LOG_GATE = 1, 2
-GDN_ALGO_AUTO, GDN_ALGO_RECURRENT, GDN_ALGO_CHUNK = 0, 1, 2
+GDN_ALGO_AUTO, GDN_ALGO_RECURRENT, GDN_ALGO_CHUNK, GDN_ALGO_CHUNK_TC = 0, 1, 2, 3
 GDN_DEVERR_SLOT, GDN_DEVERR_ACCEPTED, GDN_DEVERR_SEQLEN = 1, 2, 4
 GDN_DEVERR_TIMEOUT, GDN_DEVERR_REPLAY = 8, 16
 GDN_MAX_T = 1024

@@ -86,6 +86,7 @@ int resolve_algo(const gdn_problem *p) {
                           (!p->cu_seqlens || p->n_tok >= 1);
     if (p->algo == GDN_ALGO_RECURRENT) return GDN_ALGO_RECURRENT;
     if (p->algo == GDN_ALGO_CHUNK) return chunk_ok ? GDN_ALGO_CHUNK : -1;
+    if (p->algo == GDN_ALGO_CHUNK_TC) return chunk_ok ? GDN_ALGO_CHUNK_TC : -1;
     return (chunk_ok && gdn::chunk_preferred(p->max_T)) ? GDN_ALGO_CHUNK : GDN_ALGO_RECURRENT;
 }
 
@@ -97,7 +98,7 @@ gdn_status validate(const gdn_problem *p, bool with_o, const void *o, bool with_
     if ((p->flags & ~kKnownFlags) != 0 || !shape_ok(p)) return GDN_ERR_BAD_DIM;
     if (p->qkv_dtype != GDN_FP32 && p->qkv_dtype != GDN_BF16) return GDN_ERR_BAD_DTYPE;
     if (!dims_supported(p->dk, p->dv)) return GDN_ERR_UNSUPPORTED;
-    if (p->algo < GDN_ALGO_AUTO || p->algo > GDN_ALGO_CHUNK) return GDN_ERR_UNSUPPORTED;
+    if (p->algo < GDN_ALGO_AUTO || p->algo > GDN_ALGO_CHUNK_TC) return GDN_ERR_UNSUPPORTED;
     *algo = resolve_algo(p);
     if (*algo < 0) return GDN_ERR_UNSUPPORTED;
     *empty = p->batch == 0;
@@ -155,6 +156,7 @@ gdn::Args make_args(const gdn_problem *p, const int32_t *accepted, void *o) {
     a.dev_err = p->dev_err;
     a.kv_rows = a.n_tok;
     a.flags = p->flags;
+    a.tc = p->algo == GDN_ALGO_CHUNK_TC;
     return a;
 }
 
@@ -168,8 +170,9 @@ gdn_status run(const gdn_problem *p, int mode, const int32_t *accepted, void *o,
     if (st != GDN_OK || empty) return st;
     const gdn::Args a = make_args(p, with_acc ? accepted : nullptr, with_o ? o : nullptr);
     const bool bf16 = p->qkv_dtype == GDN_BF16;
-    const cudaError_t e = algo == GDN_ALGO_CHUNK ? gdn::launch_chunk(&a, 1, mode, stream)
-                                                 : gdn::launch_recurrent(a, mode, bf16, stream);
+    const bool chunk = algo == GDN_ALGO_CHUNK || algo == GDN_ALGO_CHUNK_TC;
+    const cudaError_t e = chunk ? gdn::launch_chunk(&a, 1, mode, stream)
+                                : gdn::launch_recurrent(a, mode, bf16, stream);
     if (e != cudaSuccess) {
         set_cuda_error(e, "kernel launch");
         return GDN_ERR_CUDA;
@@ -230,7 +233,7 @@ gdn_status run_layers(const gdn_problem *ps, int32_t n, int mode, const int32_t 
             a[l] = make_args(&ps[l0 + l], with_acc ? accepted : nullptr,
                              with_o ? o[l0 + l] : nullptr);
         cudaError_t e = cudaSuccess;
-        if (algo == GDN_ALGO_CHUNK) {
+        if (algo == GDN_ALGO_CHUNK || algo == GDN_ALGO_CHUNK_TC) {
             e = gdn::launch_chunk(a, m, mode, stream);
         } else {
             for (int l = 0; l < m && e == cudaSuccess; ++l)
@@ -381,7 +384,7 @@ int32_t gdn_select_algo(const gdn_problem *p) {
     if (!p || !shape_ok(p)) return -1;
     if (p->qkv_dtype != GDN_FP32 && p->qkv_dtype != GDN_BF16) return -1;
     if (!dims_supported(p->dk, p->dv)) return -1;
-    if (p->algo < GDN_ALGO_AUTO || p->algo > GDN_ALGO_CHUNK) return -1;
+    if (p->algo < GDN_ALGO_AUTO || p->algo > GDN_ALGO_CHUNK_TC) return -1;
     return resolve_algo(p);
 }
 

@@ -69,10 +69,18 @@ constexpr uint32_t kTokHalfBytes = CT * 64 * 2;   // token box: 64 of 128 bf16 x
 constexpr uint32_t kTokBytes = 2 * kTokHalfBytes; // one [16][128] bf16 tile
 constexpr unsigned long long kWaitNs = 2000000000ull;
 
-struct TokBuf {  // 1024-byte aligned: three swizzled [16][128] bf16 tiles
-    unsigned char k[kTokBytes];
-    unsigned char q[kTokBytes];
-    unsigned char v[kTokBytes];
+// Token tiles of one step, 1024-byte aligned, each a swizzled [16][128] bf16
+// tile in two halves of 64 columns (one TMA box each).  The q and k halves of
+// the same columns sit next to each other, so [q; k] is one 32-row operand of
+// uniform row-group stride for the tensor cores.
+constexpr uint32_t kQKStride = 2 * kTokHalfBytes;  // q/k: bytes from one column half to the next
+struct TokBuf {
+    unsigned char qk[2][2][kTokHalfBytes];  // [column half][0: q, 1: k]
+    unsigned char v[kTokBytes];             // halves kTokHalfBytes apart
+    __device__ unsigned char *q() { return qk[0][0]; }
+    __device__ unsigned char *k() { return qk[0][1]; }
+    __device__ const unsigned char *q() const { return qk[0][0]; }
+    __device__ const unsigned char *k() const { return qk[0][1]; }
 };
 
 struct Aux {
@@ -84,6 +92,8 @@ struct Aux {
     float dcol[CT];         // D[a'-1][s] for s < a' (a' = the commit point within the chunk), else 0
     float dlast[CT];        // D[15][s]: the whole chunk's decay to its end
     unsigned long long tile_full, tok_full[2];
+    unsigned long long mma_full;  // tcgen05 products completed
+    uint32_t tmem_base;           // TMEM address of this block's columns
     int abort_flag;
 };
 
@@ -188,13 +198,127 @@ __device__ __forceinline__ void ldsm_x4_trans(uint32_t &r0, uint32_t &r1, uint32
 
 // Byte offset of bf16 element (t, i) in a swizzled [16][128] token tile
 // (two boxes of 64 columns, 128 bytes per token row).
-__device__ __forceinline__ uint32_t tok_off(int t, int i) {
-    return (uint32_t)((i >> 6) * kTokHalfBytes + t * 128 + ((((i & 63) >> 3) ^ (t & 7)) << 4) +
-                      (i & 7) * 2);
+// `half` = bytes from one column half to the next: kQKStride for q and k,
+// kTokHalfBytes for v.
+__device__ __forceinline__ uint32_t tok_off(int t, int i, uint32_t half) {
+    return (uint32_t)((i >> 6) * half + t * 128 + ((((i & 63) >> 3) ^ (t & 7)) << 4) + (i & 7) * 2);
 }
 
+// Two adjacent bf16 of q or k (half stride kQKStride).
 __device__ __forceinline__ uint32_t ld_tok32(const unsigned char *tile, int t, int i) {
-    return *reinterpret_cast<const uint32_t *>(tile + tok_off(t, i));
+    return *reinterpret_cast<const uint32_t *>(tile + tok_off(t, i, kQKStride));
+}
+
+// ------------------------------------------------------------ tcgen05 helpers
+//
+// Tensor memory (TMEM) of one block: 256 of the SM's 512 columns (two blocks
+// per SM), 128 lanes of 32 bits each.  A TMEM address is (lane << 16) | column;
+// warp w of the block reaches lanes [32w, 32w + 32) only, lane 32w + t from
+// its thread t.
+constexpr uint32_t kTmemCols = 256;
+constexpr uint32_t kTmP = 0;      // P^T = H^T Q^T accumulator: 16 columns (one per token)
+constexpr uint32_t kTmZ = 16;     // Z^T = H^T K^T accumulator: 16 columns
+constexpr uint32_t kTmAhi = 32;   // A = H^T as bf16 hi, 64 columns (two key rows per column)
+constexpr uint32_t kTmAlo = 96;   // A = H^T as bf16 lo, 64 columns
+constexpr uint32_t kTmS = 32;     // state-update accumulator (128 columns, over A once it is used)
+constexpr uint32_t kTmWhi = 160;  // (diag(d) W)^T as bf16 hi, 8 columns (two tokens per column)
+constexpr uint32_t kTmWlo = 168;  // and lo
+
+__device__ __forceinline__ void tmem_alloc(uint32_t dst_smem) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;\n" ::"r"(dst_smem),
+                 "r"(kTmemCols)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;\n" ::: "memory");
+}
+
+__device__ __forceinline__ void tmem_dealloc(uint32_t taddr) {
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;\n" ::"r"(taddr), "r"(kTmemCols)
+                 : "memory");
+}
+
+__device__ __forceinline__ void tc_fence_before() {
+    asm volatile("tcgen05.fence::before_thread_sync;\n" ::: "memory");
+}
+__device__ __forceinline__ void tc_fence_after() {
+    asm volatile("tcgen05.fence::after_thread_sync;\n" ::: "memory");
+}
+
+// Thread t of warp w: 16 (or 8) consecutive 32-bit columns of lane 32w + t.
+__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16]) {
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, "
+        "%12, %13, %14, %15, %16};\n" ::"r"(taddr),
+        "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]),
+        "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15])
+        : "memory");
+}
+__device__ __forceinline__ void tmem_st8(uint32_t taddr, const uint32_t (&r)[8]) {
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};\n" ::"r"(taddr),
+        "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7])
+        : "memory");
+}
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, float (&f)[16]) {
+    uint32_t r[16];
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, "
+        "%12, %13, %14, %15}, [%16];\n"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+          "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
+          "=r"(r[14]), "=r"(r[15])
+        : "r"(taddr)
+        : "memory");
+#pragma unroll
+    for (int i = 0; i < 16; ++i) f[i] = __uint_as_float(r[i]);
+}
+__device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;\n" ::: "memory"); }
+__device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;\n" ::: "memory"); }
+
+// Shared-memory matrix descriptor (tcgen05 format): start address, leading and
+// stride byte offsets (16-byte units), version 1, 128-byte swizzle.  The
+// matrices it describes are the TMA-written token tiles: rows of 128 bytes in
+// 1024-byte groups of eight, 16-byte chunks XOR-swizzled by row % 8.
+__device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
+    uint64_t d = (uint64_t)((saddr & 0x3FFFFu) >> 4);
+    d |= (uint64_t)((lbo >> 4) & 0x3FFFu) << 16;
+    d |= (uint64_t)((sbo >> 4) & 0x3FFFu) << 32;
+    d |= (uint64_t)1 << 46;  // descriptor version
+    d |= (uint64_t)2 << 61;  // 128-byte swizzle
+    return d;
+}
+
+// Instruction descriptor of kind::f16: bf16 A and B, fp32 accumulator, A
+// K-major (it comes from TMEM), B K-major or MN-major, M = 128, N = n.
+__host__ __device__ constexpr uint32_t umma_idesc(uint32_t n, bool b_mn_major) {
+    return (1u << 4)                       // accumulator: f32
+           | (1u << 7) | (1u << 10)        // A, B: bf16
+           | ((b_mn_major ? 1u : 0u) << 16)
+           | ((n >> 3) << 17)              // N / 8
+           | ((128u >> 4) << 24);          // M / 16
+}
+
+// D (TMEM) = A (TMEM) B (shared memory) [+ D]: one 128 x N x 16 product, issued
+// by one thread, completing asynchronously (see umma_commit).
+__device__ __forceinline__ void umma_ts(uint32_t d, uint32_t a, uint64_t bdesc, uint32_t idesc,
+                                        uint32_t accumulate) {
+    asm volatile(
+        "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
+        " tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n}\n" ::"r"(d),
+        "r"(a), "l"(bdesc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
+// The mbarrier receives one arrival once every product issued before by this
+// thread has completed (and its TMEM results are visible).
+__device__ __forceinline__ void umma_commit(uint32_t bar) {
+    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n" ::"r"(
+                     bar)
+                 : "memory");
+}
+
+// fp32 pair -> bf16x2 words hi and lo (element 0 in the low half).
+__device__ __forceinline__ void split_pair(float x0, float x1, uint32_t &hi, uint32_t &lo) {
+    split2(x0, x1, hi, lo);
 }
 
 // ------------------------------------------------------------ per-unit plan
@@ -309,10 +433,10 @@ __device__ __forceinline__ void issue_tokens(const Maps &maps, const UnitPlan &p
     mbar_arrive_expect_tx(tok_bar, (MODE == kCommit ? 2u : 3u) * kTokBytes);
 #pragma unroll
     for (int hb = 0; hb < 2; ++hb) {
-        tma_load_3d(smem_u32(tb.k) + hb * kTokHalfBytes, &maps.k, 64 * hb, pl.h, row, tok_bar);
+        tma_load_3d(smem_u32(tb.qk[hb][1]), &maps.k, 64 * hb, pl.h, row, tok_bar);
         tma_load_3d(smem_u32(tb.v) + hb * kTokHalfBytes, &maps.v, 64 * hb, pl.h, row, tok_bar);
         if (MODE != kCommit)
-            tma_load_3d(smem_u32(tb.q) + hb * kTokHalfBytes, &maps.q, 64 * hb, pl.h, qrow, tok_bar);
+            tma_load_3d(smem_u32(tb.qk[hb][0]), &maps.q, 64 * hb, pl.h, qrow, tok_bar);
     }
 }
 
@@ -410,6 +534,10 @@ constexpr int CW = D / NW;       // 32 columns per warp
 constexpr int MT = CW / 16;      // 2 m-tiles
 constexpr int CPT = 2 * MT;      // 4 columns per lane
 constexpr int kTinvLanes = CT / NW;  // Tinv columns per warp
+// Threads that issue the copies (each issue may stall its warp for a while when
+// the copy engine is busy, so the work is spread over warps 1-3; warp 0
+// issues the tensor-core products).
+constexpr int kTokIssuer = 96, kTileIssuer = 32, kPrefIssuer = 64;
 
 // Columns CPT g + [0, CPT) of warp w's slice, key row `row`, from the swizzled tile.
 __device__ __forceinline__ float4 ld_tile_row(const unsigned char *tile, int warp, int g, int row) {
@@ -455,7 +583,7 @@ __device__ __forceinline__ void state_update(float (&hr)[8][4][CPT], const float
 #pragma unroll
             for (int e = 0; e < CPT; ++e) hv[rr][e] = gam * hr[kb][rr][e];
         uint32_t b00, b01, b10, b11;  // (n-tile 2kb: b0, b1), (n-tile 2kb+1: b0, b1)
-        ldsm_x4_trans(b00, b01, b10, b11, k_smem + tok_off(krow, 16 * kb + 8 * (mi >> 1)));
+        ldsm_x4_trans(b00, b01, b10, b11, k_smem + tok_off(krow, 16 * kb + 8 * (mi >> 1), kQKStride));
 #pragma unroll
         for (int m = 0; m < MT; ++m) {
             mma(hv[0][2 * m], hv[1][2 * m], hv[0][2 * m + 1], hv[1][2 * m + 1], ah[m][0], ah[m][1],
@@ -488,7 +616,11 @@ __device__ __forceinline__ void state_update(float (&hr)[8][4][CPT], const float
 // the verify kernel keeps no state in registers.  VAR: the call's flags (bf16
 // o, log-space gates) are read at run time; otherwise they are 0 at compile
 // time, so the default calls carry no code for the variants.
-template <int MODE, bool RAGGED, int NL, bool MULTI, bool REPLAY, bool VAR>
+//
+// TC: the two state-sized products on tcgen05 (A = H^T in TMEM, accumulators in
+// TMEM, one issuing thread) instead of mma.sync; the small solves and the
+// outputs then run on CUDA cores with one value column per thread.
+template <int MODE, bool RAGGED, int NL, bool MULTI, bool REPLAY, bool VAR, bool TC>
 __global__ void __launch_bounds__(kThreads, kBlocksPerSM)
     chunk_kernel(const __grid_constant__ Launch<NL> L) {
     extern __shared__ unsigned char smem_raw[];
@@ -516,6 +648,7 @@ __global__ void __launch_bounds__(kThreads, kBlocksPerSM)
         mbar_init(tile_bar, 1);
         mbar_init(smem_u32(&ax.tok_full[0]), 1);
         mbar_init(smem_u32(&ax.tok_full[1]), 1);
+        mbar_init(smem_u32(&ax.mma_full), 1);
         ax.abort_flag = 0;
         asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
 #pragma unroll
@@ -523,7 +656,15 @@ __global__ void __launch_bounds__(kThreads, kBlocksPerSM)
             asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&L.maps[0].pool + m))
                          : "memory");
     }
+    if (TC && warp == 0) tmem_alloc(smem_u32(&ax.tmem_base));
+    tc_fence_before();
     __syncthreads();
+    tc_fence_after();
+    const uint32_t tm = TC ? ax.tmem_base : 0u;           // lane 0, first column
+    const uint32_t tl = tm + ((uint32_t)(32 * warp) << 16);  // this warp's first lane
+    const uint32_t mma_bar = smem_u32(&ax.mma_full);
+    int mma_phase = 0;
+    const int j = 32 * warp + lane;  // tcgen05 path: this thread's value column
     if (tid == 0) early_prefetch<MODE, RAGGED, NL, REPLAY>(L, blockIdx.x, G, W, U);
     asm volatile("griddepcontrol.wait;" ::: "memory");
 
@@ -570,7 +711,9 @@ __global__ void __launch_bounds__(kThreads, kBlocksPerSM)
     // The unit's state as H^T in the A-fragment layout: the checkpoint tile,
     // then the state after each chunk (single-chunk verify needs none).
     constexpr bool kKeep = MULTI || MODE != kVerify;
-    float hr[kKeep ? 8 : 1][4][CPT];
+    float hr[kKeep ? 8 : 1][4][CPT];  // mma.sync path (unused, and removed, on the tcgen05 path)
+    // tcgen05 path: this thread's column of the state (key rows 0..127).
+    float hcol[(kKeep && TC) ? D : 1];
 
     bool aborted = false;
     for (; unit < W; unit += G) {
@@ -587,15 +730,14 @@ __global__ void __launch_bounds__(kThreads, kBlocksPerSM)
             gb = gate_load(L.a[cur.layer].beta, p, cur, 0, tid);
             if (!cur.skip && issued == processed) {
                 // Nothing is in flight: the next unit's loads can all go now.
-                if (tid == 0) {
+                if (tid == kTokIssuer)
                     issue_tokens<MODE>(L.maps[cur.layer], cur, 0, sm.tok[tok_issued & 1],
                                        smem_u32(&ax.tok_full[tok_issued & 1]));
-                    issue_tile(L.maps[cur.layer], cur, sm.tile, tile_bar);
-                }
+                if (tid == kTileIssuer) issue_tile(L.maps[cur.layer], cur, sm.tile, tile_bar);
                 ++issued;
                 ++tok_issued;
             }
-            if (tid == 0 && !nxt.skip) prefetch_unit<MODE>(L.maps[nxt.layer], nxt);
+            if (tid == kPrefIssuer && !nxt.skip) prefetch_unit<MODE>(L.maps[nxt.layer], nxt);
             continue;
         }
         const int Tu = me.teff;  // tokens of the unit that matter: T_r, or a_r for commit
@@ -612,7 +754,7 @@ __global__ void __launch_bounds__(kThreads, kBlocksPerSM)
             __syncthreads();  // the previous step is done with the small matrices
             // The next step's token block goes into the other buffer now.
             if (tok_issued == steps + 1 && (more || !cur.skip)) {
-                if (tid == 0) {
+                if (tid == kTokIssuer) {
                     TokBuf &nb = sm.tok[tok_issued & 1];
                     const uint32_t nbar = smem_u32(&ax.tok_full[tok_issued & 1]);
                     if (more)
@@ -648,7 +790,7 @@ __global__ void __launch_bounds__(kThreads, kBlocksPerSM)
             // 2. Gram blocks k_t.k_s and q_t.k_s: warp w computes matrix w / 2,
             //    columns 8 (w % 2) + [0, 8), over all 128 key dims.
             {
-                const unsigned char *At = (warp >> 1) ? tb.q : tb.k;
+                const unsigned char *At = (warp >> 1) ? tb.q() : tb.k();
                 const int nt = warp & 1;
                 float a0[4] = {0.f, 0.f, 0.f, 0.f}, a1[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
@@ -657,8 +799,8 @@ __global__ void __launch_bounds__(kThreads, kBlocksPerSM)
                     float *acc = (kb & 1) ? a1 : a0;
                     mma(acc[0], acc[1], acc[2], acc[3], ld_tok32(At, g, col),
                         ld_tok32(At, g + 8, col), ld_tok32(At, g, col + 8),
-                        ld_tok32(At, g + 8, col + 8), ld_tok32(tb.k, 8 * nt + g, col),
-                        ld_tok32(tb.k, 8 * nt + g, col + 8));
+                        ld_tok32(At, g + 8, col + 8), ld_tok32(tb.k(), 8 * nt + g, col),
+                        ld_tok32(tb.k(), 8 * nt + g, col + 8));
                 }
                 float(*Gm)[CT] = ax.gram[warp >> 1];
                 Gm[g][8 * nt + 2 * c] = a0[0] + a1[0];
@@ -705,6 +847,229 @@ __global__ void __launch_bounds__(kThreads, kBlocksPerSM)
                     aborted = true;
                     break;
                 }
+            }
+
+            if constexpr (TC) {
+                // 5. The state at the chunk's start as A = H^T in TMEM, bf16 hi and
+                //    lo (thread t of warp w holds value column j = 32w + t: TMEM lane j,
+                //    two key rows per 32-bit column), then, issued by thread 0 on the
+                //    tensor cores: P^T = H^T Q^T and Z^T = H^T K^T (M = 128 value
+                //    columns, N = 16 tokens, K = 128 key rows, hi and lo products).
+                //    From the staged tile (first chunk) or from the state in registers.
+                const bool outs = MODE != kCommit && (!REPLAY || CT * ch + T > me.nskip);
+                {
+                    const unsigned char *box = sm.tile + warp * kBoxBytes + (lane & 3) * 4;
+#pragma unroll
+                    for (int q4 = 0; q4 < 4; ++q4) {
+                        uint32_t wh[16], wl[16];
+#pragma unroll
+                        for (int pp = 0; pp < 16; ++pp) {
+                            const int i0 = 32 * q4 + 2 * pp;
+                            float x0, x1;
+                            if (!MULTI || ch == 0) {
+                                x0 = *reinterpret_cast<const float *>(
+                                    box + i0 * 128 + (((lane >> 2) ^ (i0 & 7)) << 4));
+                                x1 = *reinterpret_cast<const float *>(
+                                    box + (i0 + 1) * 128 + (((lane >> 2) ^ ((i0 + 1) & 7)) << 4));
+                                if (kKeep) {
+                                    hcol[kKeep ? i0 : 0] = x0;
+                                    hcol[kKeep ? i0 + 1 : 0] = x1;
+                                }
+                            } else {
+                                x0 = hcol[kKeep ? i0 : 0];
+                                x1 = hcol[kKeep ? i0 + 1 : 0];
+                            }
+                            split2(x0, x1, wh[pp], wl[pp]);
+                        }
+                        tmem_st16(tl + kTmAhi + 16 * q4, wh);
+                        tmem_st16(tl + kTmAlo + 16 * q4, wl);
+                    }
+                    tmem_wait_st();
+                }
+                tc_fence_before();
+                __syncthreads();
+                // The tile is in TMEM (and registers): the stage is free for the next unit.
+                if (!MULTI || ch == 0) {
+                    ++processed;
+                    if (!cur.skip) {
+                        if (tid == kTileIssuer) issue_tile(L.maps[cur.layer], cur, sm.tile, tile_bar);
+                        ++issued;
+                    }
+                    if (tid == kPrefIssuer && !nxt.skip) prefetch_unit<MODE>(L.maps[nxt.layer], nxt);
+                }
+                if (tid == 0) {
+                    // [Q; K] (32 token rows: P and Z in one product) or K alone (16 rows).
+                    tc_fence_after();
+                    const uint32_t id = outs ? umma_idesc(32, false) : umma_idesc(16, false);
+                    const uint32_t d = outs ? tm + kTmP : tm + kTmZ;
+                    const uint32_t b0 = smem_u32(outs ? tb.qk[0][0] : tb.qk[0][1]);
+#pragma unroll
+                    for (int kk = 0; kk < 8; ++kk) {
+                        const uint64_t b = sw128_desc(b0 + (kk >> 2) * kQKStride + (kk & 3) * 32, 16, 1024);
+                        umma_ts(d, tm + kTmAhi + 8 * kk, b, id, kk > 0 ? 1u : 0u);
+                        umma_ts(d, tm + kTmAlo + 8 * kk, b, id, 1u);
+                    }
+                    umma_commit(mma_bar);
+                }
+
+                // While the products run: Tinv = (I + A)^-1 by forward substitution.
+                // Lane groups compute column tj = w + 4 (lane % 4); the first 4 lanes
+                // store it.  x_t = [t == tj, t < T] - sum_{s<t} A[t][s] x_s gives zeros
+                // above the diagonal and in rows t >= T (A is zero there).
+                {
+                    const int tj = warp + NW * (lane % kTinvLanes);
+                    float xt[CT];
+#pragma unroll
+                    for (int t = 0; t < CT; ++t) {
+                        float acc = (t == tj && t < T) ? 1.0f : 0.0f;
+#pragma unroll
+                        for (int s4 = 0; s4 < t; s4 += 4) {
+                            const float4 a4 = *reinterpret_cast<const float4 *>(&ax.A[t][s4]);
+                            acc = fmaf(-a4.x, xt[s4], acc);
+                            if (s4 + 1 < t) acc = fmaf(-a4.y, xt[s4 + 1], acc);
+                            if (s4 + 2 < t) acc = fmaf(-a4.z, xt[s4 + 2], acc);
+                            if (s4 + 3 < t) acc = fmaf(-a4.w, xt[s4 + 3], acc);
+                        }
+                        xt[t] = acc;
+                        if (lane < kTinvLanes) ax.Tinv[t][tj] = acc;
+                    }
+                }
+                const bool mma_ok = wait_parity(mma_bar, mma_phase & 1);
+                ++mma_phase;
+                if (__syncthreads_or(!mma_ok)) {  // also: Tinv is complete
+                    aborted = true;
+                    break;
+                }
+                tc_fence_after();
+                float pz[CT], zz[CT];
+                if (outs) tmem_ld16(tl + kTmP, pz);
+                tmem_ld16(tl + kTmZ, zz);
+                tmem_wait_ld();
+
+                // 6. r_t = beta_t (v_t - gamma_t Z_t) for this thread's column (0 for t >= T);
+                // 7. w = Tinv r (Tinv is zero above its diagonal and in rows t >= T).
+                float w[CT];
+                {
+                    float r[CT];
+#pragma unroll
+                    for (int t = 0; t < CT; ++t) {
+                        const uint32_t vb =
+                            *reinterpret_cast<const unsigned short *>(tb.v + tok_off(t, j, kTokHalfBytes));
+                        const float vt = __uint_as_float(vb << 16);
+                        r[t] = t < T ? ax.beta[t] * (vt - ax.gamma[t] * zz[t]) : 0.0f;
+                    }
+#pragma unroll
+                    for (int t = 0; t < CT; ++t) {
+                        float acc = 0.0f;
+#pragma unroll
+                        for (int s4 = 0; s4 <= t; s4 += 4) {
+                            const float4 a4 = *reinterpret_cast<const float4 *>(&ax.Tinv[t][s4]);
+                            acc = fmaf(a4.x, r[s4], acc);
+                            acc = fmaf(a4.y, r[s4 + 1], acc);
+                            acc = fmaf(a4.z, r[s4 + 2], acc);
+                            acc = fmaf(a4.w, r[s4 + 3], acc);
+                        }
+                        w[t] = acc;
+                    }
+                }
+
+                // 8. o_t = gamma_t P_t + sum_{s<=t} M[t][s] w_s (M is zero above its
+                //    diagonal); a warp stores 32 adjacent columns of one token row.
+                if (MODE != kCommit && outs) {
+                    const long long orow = (long long)me.qrow0 + CT * ch;
+                    const bool o_bf16 = flags & GDN_FLAG_O_BF16;
+                    float *go = static_cast<float *>(L.a[me.layer].o) + me.h * D + j;
+                    __nv_bfloat16 *gob = static_cast<__nv_bfloat16 *>(L.a[me.layer].o) + me.h * D + j;
+                    float ov[CT];  // all outputs first: no store sits between the M loads
+#pragma unroll
+                    for (int t = 0; t < CT; ++t) {
+                        float acc = ax.gamma[t] * pz[t];
+#pragma unroll
+                        for (int s4 = 0; s4 <= t; s4 += 4) {
+                            const float4 m4 = *reinterpret_cast<const float4 *>(&ax.M[t][s4]);
+                            acc = fmaf(m4.x, w[s4], acc);
+                            acc = fmaf(m4.y, w[s4 + 1], acc);
+                            acc = fmaf(m4.z, w[s4 + 2], acc);
+                            acc = fmaf(m4.w, w[s4 + 3], acc);
+                        }
+                        ov[t] = acc;
+                    }
+#pragma unroll
+                    for (int t = 0; t < CT; ++t) {
+                        if (t < T && CT * ch + t >= me.nskip) {
+                            const size_t i = (size_t)(orow + t) * row_stride;
+                            if (o_bf16)
+                                gob[i] = __float2bfloat16_rn(ov[t]);
+                            else
+                                go[i] = ov[t];
+                        }
+                    }
+                }
+
+                // 9. The committed state (its chunk only), then the state after the
+                //    whole chunk when another chunk follows:
+                //      H^T <- gam H^T + (diag(dvec) W)^T K  (tensor cores: M = 128 value
+                //      columns, N = 128 key rows, K = 16 tokens, K from its MN-major tile)
+                const bool commit_here = MODE == kCommit ? !more : (MODE == kFused && ch == ca);
+                if constexpr (kKeep) {
+                    bool mma_failed = false;
+#pragma unroll 1
+                    for (int pass = 0; pass < 2; ++pass) {
+                        const bool store = pass == 0;
+                        if (store ? !commit_here : !more) continue;
+                        const float *dvec = store ? ax.dcol : ax.dlast;
+                        const float gam = store ? ax.gamma[me.u.a - CT * ch - 1] : ax.gamma[CT - 1];
+                        {
+                            uint32_t wh[8], wl[8];
+#pragma unroll
+                            for (int pp = 0; pp < 8; ++pp)
+                                split2(dvec[2 * pp] * w[2 * pp], dvec[2 * pp + 1] * w[2 * pp + 1], wh[pp],
+                                       wl[pp]);
+                            tmem_st8(tl + kTmWhi, wh);
+                            tmem_st8(tl + kTmWlo, wl);
+                            tmem_wait_st();
+                        }
+                        tc_fence_before();
+                        __syncthreads();
+                        if (tid == 0) {
+                            tc_fence_after();
+                            constexpr uint32_t id128 = umma_idesc(128, true);
+                            const uint64_t bk = sw128_desc(smem_u32(tb.qk[0][1]), kQKStride, 1024);
+                            umma_ts(tm + kTmS, tm + kTmWhi, bk, id128, 0u);
+                            umma_ts(tm + kTmS, tm + kTmWlo, bk, id128, 1u);
+                            umma_commit(mma_bar);
+                        }
+                        const bool ok2 = wait_parity(mma_bar, mma_phase & 1);
+                        ++mma_phase;
+                        if (__syncthreads_or(!ok2)) {
+                            mma_failed = true;
+                            break;
+                        }
+                        tc_fence_after();
+                        float *dst = opaque(me.u.tile) + j;
+#pragma unroll
+                        for (int q8 = 0; q8 < 8; ++q8) {
+                            float sv[16];
+                            tmem_ld16(tl + kTmS + 16 * q8, sv);
+                            tmem_wait_ld();
+#pragma unroll
+                            for (int e = 0; e < 16; ++e) {
+                                const int i = 16 * q8 + e;
+                                const float hv = fmaf(gam, hcol[kKeep ? i : 0], sv[e]);
+                                if (store)
+                                    dst[i * D] = hv;
+                                else
+                                    hcol[kKeep ? i : 0] = hv;
+                            }
+                        }
+                    }
+                    if (mma_failed) {
+                        aborted = true;
+                        break;
+                    }
+                }
+                ++steps;
+                continue;
             }
 
             // 5. P = H^T Q^T and Z = H^T K^T for this warp's columns, H the state at
@@ -765,7 +1130,7 @@ __global__ void __launch_bounds__(kThreads, kBlocksPerSM)
                 uint32_t b[4][2];
 #pragma unroll
                 for (int nt = NT0; nt < 4; ++nt) {
-                    const unsigned char *Bt = nt < 2 ? tb.q : tb.k;
+                    const unsigned char *Bt = nt < 2 ? tb.q() : tb.k();
                     const int tok = 8 * (nt & 1) + g;
                     b[nt][0] = ld_tok32(Bt, tok, 16 * kb + 2 * c);
                     b[nt][1] = ld_tok32(Bt, tok, 16 * kb + 2 * c + 8);
@@ -798,10 +1163,10 @@ __global__ void __launch_bounds__(kThreads, kBlocksPerSM)
             if (!MULTI || ch == 0) {
                 ++processed;
                 if (!cur.skip) {
-                    if (tid == 0) issue_tile(L.maps[cur.layer], cur, sm.tile, tile_bar);
+                    if (tid == kTileIssuer) issue_tile(L.maps[cur.layer], cur, sm.tile, tile_bar);
                     ++issued;
                 }
-                if (tid == 0 && !nxt.skip) prefetch_unit<MODE>(L.maps[nxt.layer], nxt);
+                if (tid == kPrefIssuer && !nxt.skip) prefetch_unit<MODE>(L.maps[nxt.layer], nxt);
             }
 
             // Token indices of this thread in the fragments: n-tile half ntt, element e:
@@ -816,7 +1181,7 @@ __global__ void __launch_bounds__(kThreads, kBlocksPerSM)
                     for (int eo = 0; eo < 2; ++eo) {
                         const int t = 8 * ntt + 2 * c + eo;
                         const uint32_t vv =
-                            *reinterpret_cast<const uint32_t *>(tb.v + tok_off(t, col0 + 2 * m));
+                            *reinterpret_cast<const uint32_t *>(tb.v + tok_off(t, col0 + 2 * m, kTokHalfBytes));
                         const float v0 = __uint_as_float(vv << 16);
                         const float v1 = __uint_as_float(vv & 0xFFFF0000u);
                         const float bt = ax.beta[t], gt = ax.gamma[t];
@@ -911,9 +1276,9 @@ __global__ void __launch_bounds__(kThreads, kBlocksPerSM)
             if constexpr (kKeep) {
                 if (commit_here)
                     state_update<true>(hr, wq, ax.dcol, ax.gamma[me.u.a - CT * ch - 1],
-                                       smem_u32(tb.k), lane, c, opaque(me.u.tile) + col0);
+                                       smem_u32(tb.k()), lane, c, opaque(me.u.tile) + col0);
                 if (more)
-                    state_update<false>(hr, wq, ax.dlast, ax.gamma[CT - 1], smem_u32(tb.k), lane,
+                    state_update<false>(hr, wq, ax.dlast, ax.gamma[CT - 1], smem_u32(tb.k()), lane,
                                         c, nullptr);
             }
             ++steps;
@@ -932,6 +1297,11 @@ __global__ void __launch_bounds__(kThreads, kBlocksPerSM)
     if (tid == 0 && aborted)
         for (int l = 0; l < (NL == 1 ? 1 : L.n); ++l)
             if (L.a[l].dev_err) atomicOr(L.a[l].dev_err, GDN_DEVERR_TIMEOUT);
+    if (TC) {
+        tc_fence_before();
+        __syncthreads();
+        if (warp == 0) tmem_dealloc(tm);
+    }
 }
 
 // ------------------------------------------------------------ host side
@@ -968,7 +1338,7 @@ constexpr int kMaxDevices = 64;
 
 struct DeviceInfo {
     int sms = 0;
-    bool smem_set[3][2][2][2][2][2] = {};  // [mode][ragged][batched][multi][replay][var]
+    bool smem_set[3][2][2][2][2][2][2] = {};  // [mode][ragged][batched][multi][replay][var][tc]
 };
 
 DeviceInfo g_dev[kMaxDevices];
@@ -976,7 +1346,8 @@ std::mutex g_dev_mutex;
 
 static_assert(sizeof(Launch<kChunkMaxLayers>) <= 32764, "kernel parameter space");
 
-template <int MODE, bool RAGGED, int NL, bool MULTI, bool REPLAY = false, bool VAR = false>
+template <int MODE, bool RAGGED, int NL, bool MULTI, bool REPLAY = false, bool VAR = false,
+          bool TC = false>
 cudaError_t launch_mode(const Launch<NL> &L, cudaStream_t stream) {
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
@@ -990,11 +1361,11 @@ cudaError_t launch_mode(const Launch<NL> &L, cudaStream_t stream) {
             e = cudaDeviceGetAttribute(&info.sms, cudaDevAttrMultiProcessorCount, dev);
             if (e != cudaSuccess) return e;
         }
-        if (!info.smem_set[MODE][RAGGED][NL != 1][MULTI][REPLAY][VAR]) {
-            e = cudaFuncSetAttribute(chunk_kernel<MODE, RAGGED, NL, MULTI, REPLAY, VAR>,
+        if (!info.smem_set[MODE][RAGGED][NL != 1][MULTI][REPLAY][VAR][TC]) {
+            e = cudaFuncSetAttribute(chunk_kernel<MODE, RAGGED, NL, MULTI, REPLAY, VAR, TC>,
                                      cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
             if (e != cudaSuccess) return e;
-            info.smem_set[MODE][RAGGED][NL != 1][MULTI][REPLAY][VAR] = true;
+            info.smem_set[MODE][RAGGED][NL != 1][MULTI][REPLAY][VAR][TC] = true;
         }
         sms = info.sms;
     }
@@ -1011,7 +1382,7 @@ cudaError_t launch_mode(const Launch<NL> &L, cudaStream_t stream) {
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, chunk_kernel<MODE, RAGGED, NL, MULTI, REPLAY, VAR>, L);
+    return cudaLaunchKernelEx(&cfg, chunk_kernel<MODE, RAGGED, NL, MULTI, REPLAY, VAR, TC>, L);
 }
 
 // The pool and token tensor maps of one layer.
@@ -1071,6 +1442,19 @@ cudaError_t launch_layers(const Args *layers, int n, int mode, cudaStream_t stre
             return ragged ? launch_mode<kCommit, true, NL, true, true, true>(L, stream)
                           : launch_mode<kCommit, false, NL, true, true, true>(L, stream);
         }
+        if (layers[0].tc) {  // tcgen05 products (opt-in): one multi-chunk instantiation per mode
+            switch (mode) {
+                case kVerify:
+                    return ragged ? launch_mode<kVerify, true, NL, true, false, true, true>(L, stream)
+                                  : launch_mode<kVerify, false, NL, true, false, true, true>(L, stream);
+                case kCommit:
+                    return ragged ? launch_mode<kCommit, true, NL, true, false, true, true>(L, stream)
+                                  : launch_mode<kCommit, false, NL, true, false, true, true>(L, stream);
+                default:
+                    return ragged ? launch_mode<kFused, true, NL, true, false, true, true>(L, stream)
+                                  : launch_mode<kFused, false, NL, true, false, true, true>(L, stream);
+            }
+        }
         if (layers[0].flags != 0) {  // variants: one multi-chunk instantiation for any length
             switch (mode) {
                 case kVerify:
@@ -1085,7 +1469,7 @@ cudaError_t launch_layers(const Args *layers, int n, int mode, cudaStream_t stre
             }
         }
     } else {
-        if (layers[0].cap > 0 || layers[0].flags != 0) return cudaErrorNotSupported;
+        if (layers[0].cap > 0 || layers[0].flags != 0 || layers[0].tc) return cudaErrorNotSupported;
     }
     if (layers[0].max_T > CT) return dispatch<NL, true>(L, mode, ragged, stream);
     return dispatch<NL, false>(L, mode, ragged, stream);
@@ -1100,8 +1484,8 @@ bool chunk_supported(bool bf16, int dk, int dv, int max_T) {
 bool chunk_preferred(int max_T) { return max_T >= 1; }
 
 cudaError_t launch_chunk(const Args *layers, int n, int mode, cudaStream_t stream) {
-    if (n > 0 && (layers[0].flags != 0 || layers[0].cap > 0)) {
-        // Variants and replay buffers run one problem per launch.
+    if (n > 0 && (layers[0].flags != 0 || layers[0].cap > 0 || layers[0].tc)) {
+        // Variants, replay buffers and the tcgen05 kernel run one problem per launch.
         for (int l = 0; l < n; ++l) {
             const cudaError_t e = launch_layers<1>(layers + l, 1, mode, stream);
             if (e != cudaSuccess) return e;

@@ -28,6 +28,7 @@ struct Args {
     void *o;                  // NULL for commit; float, or bf16 with GDN_FLAG_O_BF16
     int32_t *dev_err;
     int flags = 0;            // GDN_FLAG_* bits
+    int tc = 0;               // chunk kernel: tcgen05 products (GDN_ALGO_CHUNK_TC)
     // ReplaySSM buffer (replay calls only; k, v, alpha, beta then point into
     // the buffer, whose rows are slot * cap + row).
     int cap = 0;              // rows per slot, 0 when there is no buffer

@@ -98,6 +98,7 @@ def call(lib, fn, c, o=O_PTR, acc=ACC_PTR):
     (dict(qkv_dtype=5), 3),
     (dict(dk=48), 4), (dict(dk=512), 4), (dict(dv=48), 4), (dict(dv=160), 4), (dict(algo=9), 4),
     (dict(algo=2, qkv_dtype=0), 4), (dict(algo=2, dk=64, dv=64), 4),
+    (dict(algo=3, qkv_dtype=0), 4), (dict(algo=3, dk=64, dv=64), 4), (dict(algo=4), 4),
     (dict(pool=None), 1), (dict(slot_ids=None), 1), (dict(q=None), 1), (dict(beta=None), 1),
     (dict(q=(1 << 40) + 8), 7), (dict(pool=(1 << 40) + 5 * (1 << 32) + 4), 7),
     (dict(alpha=(1 << 40) + 3 * (1 << 32) + 2), 7),

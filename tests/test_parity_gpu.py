@@ -20,7 +20,8 @@ from speculative_decode_gated_gb300 import binding, inputs, staging
 
 pytestmark = pytest.mark.gpu
 
-AUTO, REC, CHUNK = binding.GDN_ALGO_AUTO, binding.GDN_ALGO_RECURRENT, binding.GDN_ALGO_CHUNK
+AUTO, REC, CHUNK, TC = (binding.GDN_ALGO_AUTO, binding.GDN_ALGO_RECURRENT, binding.GDN_ALGO_CHUNK,
+                         binding.GDN_ALGO_CHUNK_TC)
 
 
 def custom(name, **kw):
@@ -91,10 +92,10 @@ def algo_applies(prob, algo):
 
 def _params():
     for name in SMALL:
-        for algo in (AUTO, REC, CHUNK):
+        for algo in (AUTO, REC, CHUNK, TC):
             for mode in ("verify", "commit", "fused"):
                 yield pytest.param(name, algo, mode,
-                                   id=f"{name}-{['auto', 'rec', 'chunk'][algo]}-{mode}")
+                                   id=f"{name}-{['auto', 'rec', 'chunk', 'tc'][algo]}-{mode}")
 
 
 @pytest.mark.parametrize("name,algo,mode", list(_params()))
@@ -118,13 +119,14 @@ FULL = ["b32_h32_d128_t16", "b64_h32_d128_t16_x24", "b128_h32_d128_ragged16"]
 
 @pytest.mark.parametrize("name", FULL)
 @pytest.mark.parametrize("mode", ["separate", "fused"])
-def test_full_size_sampled(name, mode):
+@pytest.mark.parametrize("algo", [AUTO, TC], ids=["auto", "tc"])
+def test_full_size_sampled(name, mode, algo):
     layers = [0, 23] if name.endswith("x24") else [0]
     for layer in layers:
         prob = inputs.make_problem(name, layer=layer)
         units = pick_units(prob, 40)
         o_ref, s_ref = oracle_units(prob, units)
-        d = staging.DeviceProblem(prob, "cuda")
+        d = staging.DeviceProblem(prob, "cuda", algo=algo)
         if mode == "separate":
             check_verify(d, units, o_ref)
             check_state_update(d, units, s_ref, d.commit)
