@@ -379,8 +379,8 @@ def run_ours(args, rank, world, local_rank):
     peak, peak_kind = measured_peaks()
     achieved = per_launch_bytes[dominant] / (avg_ms[dominant] * 1e-3) / 1e9
     algo_used = binding.gdn_select_algo(dps[0].c)
-    ktag = (("gdn_chunk" if algo_used == binding.GDN_ALGO_CHUNK else "gdn_recurrent")
-            + "_" + MODE_NAME[dominant])
+    ktag = ({binding.GDN_ALGO_CHUNK: "gdn_chunk", binding.GDN_ALGO_CHUNK_TC: "gdn_chunk_tc"}
+            .get(algo_used, "gdn_recurrent") + "_" + MODE_NAME[dominant])
     traffic = profile_traffic(ktag, name)
 
     e2e = (run_e2e(args, dps, stream, dev, fused)
@@ -415,7 +415,7 @@ def run_ours(args, rank, world, local_rank):
                           "verify then commit per layer" if args.order == "interleaved" else
                           "all verifies then all commits"),
                 "l2": "inputs larger than L2 (each step touches ~%.1f GB)" % (bytes_call * L / 1e9),
-                "algo": {1: "recurrent", 2: "chunk"}.get(algo_used, str(algo_used)),
+                "algo": {1: "recurrent", 2: "chunk", 3: "chunk_tc"}.get(algo_used, str(algo_used)),
                 "accepted": ("greedy prefix match of token ids on the device, every step"
                              if args.with_accept else "given (device array)"),
             },
@@ -501,7 +501,8 @@ def main():
     ap.add_argument("--mode", choices=["separate", "fused"], default=None,
                     help="separate verify + commit (default) or the fused call")
     ap.add_argument("--order", choices=["interleaved", "engine"], default="interleaved")
-    ap.add_argument("--algo", type=int, default=0, help="0 auto, 1 recurrent, 2 chunk")
+    ap.add_argument("--algo", type=int, default=0,
+                    help="0 auto, 1 recurrent, 2 chunk (mma.sync), 3 chunk (tcgen05)")
     ap.add_argument("--layers", type=int, default=0,
                     help="run only the first N layers (small cases for profiling; 0 = all)")
     ap.add_argument("--cpu-units", type=int, default=256)
