@@ -64,6 +64,13 @@ SMALL = {
                                   T=64, pool_slots=3, accept="full", seed=23),
     "b2_h2_d128_t200": custom("b2_h2_d128_t200", batch=2, heads=2, dk=128, dv=128, T=200,
                               pool_slots=2, seed=24),
+    # ragged batches with empty requests (no rows: nothing to verify, a_r = 0),
+    # in the middle and at the end
+    "ragged_empty_b6_d128": custom("ragged_empty_b6_d128", batch=6, heads=2, dk=128, dv=128,
+                                   lengths=[3, 0, 16, 0, 5, 0], pool_slots=8, seed=27),
+    # the longest draft the ABI accepts (64 chained chunks)
+    "b1_h1_d128_t1024": custom("b1_h1_d128_t1024", batch=1, heads=1, dk=128, dv=128, T=1024,
+                               pool_slots=2, accept="full", seed=28),
     # dk = 256 (recurrent kernel, four threads per value column)
     "b2_h2_dk256_dv64_t6": custom("b2_h2_dk256_dv64_t6", batch=2, heads=2, dk=256, dv=64, T=6,
                                   pool_slots=3, seed=25),
