@@ -15,10 +15,13 @@ section "Make speculative verification cheaper").
 
 The greedy accept-length rule lives in `accept.py` (pure Python loops); the
 ReplaySSM buffer (checkpoint plus buffered rows, periodic flush) in `replay.py`,
-which runs this recurrence over the replayed rows.
+which runs this recurrence over the replayed rows; the step that commits the
+previous step's accepted prefix and then verifies the next drafts in
+`lagged.py`.
 
-Parity unpinned: none.  Every function here is pinned by `tests/test_oracle_pins.py`
-and `tests/test_accept_oracle.py` and `tests/test_replay_oracle.py`.
+Parity unpinned: none.  Every function here is pinned by `tests/test_oracle_pins.py`,
+`tests/test_accept_oracle.py`, `tests/test_replay_oracle.py` and
+`tests/test_lagged_oracle.py`.
 """
 from __future__ import annotations
 
@@ -33,6 +36,7 @@ import numpy as np
 
 from .accept import accept_prefix  # noqa: F401  (greedy accept length)
 from .replay import replay_commit, replay_verify  # noqa: F401  (ReplaySSM buffer)
+from .lagged import commit_verify  # noqa: F401  (commit the previous step, verify the next)
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 _SRC = os.path.join(_HERE, "gdn_oracle.c")
