@@ -43,7 +43,7 @@ WORKLOAD = "b64_h32_d128_t16_x24"
 METRIC = "us per layer-call (verify+commit) and achieved HBM GB/s vs ~8 TB/s, 1xGB300"
 UNIT = "us/layer-call"
 NOMINAL_HBM_GBS = 8000.0
-MODE_NAME = {"v": "verify", "c": "commit", "f": "fused",
+MODE_NAME = {"v": "verify", "c": "commit", "f": "fused", "cv": "commit_verify",
              "C": "commit_layers", "F": "fused_layers",  # upper case: one launch, all layers
              "a": "accept", "rv": "replay_verify", "rc": "replay_commit"}
 
@@ -69,6 +69,13 @@ def alg_bytes(prob, mode: str) -> int:
         per_r = tile + lens * (2 * q_k + v_ + 8 + o_)
     elif mode == "commit":
         per_r = (acc > 0) * (2 * tile) + acc * (q_k + v_ + 8)
+    elif mode == "commit_verify":
+        # the previous step (here: the same problem one step earlier) commits its
+        # accepted rows from its cached W: k, alpha and W of a rows; this step
+        # verifies its drafts and caches their W (o-sized)
+        meta += prob.batch * 4 * (2 if prob.ragged else 1)
+        per_r = (tile + (acc > 0) * tile + acc * (q_k + 4 + o_)
+                 + lens * (2 * q_k + v_ + 8 + o_ + o_))
     else:
         per_r = tile + (acc > 0) * tile + lens * (2 * q_k + v_ + 8 + o_)
     return int(H * per_r.sum() + meta)
@@ -274,7 +281,7 @@ def run_ours(args, rank, world, local_rank):
         raise SystemExit("--batch-layers needs a multi-layer workload and --mode fused or "
                          "--order engine")
     stream = torch.cuda.current_stream(dev)
-    per_layer = {m: [alg_bytes(pr, MODE_NAME[m]) for pr in layers] for m in ("v", "c", "f")}
+    per_layer = {m: [alg_bytes(pr, MODE_NAME[m]) for pr in layers] for m in ("v", "c", "f", "cv")}
     # bytes_of[kind]: algorithmic bytes of each launch of that kind in one step
     bytes_of = dict(per_layer, C=[sum(per_layer["c"])], F=[sum(per_layer["f"])])
     replay_bufs = None
@@ -291,6 +298,20 @@ def run_ours(args, rank, world, local_rank):
         for d, r in zip(dps, reps):
             calls.append(("rv", staging.replay_launcher(d, r, "verify", stream)))
             calls.append(("rc", staging.replay_launcher(d, r, "commit", stream)))
+    elif args.order == "lagged":
+        if fused or batched:
+            raise SystemExit("--order lagged is one call per layer and step")
+        # Each layer's previous step is its own problem one step earlier (same
+        # requests, tokens and accepted lengths); the W cache alternates between
+        # two buffers, read by one step and written by the next.
+        kinds = ["cv"]
+        calls = []
+        for d in dps:
+            ws = [torch.zeros((d.host.n_tok, d.host.heads, d.host.dv), device=dev) for _ in range(2)]
+            prevs = [binding.make_prev_step(k=d.k, alpha=d.alpha, w=ws[j], accepted=d.accepted,
+                                            max_T=d.host.max_T, cu_seqlens=d.cu_seqlens)
+                     for j in range(2)]
+            calls.append(("cv", staging.commit_verify_launcher(d, prevs, ws, stream)))
     elif batched and fused:
         kinds = ["F"]
         calls = [("F", staging.layers_launcher(dps, "fused", stream))]
@@ -384,7 +405,7 @@ def run_ours(args, rank, world, local_rank):
     traffic = profile_traffic(ktag, name)
 
     e2e = (run_e2e(args, dps, stream, dev, fused)
-           if not (args.no_e2e or batched or args.replay) else None)
+           if not (args.no_e2e or batched or args.replay or args.order == "lagged") else None)
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline and not args.replay:
@@ -413,6 +434,8 @@ def run_ours(args, rank, world, local_rank):
                           "fused per layer" if fused else
                           "all verifies, then all layers' commits in one launch" if batched else
                           "verify then commit per layer" if args.order == "interleaved" else
+                          "per layer: commit the previous step, verify this one (one call)"
+                          if args.order == "lagged" else
                           "all verifies then all commits"),
                 "l2": "inputs larger than L2 (each step touches ~%.1f GB)" % (bytes_call * L / 1e9),
                 "algo": {1: "recurrent", 2: "chunk", 3: "chunk_tc"}.get(algo_used, str(algo_used)),
@@ -500,7 +523,7 @@ def main():
     ap.add_argument("--workload", default=WORKLOAD, choices=sorted(inputs.WORKLOADS))
     ap.add_argument("--mode", choices=["separate", "fused"], default=None,
                     help="separate verify + commit (default) or the fused call")
-    ap.add_argument("--order", choices=["interleaved", "engine"], default="interleaved")
+    ap.add_argument("--order", choices=["interleaved", "engine", "lagged"], default="interleaved")
     ap.add_argument("--algo", type=int, default=0,
                     help="0 auto, 1 recurrent, 2 chunk (mma.sync), 3 chunk (tcgen05)")
     ap.add_argument("--layers", type=int, default=0,

@@ -247,6 +247,45 @@ GDN_API gdn_status gdn_replay_commit(const gdn_problem *p, const gdn_replay *rb,
 
 /* Waits for `stream`, copies *p->dev_err to *host_code (0 when dev_err is NULL).
  * Returns GDN_ERR_DEVICE_ARG when the word is non-zero, GDN_OK when it is zero. */
+/* Commit the previous step, then verify the next one, in one pass over each
+ * checkpoint (OCRia write-up, section "Make speculative verification
+ * cheaper": rollback keeps the accepted prefix; in an engine the accepted
+ * lengths of a step are known only after all its layers have verified, so a
+ * layer's commit of step n - 1 can run at its verify of step n).
+ *
+ * For every request r and head h, with S the state in pool[slot_ids[r]][h]:
+ *   1. if prev->accepted[r] = a > 0: S <- the state after the first a rows of
+ *      the previous step replayed from S, written back to the slot (as
+ *      gdn_commit with that step's problem would);
+ *   2. o <- the outputs of this step's drafts from S (as gdn_verify would).
+ * The previous step's own W (a by-product of its call, written to its `w`) is
+ * what makes step 1 a single rank-a update: no products of the checkpoint.
+ *
+ *   p     this step: everything gdn_verify takes.  bf16 q/k/v, dk = dv = 128,
+ *         max_T <= 16 (GDN_ERR_UNSUPPORTED otherwise); AUTO or GDN_ALGO_CHUNK.
+ *   prev  the previous step of the same requests (same batch, heads, slot ids),
+ *         or NULL for the first step (nothing is committed).
+ *   o     as gdn_verify.
+ *   w     device float32 [N_tok][heads][dv], 16-byte aligned, written: this
+ *         step's W, for the next call's prev->w (the caller alternates two
+ *         buffers).  Must not overlap any other array of the call.
+ * Device errors: prev->accepted[r] outside [0, T_prev,r] sets
+ * GDN_DEVERR_ACCEPTED, bad previous row offsets GDN_DEVERR_SEQLEN; the unit is
+ * skipped (no write, no outputs). */
+typedef struct gdn_prev_step {
+    const int32_t *cu_seqlens;   /* device [batch+1] row offsets of the previous step, or NULL (uniform max_T) */
+    int32_t max_T;               /* its uniform length, or its ragged maximum; 0..16 */
+    int32_t reserved;            /* must be 0 */
+    int64_t n_tok;               /* rows of its arrays (ragged; ignored when cu_seqlens is NULL) */
+    const void *k;               /* device, its k [n_tok][heads][dk], 16-byte aligned */
+    const float *alpha;          /* device, its alpha (or g with GDN_FLAG_LOG_GATE) [n_tok][heads] */
+    const float *w;              /* device, the w its call wrote [n_tok][heads][dv], 16-byte aligned */
+    const int32_t *accepted;     /* device [batch]: its accepted lengths */
+} gdn_prev_step;
+
+GDN_API gdn_status gdn_commit_verify(const gdn_problem *p, const gdn_prev_step *prev, void *o,
+                                     float *w, cudaStream_t stream);
+
 GDN_API gdn_status gdn_read_device_error(const gdn_problem *p, cudaStream_t stream,
                                          int32_t *host_code);
 

@@ -30,7 +30,8 @@ GDN_MAX_T = 1024
 EXPORTED = (
     "gdn_verify", "gdn_commit", "gdn_verify_commit_fused",
     "gdn_verify_layers", "gdn_commit_layers", "gdn_verify_commit_fused_layers",
-    "gdn_accept_prefix", "gdn_replay_verify", "gdn_replay_commit", "gdn_read_device_error",
+    "gdn_accept_prefix", "gdn_replay_verify", "gdn_replay_commit", "gdn_commit_verify",
+    "gdn_read_device_error",
     "gdn_select_algo", "gdn_status_string", "gdn_last_error_string", "gdn_version",
 )
 
@@ -68,6 +69,16 @@ class gdn_replay(ctypes.Structure):
     ]
 
 
+class gdn_prev_step(ctypes.Structure):
+    """Mirror of the C struct gdn_prev_step (include/gdn.h), field for field."""
+
+    _fields_ = [
+        ("cu_seqlens", ctypes.c_void_p), ("max_T", ctypes.c_int32), ("reserved", ctypes.c_int32),
+        ("n_tok", ctypes.c_int64), ("k", ctypes.c_void_p), ("alpha", ctypes.c_void_p),
+        ("w", ctypes.c_void_p), ("accepted", ctypes.c_void_p),
+    ]
+
+
 _lib_handle: Optional[ctypes.CDLL] = None
 
 
@@ -92,13 +103,14 @@ def lib() -> ctypes.CDLL:
         R = ctypes.POINTER(gdn_replay)
         h.gdn_replay_verify.argtypes = [P, R, S, S]
         h.gdn_replay_commit.argtypes = [P, R, S, S]
+        h.gdn_commit_verify.argtypes = [P, ctypes.POINTER(gdn_prev_step), S, S, S]
         h.gdn_read_device_error.argtypes = [P, S, ctypes.POINTER(ctypes.c_int32)]
         h.gdn_select_algo.argtypes = [P]
         h.gdn_status_string.argtypes = [ctypes.c_int]
         for name in ("gdn_verify", "gdn_commit", "gdn_verify_commit_fused",
                      "gdn_verify_layers", "gdn_commit_layers", "gdn_verify_commit_fused_layers",
                      "gdn_accept_prefix", "gdn_replay_verify", "gdn_replay_commit",
-                     "gdn_read_device_error", "gdn_select_algo"):
+                     "gdn_commit_verify", "gdn_read_device_error", "gdn_select_algo"):
             getattr(h, name).restype = ctypes.c_int
         for name in ("gdn_status_string", "gdn_last_error_string", "gdn_version"):
             getattr(h, name).restype = ctypes.c_char_p
@@ -340,3 +352,44 @@ def gdn_last_error_string() -> str:
 
 def gdn_version() -> str:
     return lib().gdn_version().decode()
+
+
+class PrevStep:
+    """A gdn_prev_step plus references to the tensors it points into."""
+
+    def __init__(self, c: gdn_prev_step, refs: tuple):
+        self.c = c
+        self.refs = refs
+
+    @property
+    def ref(self):
+        return ctypes.byref(self.c)
+
+
+def make_prev_step(*, k: torch.Tensor, alpha: torch.Tensor, w: torch.Tensor,
+                   accepted: torch.Tensor, max_T: int,
+                   cu_seqlens: Optional[torch.Tensor] = None) -> PrevStep:
+    """The previous step of the same requests: its k [N_tok, H, dk], alpha [N_tok, H],
+    the w its gdn_commit_verify wrote [N_tok, H, dv] fp32, its accepted [B] int32,
+    and its row offsets [B+1] int32 or None (uniform length max_T)."""
+    dev = k.device
+    _check(k, "k", (torch.bfloat16, torch.float32), dev)
+    _check(alpha, "alpha", (torch.float32,), dev)
+    _check(w, "w", (torch.float32,), dev)
+    _check(accepted, "accepted", (torch.int32,), dev)
+    _check(cu_seqlens, "cu_seqlens", (torch.int32,), dev)
+    c = gdn_prev_step()
+    c.cu_seqlens = _ptr(cu_seqlens)
+    c.max_T, c.reserved = int(max_T), 0
+    c.n_tok = k.shape[0]
+    c.k, c.alpha, c.w, c.accepted = _ptr(k), _ptr(alpha), _ptr(w), _ptr(accepted)
+    return PrevStep(c, (k, alpha, w, accepted, cu_seqlens))
+
+
+def gdn_commit_verify(prob: Problem, prev: Optional[PrevStep], o: torch.Tensor, w: torch.Tensor,
+                      stream=None) -> None:
+    """Commit `prev` (None: nothing), then verify `prob`; w: this step's W [N_tok, H, dv] fp32."""
+    _check(o, "o", (_o_dtype(prob),), None)
+    _check(w, "w", (torch.float32,), None)
+    _raise(lib().gdn_commit_verify(prob.ref, None if prev is None else prev.ref, _ptr(o), _ptr(w),
+                                   _stream(stream)), "gdn_commit_verify")

@@ -294,9 +294,79 @@ gdn_status run_replay(const gdn_problem *p, const gdn_replay *rb, int mode,
     return GDN_OK;
 }
 
+
+// Commit-then-verify: `p` is this step (verify part), `prev` the previous step
+// of the same requests (NULL: nothing to commit), `w` this call's W output.
+gdn_status run_commit_verify(const gdn_problem *p, const gdn_prev_step *prev, void *o, float *w,
+                             cudaStream_t stream) {
+    int algo = 0;
+    bool empty = false;
+    gdn_status st = validate(p, true, o, false, nullptr, &algo, &empty);
+    if (st != GDN_OK) return st;
+    if (prev && prev->reserved != 0) return GDN_ERR_BAD_DIM;
+    if (prev && (prev->max_T < 0 || (prev->cu_seqlens && prev->n_tok < 0))) return GDN_ERR_BAD_DIM;
+    if (empty) return GDN_OK;
+    // Single 16-token chunks on the mma.sync chunk kernel only.
+    if (algo != GDN_ALGO_CHUNK || p->max_T > 16 || (prev && prev->max_T > 16))
+        return GDN_ERR_UNSUPPORTED;
+    if (!w) return GDN_ERR_NULL_PTR;
+    if (!aligned16(w)) return GDN_ERR_ALIGN;
+    const int64_t H = p->heads, n_tok = token_rows(p);
+    const int64_t prows = prev ? (prev->cu_seqlens ? prev->n_tok : (int64_t)p->batch * prev->max_T) : 0;
+    if (prev && prows > 0) {
+        if (!prev->k || !prev->alpha || !prev->w || !prev->accepted) return GDN_ERR_NULL_PTR;
+        if (!aligned16(prev->k) || !aligned16(prev->w) || !aligned4(prev->alpha) ||
+            !aligned4(prev->accepted) || !aligned4(prev->cu_seqlens))
+            return GDN_ERR_ALIGN;
+    }
+    // Aliasing: w is written, so it must not overlap anything else of the call;
+    // the pool (written by the commit) must not overlap the previous step's arrays.
+    const LayerRanges lr = layer_ranges(p);
+    const Range rw = range(w, n_tok * H * p->dv * 4);
+    const Range rp = lr.pool, ro = o_range(p, o);
+    const Range pk = range(prev ? prev->k : nullptr, prows * H * p->dk * (p->qkv_dtype == GDN_BF16 ? 2 : 4));
+    const Range pa = range(prev ? prev->alpha : nullptr, prows * H * 4);
+    const Range pw = range(prev ? prev->w : nullptr, prows * H * p->dv * 4);
+    const Range pacc = range(prev ? prev->accepted : nullptr, prev && prows > 0 ? (int64_t)p->batch * 4 : 0);
+    const Range pcu = range(prev ? prev->cu_seqlens : nullptr,
+                            prev && prev->cu_seqlens ? ((int64_t)p->batch + 1) * 4 : 0);
+    const Range rs = range(p->slot_ids, (int64_t)p->batch * 4);
+    const Range rc = range(p->cu_seqlens, p->cu_seqlens ? ((int64_t)p->batch + 1) * 4 : 0);
+    const Range re = range(p->dev_err, p->dev_err ? 4 : 0);
+    const Range all_w[] = {lr.q, lr.k, lr.v, lr.alpha, lr.beta, rp, ro, pk, pa, pw, pacc, pcu, rs, rc, re};
+    for (const Range &x : all_w)
+        if (overlap(rw, x)) return GDN_ERR_ALIAS;
+    const Range prev_in[] = {pk, pa, pw, pacc, pcu};
+    for (const Range &x : prev_in)
+        if (overlap(rp, x) || overlap(ro, x)) return GDN_ERR_ALIAS;
+
+    gdn::Args a = make_args(p, nullptr, o);
+    a.w_out = w;
+    if (prev && prows > 0) {
+        a.p_cu = prev->cu_seqlens;
+        a.p_maxT = prev->max_T;
+        a.p_ntok = prows;
+        a.p_k = prev->k;
+        a.p_alpha = prev->alpha;
+        a.p_w = prev->w;
+        a.p_acc = prev->accepted;
+    }
+    const cudaError_t e = gdn::launch_chunk(&a, 1, gdn::kLagged, stream);
+    if (e != cudaSuccess) {
+        set_cuda_error(e, "kernel launch");
+        return GDN_ERR_CUDA;
+    }
+    return GDN_OK;
+}
+
 }  // namespace
 
 extern "C" {
+
+gdn_status gdn_commit_verify(const gdn_problem *p, const gdn_prev_step *prev, void *o, float *w,
+                             cudaStream_t stream) {
+    return run_commit_verify(p, prev, o, w, stream);
+}
 
 gdn_status gdn_verify(const gdn_problem *p, void *o, cudaStream_t stream) {
     return run(p, gdn::kVerify, nullptr, o, stream);

@@ -77,6 +77,7 @@ constexpr uint32_t kQKStride = 2 * kTokHalfBytes;  // q/k: bytes from one column
 struct TokBuf {
     unsigned char qk[2][2][kTokHalfBytes];  // [column half][0: q, 1: k]
     unsigned char v[kTokBytes];             // halves kTokHalfBytes apart
+    unsigned char kp[kTokBytes];            // commit-then-verify: the previous step's k rows
     __device__ unsigned char *q() { return qk[0][0]; }
     __device__ unsigned char *k() { return qk[0][1]; }
     __device__ const unsigned char *q() const { return qk[0][0]; }
@@ -91,6 +92,10 @@ struct Aux {
     float alpha[CT], beta[CT], gamma[CT];
     float dcol[CT];         // D[a'-1][s] for s < a' (a' = the commit point within the chunk), else 0
     float dlast[CT];        // D[15][s]: the whole chunk's decay to its end
+    // Commit-then-verify: the previous step's gates and its commit weights.
+    float palpha[CT];       // alpha of its rows t < a_prev (1 beyond)
+    float pdcol[CT];        // prod_{s<r<a_prev} alpha_r for s < a_prev, else 0
+    float pgam;             // prod_{r<a_prev} alpha_r
     unsigned long long tile_full, tok_full[2];
     unsigned long long mma_full;  // tcgen05 products completed
     uint32_t tmem_base;           // TMEM address of this block's columns
@@ -333,11 +338,14 @@ struct UnitPlan {
     int nskip = 0;  // rows before this one have no output (replay: the buffered rows)
     int slot = 0;
     int n = 0;      // replay: rows buffered in the slot (loaded with the plan)
+    int prow0 = 0;  // commit-then-verify: the previous step's first row of the request
+    int pa = 0;     // and its accepted length (0: nothing to commit)
     bool skip = true;
 };
 
 struct Maps {
     CUtensorMap pool, q, k, v;
+    CUtensorMap kp;  // commit-then-verify: the previous step's k
 };
 
 // One launch: NL problems that share every request-level field (batch, heads,
@@ -366,7 +374,17 @@ __device__ __forceinline__ RawMeta load_unit_meta(const Args &p, int w, int W, i
         m.cu1 = m.cu0 + p.max_T;
     }
     m.slot = ld_early(p.slot_ids + r);
-    m.acc = MODE != kVerify ? ld_early(p.accepted + r) : -1;
+    m.acc = (MODE == kCommit || MODE == kFused) ? ld_early(p.accepted + r) : -1;
+    if (MODE == kLagged) {
+        if (p.p_cu) {
+            m.pcu0 = ld_early(p.p_cu + r);
+            m.pcu1 = ld_early(p.p_cu + r + 1);
+        } else {
+            m.pcu0 = r * p.p_maxT;
+            m.pcu1 = m.pcu0 + p.p_maxT;
+        }
+        m.pacc = p.p_acc ? ld_early(p.p_acc + r) : 0;
+    }
     return m;
 }
 
@@ -377,7 +395,22 @@ __device__ __forceinline__ UnitPlan plan_unit(const Launch<NL> &L, int w, int U,
     const int unit = w - pl.layer * U;
     const Args &p = L.a[pl.layer];
     pl.h = unit - (unit / p.H) * p.H;
-    const bool ok = check_meta(p, m, pl.h, MODE, pl.u);
+    bool ok = check_meta(p, m, pl.h, MODE == kLagged ? kVerify : MODE, pl.u);
+    if (MODE == kLagged && ok && p.p_acc) {
+        // The previous step: its rows must lie in its arrays, a_prev in [0, T_prev].
+        const int pT = m.pcu1 - m.pcu0;
+        int err = 0;
+        if (p.p_cu && (pT < 0 || pT > p.p_maxT || m.pcu0 < 0 || (long long)m.pcu1 > p.p_ntok))
+            err |= GDN_DEVERR_SEQLEN;
+        else if (m.pacc < 0 || m.pacc > pT)
+            err |= GDN_DEVERR_ACCEPTED;
+        if (err) {
+            if (threadIdx.x == 0 && p.dev_err) atomicOr(p.dev_err, err);
+            ok = false;
+        }
+        pl.prow0 = m.pcu0;
+        pl.pa = ok ? m.pacc : 0;
+    }
     pl.tile = ok ? m.slot * p.H + pl.h : 0;
     pl.slot = ok ? m.slot : 0;
     pl.qrow0 = pl.u.row0;
@@ -390,7 +423,8 @@ __device__ __forceinline__ UnitPlan plan_unit(const Launch<NL> &L, int w, int U,
         return pl;
     }
     pl.teff = ok ? ((MODE == kCommit) ? pl.u.a : pl.u.T) : 0;
-    pl.skip = !ok || pl.teff == 0;
+    // Commit-then-verify: a request with no new rows may still have a prefix to commit.
+    pl.skip = !ok || (pl.teff == 0 && (MODE != kLagged || pl.pa == 0));
     return pl;
 }
 
@@ -430,7 +464,12 @@ __device__ __forceinline__ void issue_tokens(const Maps &maps, const UnitPlan &p
                                              TokBuf &tb, uint32_t tok_bar) {
     const int row = pl.u.row0 + CT * ch;
     const int qrow = pl.qrow0 + CT * ch;  // may be negative (replay): those rows read as zero
-    mbar_arrive_expect_tx(tok_bar, (MODE == kCommit ? 2u : 3u) * kTokBytes);
+    const bool prev = MODE == kLagged && pl.pa > 0;  // the previous step's k rows too
+    mbar_arrive_expect_tx(tok_bar, (MODE == kCommit ? 2u : 3u) * kTokBytes + (prev ? kTokBytes : 0u));
+    if (prev)
+#pragma unroll
+        for (int hb = 0; hb < 2; ++hb)
+            tma_load_3d(smem_u32(tb.kp) + hb * kTokHalfBytes, &maps.kp, 64 * hb, pl.h, pl.prow0, tok_bar);
 #pragma unroll
     for (int hb = 0; hb < 2; ++hb) {
         tma_load_3d(smem_u32(tb.qk[hb][1]), &maps.k, 64 * hb, pl.h, row, tok_bar);
@@ -522,6 +561,22 @@ __device__ __forceinline__ float gate_load(const float *gate, const Args &p, con
     return ld_early(gate + (size_t)row * p.H + h);
 }
 
+// Commit-then-verify: the previous step's gate of its row min(tid, a_prev - 1)
+// (1 when there is nothing to commit).
+template <int MODE>
+__device__ __forceinline__ float prev_gate_load(const Args &p, const UnitPlan &pl, int tid) {
+    if (MODE != kLagged || pl.pa <= 0 || pl.skip) return 1.0f;
+    long long row = (long long)pl.prow0 + (tid < pl.pa ? tid : pl.pa - 1);
+    row = row < 0 ? 0 : (row >= p.p_ntok ? p.p_ntok - 1 : row);
+    return ld_early(p.p_alpha + (size_t)row * p.H + pl.h);
+}
+
+__device__ __forceinline__ float2 ld_early2(const float *ptr) {
+    float2 v;
+    asm volatile("ld.global.nc.v2.f32 {%0, %1}, [%2];" : "=f"(v.x), "=f"(v.y) : "l"(ptr));
+    return v;
+}
+
 // ------------------------------------------------------------ the kernel
 
 // Four warps share one unit: warp w owns the 32 value columns [32w, 32w + 32),
@@ -557,11 +612,12 @@ __device__ __forceinline__ int key_row(int kb, int c, int rr) {
 // 16 key rows at a time; the accumulators start from the state in `hr` (the
 // A-fragment layout of H^T is also the accumulator layout of this product).
 // STORE: the result goes to `dst` (this thread's columns of the pool tile,
-// 16-byte stores); else it replaces `hr`.
-template <bool STORE>
+// 16-byte stores); KEEP: it replaces `hr`.  `khalf`: bytes from one column
+// half of the k tile to the next.
+template <bool STORE, bool KEEP>
 __device__ __forceinline__ void state_update(float (&hr)[8][4][CPT], const float (&wq)[MT][2][4],
                                              const float *dvec, float gam, uint32_t k_smem,
-                                             int lane, int c, float *dst) {
+                                             uint32_t khalf, int lane, int c, float *dst) {
     uint32_t ah[MT][4], al[MT][4];
 #pragma unroll
     for (int ntt = 0; ntt < 2; ++ntt) {
@@ -583,7 +639,7 @@ __device__ __forceinline__ void state_update(float (&hr)[8][4][CPT], const float
 #pragma unroll
             for (int e = 0; e < CPT; ++e) hv[rr][e] = gam * hr[kb][rr][e];
         uint32_t b00, b01, b10, b11;  // (n-tile 2kb: b0, b1), (n-tile 2kb+1: b0, b1)
-        ldsm_x4_trans(b00, b01, b10, b11, k_smem + tok_off(krow, 16 * kb + 8 * (mi >> 1), kQKStride));
+        ldsm_x4_trans(b00, b01, b10, b11, k_smem + tok_off(krow, 16 * kb + 8 * (mi >> 1), khalf));
 #pragma unroll
         for (int m = 0; m < MT; ++m) {
             mma(hv[0][2 * m], hv[1][2 * m], hv[0][2 * m + 1], hv[1][2 * m + 1], ah[m][0], ah[m][1],
@@ -600,13 +656,12 @@ __device__ __forceinline__ void state_update(float (&hr)[8][4][CPT], const float
         }
 #pragma unroll
         for (int rr = 0; rr < 4; ++rr) {
-            if (STORE) {
+            if (STORE)
                 *reinterpret_cast<float4 *>(dst + key_row(kb, c, rr) * D) =
                     make_float4(hv[rr][0], hv[rr][1], hv[rr][2], hv[rr][3]);
-            } else {
+            if (KEEP)
 #pragma unroll
                 for (int e = 0; e < CPT; ++e) hr[kb][rr][e] = hv[rr][e];
-            }
         }
     }
 }
@@ -740,6 +795,29 @@ __global__ void __launch_bounds__(kThreads, kBlocksPerSM)
             if (tid == kPrefIssuer && !nxt.skip) prefetch_unit<MODE>(L.maps[nxt.layer], nxt);
             continue;
         }
+        // Commit-then-verify: the previous step's gate (thread t < 16: row t) and the
+        // W its call cached for this thread's columns and rows t < a_prev (0 beyond),
+        // in the accumulator layout of the W product (token 8 ntt + 2c + (e & 1),
+        // column col0 + 2m + (e >> 1)); consumed after the tile wait.
+        float gpa = 1.0f;
+        float wp[MODE == kLagged ? MT : 1][2][4];
+        if constexpr (MODE == kLagged) {
+            const Args &pa = L.a[me.layer];
+            gpa = prev_gate_load<MODE>(pa, me, tid);
+#pragma unroll
+            for (int m = 0; m < MT; ++m)
+#pragma unroll
+                for (int ntt = 0; ntt < 2; ++ntt)
+#pragma unroll
+                    for (int eo = 0; eo < 2; ++eo) {
+                        const int t = 8 * ntt + 2 * c + eo;
+                        float2 x = make_float2(0.0f, 0.0f);
+                        if (t < me.pa)
+                            x = ld_early2(pa.p_w + ((size_t)(me.prow0 + t) * pa.H + me.h) * D + col0 + 2 * m);
+                        wp[m][ntt][eo] = x.x;
+                        wp[m][ntt][2 + eo] = x.y;
+                    }
+        }
         const int Tu = me.teff;  // tokens of the unit that matter: T_r, or a_r for commit
         const int nch = MULTI ? (Tu + CT - 1) / CT : 1;
         // The commit point: chunk `ca` holds token a_r - 1.
@@ -769,6 +847,8 @@ __global__ void __launch_bounds__(kThreads, kBlocksPerSM)
                 const float at = (flags & GDN_FLAG_LOG_GATE) ? expf(ga) : ga;
                 ax.alpha[tid] = tid < T ? at : 1.0f;
                 ax.beta[tid] = tid < T ? gb : 0.0f;
+                if (MODE == kLagged)
+                    ax.palpha[tid] = tid < me.pa ? ((flags & GDN_FLAG_LOG_GATE) ? expf(gpa) : gpa) : 1.0f;
             }
             // Gates of the next step, loaded straight into the registers just
             // freed (consumed one step later, so this load is never waited on here).
@@ -836,6 +916,18 @@ __global__ void __launch_bounds__(kThreads, kBlocksPerSM)
                     if (MODE != kVerify && t == tc) ax.dcol[s] = (s <= t) ? d : 0.0f;
                     if (MULTI && t == CT - 1) ax.dlast[s] = d;
                 }
+                if (MODE == kLagged && tid <= CT) {
+                    // The previous step's commit weights: pdcol[s] = prod_{s<r<a_prev} alpha_r
+                    // (thread s < 16), pgam = prod_{r<a_prev} alpha_r (thread 16).
+                    const int lo = tid < CT ? tid + 1 : 0;  // first factor's row
+                    float d = 1.0f;
+#pragma unroll
+                    for (int r = 0; r < CT; ++r) d *= (r >= lo && r < me.pa) ? ax.palpha[r] : 1.0f;
+                    if (tid < CT)
+                        ax.pdcol[tid] = tid < me.pa ? d : 0.0f;
+                    else
+                        ax.pgam = d;
+                }
             }
             __syncthreads();
 
@@ -849,6 +941,24 @@ __global__ void __launch_bounds__(kThreads, kBlocksPerSM)
                 }
             }
 
+            // 4b. Commit-then-verify: the checkpoint into registers, then the previous
+            //     step's accepted prefix on top of it (its W cached by its call), written
+            //     to the slot; this step's drafts are verified from that state.
+            if constexpr (MODE == kLagged) {
+#pragma unroll
+                for (int kb = 0; kb < 8; ++kb)
+#pragma unroll
+                    for (int rr = 0; rr < 4; ++rr) {
+                        const float4 x = ld_tile_row(sm.tile, warp, g, key_row(kb, c, rr));
+                        hr[kb][rr][0] = x.x;
+                        hr[kb][rr][1] = x.y;
+                        hr[kb][rr][2] = x.z;
+                        hr[kb][rr][3] = x.w;
+                    }
+                if (me.pa > 0)
+                    state_update<true, true>(hr, wp, ax.pdcol, ax.pgam, smem_u32(tb.kp), kTokHalfBytes,
+                                             lane, c, opaque(me.u.tile) + col0);
+            }
             if constexpr (TC) {
                 // 5. The state at the chunk's start as A = H^T in TMEM, bf16 hi and
                 //    lo (thread t of warp w holds value column j = 32w + t: TMEM lane j,
@@ -1109,7 +1219,7 @@ __global__ void __launch_bounds__(kThreads, kBlocksPerSM)
                     if (lane < kTinvLanes) ax.Tinv[t][tj] = acc;
                 }
                 float hv[4][CPT];
-                if (!MULTI || ch == 0) {
+                if ((!MULTI || ch == 0) && MODE != kLagged) {
 #pragma unroll
                     for (int rr = 0; rr < 4; ++rr) {
                         const float4 x = ld_tile_row(sm.tile, warp, g, key_row(kb, c, rr));
@@ -1218,6 +1328,23 @@ __global__ void __launch_bounds__(kThreads, kBlocksPerSM)
                 }
             }
 
+            // 7b. Commit-then-verify: W of this step's drafts, cached for the next call's
+            //     commit (same layout as o: [row][head][column], rows t < T only).
+            if constexpr (MODE == kLagged) {
+                float *gw = L.a[me.layer].w_out + me.h * D + col0;
+#pragma unroll
+                for (int m = 0; m < MT; ++m)
+#pragma unroll
+                    for (int ntt = 0; ntt < 2; ++ntt)
+#pragma unroll
+                        for (int eo = 0; eo < 2; ++eo) {
+                            const int t = 8 * ntt + 2 * c + eo;
+                            if (t < T)
+                                *reinterpret_cast<float2 *>(gw + (size_t)(me.u.row0 + t) * row_stride + 2 * m) =
+                                    make_float2(wq[m][ntt][eo], wq[m][ntt][2 + eo]);
+                        }
+            }
+
             // 8. O^T = P^T diag(gamma) + W^T M^T, stored as float2 pairs of adjacent columns.
             if (MODE != kCommit && outs) {
                 uint32_t bh[2][2], bl[2][2];
@@ -1275,11 +1402,12 @@ __global__ void __launch_bounds__(kThreads, kBlocksPerSM)
             const bool commit_here = MODE == kCommit ? !more : (MODE == kFused && ch == ca);
             if constexpr (kKeep) {
                 if (commit_here)
-                    state_update<true>(hr, wq, ax.dcol, ax.gamma[me.u.a - CT * ch - 1],
-                                       smem_u32(tb.k()), lane, c, opaque(me.u.tile) + col0);
+                    state_update<true, false>(hr, wq, ax.dcol, ax.gamma[me.u.a - CT * ch - 1],
+                                              smem_u32(tb.k()), kQKStride, lane, c,
+                                              opaque(me.u.tile) + col0);
                 if (more)
-                    state_update<false>(hr, wq, ax.dlast, ax.gamma[CT - 1], smem_u32(tb.k()), lane,
-                                        c, nullptr);
+                    state_update<false, true>(hr, wq, ax.dlast, ax.gamma[CT - 1], smem_u32(tb.k()),
+                                              kQKStride, lane, c, nullptr);
             }
             ++steps;
         }
@@ -1338,7 +1466,7 @@ constexpr int kMaxDevices = 64;
 
 struct DeviceInfo {
     int sms = 0;
-    bool smem_set[3][2][2][2][2][2][2] = {};  // [mode][ragged][batched][multi][replay][var][tc]
+    bool smem_set[4][2][2][2][2][2][2] = {};  // [mode][ragged][batched][multi][replay][var][tc]
 };
 
 DeviceInfo g_dev[kMaxDevices];
@@ -1406,6 +1534,8 @@ cudaError_t encode_layer(const Args &p, Maps *maps) {
         !encode_tokens(encode, &maps->v, p.v, p.H, p.kv_rows) ||
         !encode_tokens(encode, &maps->q, p.q, p.H, p.n_tok))
         return cudaErrorInvalidValue;
+    if (p.p_k && !encode_tokens(encode, &maps->kp, p.p_k, p.H, p.p_ntok))  // the previous step's k
+        return cudaErrorInvalidValue;
     return cudaSuccess;
 }
 
@@ -1435,6 +1565,15 @@ cudaError_t launch_layers(const Args *layers, int n, int mode, cudaStream_t stre
     }
     const bool ragged = layers[0].cu_seqlens != nullptr;
     if constexpr (NL == 1) {
+        if (mode == kLagged) {  // commit-then-verify: single chunks, mma.sync products
+            if (layers[0].max_T > CT || layers[0].p_maxT > CT || layers[0].tc || layers[0].cap > 0)
+                return cudaErrorNotSupported;
+            if (layers[0].flags != 0)
+                return ragged ? launch_mode<kLagged, true, NL, false, false, true>(L, stream)
+                              : launch_mode<kLagged, false, NL, false, false, true>(L, stream);
+            return ragged ? launch_mode<kLagged, true, NL, false>(L, stream)
+                          : launch_mode<kLagged, false, NL, false>(L, stream);
+        }
         if (layers[0].cap > 0) {  // replay buffer (single problems): verify or commit
             if (mode == kVerify)
                 return ragged ? launch_mode<kVerify, true, NL, true, true, true>(L, stream)
@@ -1469,7 +1608,8 @@ cudaError_t launch_layers(const Args *layers, int n, int mode, cudaStream_t stre
             }
         }
     } else {
-        if (layers[0].cap > 0 || layers[0].flags != 0 || layers[0].tc) return cudaErrorNotSupported;
+        if (layers[0].cap > 0 || layers[0].flags != 0 || layers[0].tc || mode == kLagged)
+            return cudaErrorNotSupported;
     }
     if (layers[0].max_T > CT) return dispatch<NL, true>(L, mode, ragged, stream);
     return dispatch<NL, false>(L, mode, ragged, stream);
@@ -1484,8 +1624,9 @@ bool chunk_supported(bool bf16, int dk, int dv, int max_T) {
 bool chunk_preferred(int max_T) { return max_T >= 1; }
 
 cudaError_t launch_chunk(const Args *layers, int n, int mode, cudaStream_t stream) {
-    if (n > 0 && (layers[0].flags != 0 || layers[0].cap > 0 || layers[0].tc)) {
-        // Variants, replay buffers and the tcgen05 kernel run one problem per launch.
+    if (n > 0 && (layers[0].flags != 0 || layers[0].cap > 0 || layers[0].tc || mode == kLagged)) {
+        // Variants, replay buffers, commit-then-verify and the tcgen05 kernel run one
+        // problem per launch.
         for (int l = 0; l < n; ++l) {
             const cudaError_t e = launch_layers<1>(layers + l, 1, mode, stream);
             if (e != cudaSuccess) return e;

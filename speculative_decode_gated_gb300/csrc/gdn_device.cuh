@@ -12,7 +12,9 @@
 
 namespace gdn {
 
-enum Mode : int { kVerify = 0, kCommit = 1, kFused = 2 };
+// kLagged: commit the previous step's accepted prefix (from the W its call
+// cached), then verify this step's drafts from the committed state.
+enum Mode : int { kVerify = 0, kCommit = 1, kFused = 2, kLagged = 3 };
 
 // Everything a kernel needs; a plain copy of gdn_problem plus the call's outputs.
 struct Args {
@@ -35,6 +37,15 @@ struct Args {
     long long kv_rows = 0;    // rows of k, v, alpha, beta: n_tok, or pool_slots * cap
     const int32_t *len_in = nullptr;
     int32_t *len_out = nullptr;
+    // Commit-then-verify calls (kLagged): the previous step of the same requests.
+    const int32_t *p_cu = nullptr;   // its row offsets [B+1], or NULL (uniform p_maxT rows)
+    int p_maxT = 0;
+    long long p_ntok = 0;            // rows of its arrays
+    const void *p_k = nullptr;       // its k [p_ntok][H][dk]
+    const float *p_alpha = nullptr;  // its alpha (or g) [p_ntok][H]
+    const float *p_w = nullptr;      // the W its call wrote [p_ntok][H][dv]
+    const int32_t *p_acc = nullptr;  // its accepted lengths [B]
+    float *w_out = nullptr;          // this call's W [n_tok][H][dv]
 };
 
 // Token range, accepted length and state tile of one (request r, head h).
@@ -51,6 +62,8 @@ struct RawMeta {
     int cu0, cu1;  // token rows [cu0, cu1)
     int slot;
     int acc;       // accepted length, -1 in verify
+    // Commit-then-verify calls: the previous step's rows [pcu0, pcu1) and accepted length.
+    int pcu0 = 0, pcu1 = 0, pacc = 0;
 };
 
 // Read-only loads that stay where they are written: issued early on purpose,

@@ -206,3 +206,23 @@ def replay_launcher(d: DeviceProblem, r: DeviceReplay, mode: str, stream):
         if st != binding.GDN_OK:
             raise binding.GdnError(st, f"gdn replay {mode}")
     return call
+
+
+def commit_verify_launcher(d: DeviceProblem, prevs, ws, stream):
+    """A zero-argument callable issuing gdn_commit_verify for `d` on `stream`,
+    alternating between two previous-step descriptors (prevs[j] reads ws[j]) and
+    writing the other W buffer: call n reads ws[n % 2] and writes ws[1 - n % 2]."""
+    lib = binding.lib()
+    ref = d.c.ref
+    s = binding._stream(stream)
+    o = d.o.data_ptr()
+    args = [(prevs[j].ref, ws[1 - j].data_ptr()) for j in range(2)]
+    state = {"n": 0}
+
+    def call():
+        pref, w = args[state["n"] & 1]
+        state["n"] += 1
+        st = lib.gdn_commit_verify(ref, pref, o, w, s)
+        if st != binding.GDN_OK:
+            raise binding.GdnError(st, "gdn_commit_verify")
+    return call

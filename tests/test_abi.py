@@ -41,7 +41,8 @@ def test_library_exports_every_declared_symbol(lib):
 
 
 @pytest.mark.parametrize("cls,cname", [(binding.gdn_problem, "gdn_problem"),
-                                       (binding.gdn_replay, "gdn_replay")])
+                                       (binding.gdn_replay, "gdn_replay"),
+                                       (binding.gdn_prev_step, "gdn_prev_step")])
 def test_struct_layout_matches_c(tmp_path, cls, cname):
     fields = [f[0] for f in cls._fields_]
     prog = tmp_path / "layout.c"
@@ -279,3 +280,49 @@ def test_replay_commit_output_checks(lib):
     assert call_replay(lib, "commit", rb=fake_replay(len_out=None)) == 1
     assert call_replay(lib, "commit", rb=fake_replay(len_out=fake_replay().len_in)) == 8
     assert call_replay(lib, "commit", rb=fake_replay(len_out=fake_problem().slot_ids)) == 8
+
+
+# ---------------------------------------------------------------- commit then verify
+
+W_PTR = (1 << 40) + 11 * (1 << 32)
+
+
+def fake_prev(**over):
+    pv = binding.gdn_prev_step()
+    base = (1 << 40) + 30 * (1 << 32)
+    step = 1 << 32
+    pv.cu_seqlens, pv.max_T, pv.reserved, pv.n_tok = None, 8, 0, 16
+    pv.k, pv.alpha, pv.w, pv.accepted = base, base + step, base + 2 * step, base + 3 * step
+    for k, v in over.items():
+        setattr(pv, k, v)
+    return pv
+
+
+def call_cv(lib, c=None, prev=None, o=O_PTR, w=W_PTR):
+    c = fake_problem() if c is None else c
+    pvp = None if prev is False else ctypes.byref(fake_prev() if prev is None else prev)
+    return lib.gdn_commit_verify(ctypes.byref(c), pvp, o, w, None)
+
+
+def test_commit_verify_validation(lib):
+    assert call_cv(lib, w=None) == 1
+    assert call_cv(lib, o=None) == 1
+    assert call_cv(lib, w=W_PTR + 8) == 7
+    assert call_cv(lib, c=fake_problem(max_T=17)) == 4          # single 16-token chunks
+    assert call_cv(lib, prev=fake_prev(max_T=17)) == 4
+    assert call_cv(lib, prev=fake_prev(reserved=1)) == 2
+    assert call_cv(lib, prev=fake_prev(max_T=-1)) == 2
+    assert call_cv(lib, c=fake_problem(dk=64, dv=64)) == 4      # chunked kernel only
+    assert call_cv(lib, c=fake_problem(algo=1)) == 4
+    assert call_cv(lib, c=fake_problem(algo=3)) == 4
+    assert call_cv(lib, c=fake_problem(qkv_dtype=0)) == 4
+    assert call_cv(lib, prev=fake_prev(w=None)) == 1
+    assert call_cv(lib, prev=fake_prev(accepted=None)) == 1
+    assert call_cv(lib, prev=fake_prev(k=fake_prev().k + 8)) == 7
+    assert call_cv(lib, prev=fake_prev(w=fake_prev().w + 4)) == 7
+    assert call_cv(lib, w=O_PTR) == 8                           # w over o
+    assert call_cv(lib, w=fake_prev().w) == 8                   # w over the previous w
+    assert call_cv(lib, w=fake_problem().q) == 8                # w over an input
+    assert call_cv(lib, prev=fake_prev(w=fake_problem().pool)) == 8   # previous arrays over the pool
+    assert call_cv(lib, prev=fake_prev(k=O_PTR)) == 8           # ... or over o
+    assert call_cv(lib, c=fake_problem(batch=0, q=None, pool=None)) == 0
