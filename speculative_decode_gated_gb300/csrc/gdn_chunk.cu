@@ -102,9 +102,11 @@ struct Aux {
     int abort_flag;
 };
 
+constexpr uint32_t kWpBoxBytes = 32 * CT * 4;  // W box: 32 value columns x 16 token rows
 struct Smem {
     unsigned char tile[kTileBytes];
     TokBuf tok[2];
+    unsigned char wprev[4 * kWpBoxBytes];  // commit-then-verify: the previous step's W rows
     Aux aux;
 };
 constexpr size_t kSmemBytes = 1024 + sizeof(Smem);
@@ -346,6 +348,7 @@ struct UnitPlan {
 struct Maps {
     CUtensorMap pool, q, k, v;
     CUtensorMap kp;  // commit-then-verify: the previous step's k
+    CUtensorMap wp;  // and the W its call cached
 };
 
 // One launch: NL problems that share every request-level field (batch, heads,
@@ -480,12 +483,22 @@ __device__ __forceinline__ void issue_tokens(const Maps &maps, const UnitPlan &p
 }
 
 // Thread 0: the four tile boxes of one unit.
+// Commit-then-verify units with a prefix to commit also bring the previous
+// step's W rows of the request (4 boxes of 32 columns x 16 rows) on the same
+// barrier.
+template <int MODE>
 __device__ __forceinline__ void issue_tile(const Maps &maps, const UnitPlan &pl,
-                                           unsigned char *tile, uint32_t tile_bar) {
-    mbar_arrive_expect_tx(tile_bar, kTileBytes);
+                                           unsigned char *tile, uint32_t tile_bar,
+                                           unsigned char *wprev) {
+    const bool wp = MODE == kLagged && pl.pa > 0;
+    mbar_arrive_expect_tx(tile_bar, kTileBytes + (wp ? 4 * kWpBoxBytes : 0u));
 #pragma unroll
     for (int b = 0; b < 4; ++b)
         tma_load_3d(smem_u32(tile) + b * kBoxBytes, &maps.pool, 32 * b, 0, pl.tile, tile_bar);
+    if (wp)
+#pragma unroll
+        for (int b = 0; b < 4; ++b)
+            tma_load_3d(smem_u32(wprev) + b * kWpBoxBytes, &maps.wp, 32 * b, pl.h, pl.prow0, tile_bar);
 }
 
 // Thread 0: pull the tile and token rows of a later unit into L2 (no shared
@@ -569,12 +582,6 @@ __device__ __forceinline__ float prev_gate_load(const Args &p, const UnitPlan &p
     long long row = (long long)pl.prow0 + (tid < pl.pa ? tid : pl.pa - 1);
     row = row < 0 ? 0 : (row >= p.p_ntok ? p.p_ntok - 1 : row);
     return ld_early(p.p_alpha + (size_t)row * p.H + pl.h);
-}
-
-__device__ __forceinline__ float2 ld_early2(const float *ptr) {
-    float2 v;
-    asm volatile("ld.global.nc.v2.f32 {%0, %1}, [%2];" : "=f"(v.x), "=f"(v.y) : "l"(ptr));
-    return v;
 }
 
 // ------------------------------------------------------------ the kernel
@@ -750,7 +757,7 @@ __global__ void __launch_bounds__(kThreads, kBlocksPerSM)
     int steps = 0;       // steps computed
     if (tid == 0 && !cur.skip) {
         issue_tokens<MODE>(L.maps[cur.layer], cur, 0, sm.tok[0], smem_u32(&ax.tok_full[0]));
-        issue_tile(L.maps[cur.layer], cur, sm.tile, tile_bar);
+        issue_tile<MODE>(L.maps[cur.layer], cur, sm.tile, tile_bar, sm.wprev);
     }
     if (tid == 0 && !nxt.skip) prefetch_unit<MODE>(L.maps[nxt.layer], nxt);
     if (!cur.skip) {
@@ -762,6 +769,8 @@ __global__ void __launch_bounds__(kThreads, kBlocksPerSM)
     // replaced by alpha = 1, beta = 0 where the values are used.
     float ga = gate_load(L.a[cur.layer].alpha, p, cur, 0, tid);
     float gb = gate_load(L.a[cur.layer].beta, p, cur, 0, tid);
+    // Commit-then-verify: the previous step's gate of the next unit (its row tid).
+    float gpa = prev_gate_load<MODE>(L.a[cur.layer], cur, tid);
 
     // The unit's state as H^T in the A-fragment layout: the checkpoint tile,
     // then the state after each chunk (single-chunk verify needs none).
@@ -783,12 +792,13 @@ __global__ void __launch_bounds__(kThreads, kBlocksPerSM)
             // Gates of the next unit (consumed one iteration later).
             ga = gate_load(L.a[cur.layer].alpha, p, cur, 0, tid);
             gb = gate_load(L.a[cur.layer].beta, p, cur, 0, tid);
+            gpa = prev_gate_load<MODE>(L.a[cur.layer], cur, tid);
             if (!cur.skip && issued == processed) {
                 // Nothing is in flight: the next unit's loads can all go now.
                 if (tid == kTokIssuer)
                     issue_tokens<MODE>(L.maps[cur.layer], cur, 0, sm.tok[tok_issued & 1],
                                        smem_u32(&ax.tok_full[tok_issued & 1]));
-                if (tid == kTileIssuer) issue_tile(L.maps[cur.layer], cur, sm.tile, tile_bar);
+                if (tid == kTileIssuer) issue_tile<MODE>(L.maps[cur.layer], cur, sm.tile, tile_bar, sm.wprev);
                 ++issued;
                 ++tok_issued;
             }
@@ -799,25 +809,6 @@ __global__ void __launch_bounds__(kThreads, kBlocksPerSM)
         // W its call cached for this thread's columns and rows t < a_prev (0 beyond),
         // in the accumulator layout of the W product (token 8 ntt + 2c + (e & 1),
         // column col0 + 2m + (e >> 1)); consumed after the tile wait.
-        float gpa = 1.0f;
-        float wp[MODE == kLagged ? MT : 1][2][4];
-        if constexpr (MODE == kLagged) {
-            const Args &pa = L.a[me.layer];
-            gpa = prev_gate_load<MODE>(pa, me, tid);
-#pragma unroll
-            for (int m = 0; m < MT; ++m)
-#pragma unroll
-                for (int ntt = 0; ntt < 2; ++ntt)
-#pragma unroll
-                    for (int eo = 0; eo < 2; ++eo) {
-                        const int t = 8 * ntt + 2 * c + eo;
-                        float2 x = make_float2(0.0f, 0.0f);
-                        if (t < me.pa)
-                            x = ld_early2(pa.p_w + ((size_t)(me.prow0 + t) * pa.H + me.h) * D + col0 + 2 * m);
-                        wp[m][ntt][eo] = x.x;
-                        wp[m][ntt][2 + eo] = x.y;
-                    }
-        }
         const int Tu = me.teff;  // tokens of the unit that matter: T_r, or a_r for commit
         const int nch = MULTI ? (Tu + CT - 1) / CT : 1;
         // The commit point: chunk `ca` holds token a_r - 1.
@@ -858,6 +849,7 @@ __global__ void __launch_bounds__(kThreads, kBlocksPerSM)
             } else {
                 ga = gate_load(L.a[cur.layer].alpha, p, cur, 0, tid);
                 gb = gate_load(L.a[cur.layer].beta, p, cur, 0, tid);
+                gpa = prev_gate_load<MODE>(L.a[cur.layer], cur, tid);
             }
             if (!wait_parity(smem_u32(&ax.tok_full[steps & 1]), (steps >> 1) & 1))
                 ax.abort_flag = 1;
@@ -955,9 +947,29 @@ __global__ void __launch_bounds__(kThreads, kBlocksPerSM)
                         hr[kb][rr][2] = x.z;
                         hr[kb][rr][3] = x.w;
                     }
-                if (me.pa > 0)
+                if (me.pa > 0) {
+                    // W of the previous step's rows, staged with the tile (box `warp`,
+                    // row t, 128-byte swizzle), in the accumulator layout of the W
+                    // product: token 8 ntt + 2c + (e & 1), column col0 + 2m + (e >> 1).
+                    float wp[MT][2][4];
+                    const unsigned char *wb = sm.wprev + warp * kWpBoxBytes;
+#pragma unroll
+                    for (int m = 0; m < MT; ++m)
+#pragma unroll
+                        for (int ntt = 0; ntt < 2; ++ntt)
+#pragma unroll
+                            for (int eo = 0; eo < 2; ++eo) {
+                                const int t = 8 * ntt + 2 * c + eo;
+                                const float2 x = *reinterpret_cast<const float2 *>(
+                                    wb + t * 128 + ((g ^ (t & 7)) << 4) + 8 * m);
+                                // rows past a_prev meet a zero weight; keep them finite
+                                const bool live = t < me.pa;
+                                wp[m][ntt][eo] = live ? x.x : 0.0f;
+                                wp[m][ntt][2 + eo] = live ? x.y : 0.0f;
+                            }
                     state_update<true, true>(hr, wp, ax.pdcol, ax.pgam, smem_u32(tb.kp), kTokHalfBytes,
                                              lane, c, opaque(me.u.tile) + col0);
+                }
             }
             if constexpr (TC) {
                 // 5. The state at the chunk's start as A = H^T in TMEM, bf16 hi and
@@ -1002,7 +1014,7 @@ __global__ void __launch_bounds__(kThreads, kBlocksPerSM)
                 if (!MULTI || ch == 0) {
                     ++processed;
                     if (!cur.skip) {
-                        if (tid == kTileIssuer) issue_tile(L.maps[cur.layer], cur, sm.tile, tile_bar);
+                        if (tid == kTileIssuer) issue_tile<MODE>(L.maps[cur.layer], cur, sm.tile, tile_bar, sm.wprev);
                         ++issued;
                     }
                     if (tid == kPrefIssuer && !nxt.skip) prefetch_unit<MODE>(L.maps[nxt.layer], nxt);
@@ -1273,7 +1285,7 @@ __global__ void __launch_bounds__(kThreads, kBlocksPerSM)
             if (!MULTI || ch == 0) {
                 ++processed;
                 if (!cur.skip) {
-                    if (tid == kTileIssuer) issue_tile(L.maps[cur.layer], cur, sm.tile, tile_bar);
+                    if (tid == kTileIssuer) issue_tile<MODE>(L.maps[cur.layer], cur, sm.tile, tile_bar, sm.wprev);
                     ++issued;
                 }
                 if (tid == kPrefIssuer && !nxt.skip) prefetch_unit<MODE>(L.maps[nxt.layer], nxt);
@@ -1536,6 +1548,15 @@ cudaError_t encode_layer(const Args &p, Maps *maps) {
         return cudaErrorInvalidValue;
     if (p.p_k && !encode_tokens(encode, &maps->kp, p.p_k, p.H, p.p_ntok))  // the previous step's k
         return cudaErrorInvalidValue;
+    if (p.p_w) {  // the previous step's W: [rows][H][dv] fp32, boxes of 32 columns x 16 rows
+        const cuuint64_t wdims[3] = {(cuuint64_t)D, (cuuint64_t)p.H, (cuuint64_t)p.p_ntok};
+        const cuuint64_t wstrides[2] = {(cuuint64_t)D * 4, (cuuint64_t)p.H * D * 4};
+        const cuuint32_t wbox[3] = {32, 1, (cuuint32_t)CT};
+        if (encode(&maps->wp, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, const_cast<float *>(p.p_w), wdims,
+                   wstrides, wbox, elem, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+            return cudaErrorInvalidValue;
+    }
     return cudaSuccess;
 }
 
