@@ -787,8 +787,8 @@ __global__ void __launch_bounds__(kThreads, kBlocksPerSM)
         if (REPLAY) finalize_replay<MODE>(L.a[cur.layer], cur, tid);
         nxt.skip = true;
         if (unit + 2 * G < W) nxt = plan_unit<MODE, NL, REPLAY>(L, unit + 2 * G, U, raw);
-        raw = load_unit_meta<MODE, RAGGED, NL>(p, unit + 3 * G, W, U);
         if (me.skip) {
+            raw = load_unit_meta<MODE, RAGGED, NL>(p, unit + 3 * G, W, U);
             // Gates of the next unit (consumed one iteration later).
             ga = gate_load(L.a[cur.layer].alpha, p, cur, 0, tid);
             gb = gate_load(L.a[cur.layer].beta, p, cur, 0, tid);
@@ -923,7 +923,9 @@ __global__ void __launch_bounds__(kThreads, kBlocksPerSM)
             }
             __syncthreads();
 
-            // 4. The checkpoint tile of this unit (first chunk only).
+            // 4. The checkpoint tile of this unit (first chunk only).  The metadata
+            //    of the unit three ahead is loaded here, mid-unit: at the top of the
+            //    loop these loads would queue behind the previous unit's stores.
             if (!MULTI || ch == 0) {
                 if (!wait_parity(tile_bar, processed & 1)) ax.abort_flag = 1;
                 __syncthreads();
@@ -931,6 +933,7 @@ __global__ void __launch_bounds__(kThreads, kBlocksPerSM)
                     aborted = true;
                     break;
                 }
+                raw = load_unit_meta<MODE, RAGGED, NL>(p, unit + 3 * G, W, U);
             }
 
             // 4b. Commit-then-verify: the checkpoint into registers, then the previous
