@@ -614,18 +614,12 @@ __device__ __forceinline__ int key_row(int kb, int c, int rr) {
     return 16 * kb + 2 * c + (rr & 1) + 8 * (rr >> 1);
 }
 
-// The state after `dvec`-weighted tokens of the chunk:
-//   H^T <- gam H^T + (dvec . W)^T K       (dvec[s] = 0 for tokens not taken)
-// 16 key rows at a time; the accumulators start from the state in `hr` (the
-// A-fragment layout of H^T is also the accumulator layout of this product).
-// STORE: the result goes to `dst` (this thread's columns of the pool tile,
-// 16-byte stores); KEEP: it replaces `hr`.  `khalf`: bytes from one column
-// half of the k tile to the next.
-template <bool STORE, bool KEEP>
-__device__ __forceinline__ void state_update(float (&hr)[8][4][CPT], const float (&wq)[MT][2][4],
-                                             const float *dvec, float gam, uint32_t k_smem,
-                                             uint32_t khalf, int lane, int c, float *dst) {
-    uint32_t ah[MT][4], al[MT][4];
+// The weights of a rank-16 state update, (dvec . W)^T split into bf16 hi + lo
+// A fragments: W in the accumulator layout of the W product (token
+// 8 ntt + 2c + (e & 1), column col0 + 2m + (e >> 1)), dvec[s] = 0 for tokens
+// not taken.
+__device__ __forceinline__ void update_weights(const float (&wq)[MT][2][4], const float *dvec, int c,
+                                               uint32_t (&ah)[MT][4], uint32_t (&al)[MT][4]) {
 #pragma unroll
     for (int ntt = 0; ntt < 2; ++ntt) {
         const float d0 = dvec[8 * ntt + 2 * c], d1 = dvec[8 * ntt + 2 * c + 1];
@@ -635,41 +629,72 @@ __device__ __forceinline__ void state_update(float (&hr)[8][4][CPT], const float
             split2(d0 * wq[m][ntt][2], d1 * wq[m][ntt][3], ah[m][2 * ntt + 1], al[m][2 * ntt + 1]);
         }
     }
+}
+
+// Key rows 16 kb .. 16 kb + 15 of the update H^T <- gam H^T + (dvec . W)^T K:
+// `hv` holds those rows of H^T on entry (the A-fragment layout of H^T is also
+// the accumulator layout of this product) and of the result on exit.
+// `khalf`: bytes from one column half of the k tile to the next.
+__device__ __forceinline__ void update_rows(float (&hv)[4][CPT], int kb, const uint32_t (&ah)[MT][4],
+                                            const uint32_t (&al)[MT][4], float gam, uint32_t k_smem,
+                                            uint32_t khalf, int lane) {
+#pragma unroll
+    for (int rr = 0; rr < 4; ++rr)
+#pragma unroll
+        for (int e = 0; e < CPT; ++e) hv[rr][e] *= gam;
     // ldmatrix.trans row address of this lane: matrix lane/8 -> (token half, dk half).
     const int mi = lane >> 3;
     const int krow = (lane & 7) + 8 * (mi & 1);
+    uint32_t b00, b01, b10, b11;  // (n-tile 2kb: b0, b1), (n-tile 2kb+1: b0, b1)
+    ldsm_x4_trans(b00, b01, b10, b11, k_smem + tok_off(krow, 16 * kb + 8 * (mi >> 1), khalf));
+#pragma unroll
+    for (int m = 0; m < MT; ++m) {
+        mma(hv[0][2 * m], hv[1][2 * m], hv[0][2 * m + 1], hv[1][2 * m + 1], ah[m][0], ah[m][1],
+            ah[m][2], ah[m][3], b00, b01);
+        mma(hv[2][2 * m], hv[3][2 * m], hv[2][2 * m + 1], hv[3][2 * m + 1], ah[m][0], ah[m][1],
+            ah[m][2], ah[m][3], b10, b11);
+    }
+#pragma unroll
+    for (int m = 0; m < MT; ++m) {
+        mma(hv[0][2 * m], hv[1][2 * m], hv[0][2 * m + 1], hv[1][2 * m + 1], al[m][0], al[m][1],
+            al[m][2], al[m][3], b00, b01);
+        mma(hv[2][2 * m], hv[3][2 * m], hv[2][2 * m + 1], hv[3][2 * m + 1], al[m][0], al[m][1],
+            al[m][2], al[m][3], b10, b11);
+    }
+}
+
+// This thread's four columns of key rows 16 kb .. 16 kb + 15 of a pool tile (16-byte stores).
+__device__ __forceinline__ void store_rows(float *dst, int kb, int c, const float (&hv)[4][CPT]) {
+#pragma unroll
+    for (int rr = 0; rr < 4; ++rr)
+        *reinterpret_cast<float4 *>(dst + key_row(kb, c, rr) * D) =
+            make_float4(hv[rr][0], hv[rr][1], hv[rr][2], hv[rr][3]);
+}
+
+// The state after `dvec`-weighted tokens of the chunk, from the state in `hr`:
+//   H^T <- gam H^T + (dvec . W)^T K       (dvec[s] = 0 for tokens not taken)
+// STORE: the result goes to `dst` (this thread's columns of the pool tile);
+// KEEP: it replaces `hr`.
+template <bool STORE, bool KEEP>
+__device__ __forceinline__ void state_update(float (&hr)[8][4][CPT], const float (&wq)[MT][2][4],
+                                             const float *dvec, float gam, uint32_t k_smem,
+                                             uint32_t khalf, int lane, int c, float *dst) {
+    uint32_t ah[MT][4], al[MT][4];
+    update_weights(wq, dvec, c, ah, al);
 #pragma unroll
     for (int kb = 0; kb < 8; ++kb) {
         float hv[4][CPT];
 #pragma unroll
         for (int rr = 0; rr < 4; ++rr)
 #pragma unroll
-            for (int e = 0; e < CPT; ++e) hv[rr][e] = gam * hr[kb][rr][e];
-        uint32_t b00, b01, b10, b11;  // (n-tile 2kb: b0, b1), (n-tile 2kb+1: b0, b1)
-        ldsm_x4_trans(b00, b01, b10, b11, k_smem + tok_off(krow, 16 * kb + 8 * (mi >> 1), khalf));
+            for (int e = 0; e < CPT; ++e) hv[rr][e] = hr[kb][rr][e];
+        update_rows(hv, kb, ah, al, gam, k_smem, khalf, lane);
+        if (STORE) store_rows(dst, kb, c, hv);
+        if (KEEP)
 #pragma unroll
-        for (int m = 0; m < MT; ++m) {
-            mma(hv[0][2 * m], hv[1][2 * m], hv[0][2 * m + 1], hv[1][2 * m + 1], ah[m][0], ah[m][1],
-                ah[m][2], ah[m][3], b00, b01);
-            mma(hv[2][2 * m], hv[3][2 * m], hv[2][2 * m + 1], hv[3][2 * m + 1], ah[m][0], ah[m][1],
-                ah[m][2], ah[m][3], b10, b11);
-        }
-#pragma unroll
-        for (int m = 0; m < MT; ++m) {
-            mma(hv[0][2 * m], hv[1][2 * m], hv[0][2 * m + 1], hv[1][2 * m + 1], al[m][0], al[m][1],
-                al[m][2], al[m][3], b00, b01);
-            mma(hv[2][2 * m], hv[3][2 * m], hv[2][2 * m + 1], hv[3][2 * m + 1], al[m][0], al[m][1],
-                al[m][2], al[m][3], b10, b11);
-        }
-#pragma unroll
-        for (int rr = 0; rr < 4; ++rr) {
-            if (STORE)
-                *reinterpret_cast<float4 *>(dst + key_row(kb, c, rr) * D) =
-                    make_float4(hv[rr][0], hv[rr][1], hv[rr][2], hv[rr][3]);
-            if (KEEP)
+            for (int rr = 0; rr < 4; ++rr)
 #pragma unroll
                 for (int e = 0; e < CPT; ++e) hr[kb][rr][e] = hv[rr][e];
-        }
     }
 }
 
@@ -774,7 +799,8 @@ __global__ void __launch_bounds__(kThreads, kBlocksPerSM)
 
     // The unit's state as H^T in the A-fragment layout: the checkpoint tile,
     // then the state after each chunk (single-chunk verify needs none).
-    constexpr bool kKeep = MULTI || MODE != kVerify;
+    // (commit-then-verify keeps none: its update is folded into the first product)
+    constexpr bool kKeep = MULTI || MODE == kCommit || MODE == kFused;
     float hr[kKeep ? 8 : 1][4][CPT];  // mma.sync path (unused, and removed, on the tcgen05 path)
     // tcgen05 path: this thread's column of the state (key rows 0..127).
     float hcol[(kKeep && TC) ? D : 1];
@@ -936,25 +962,16 @@ __global__ void __launch_bounds__(kThreads, kBlocksPerSM)
                 raw = load_unit_meta<MODE, RAGGED, NL>(p, unit + 3 * G, W, U);
             }
 
-            // 4b. Commit-then-verify: the checkpoint into registers, then the previous
-            //     step's accepted prefix on top of it (its W cached by its call), written
-            //     to the slot; this step's drafts are verified from that state.
+            // 4b. Commit-then-verify: the weights of the previous step's accepted
+            //     prefix (its W, cached by its call and staged with the tile: box
+            //     `warp`, row t, 128-byte swizzle), split for the tensor cores.  The
+            //     update itself runs 16 key rows at a time inside the first product
+            //     below, which then works on the committed state; each block of rows
+            //     is written to the slot as it is made.
+            uint32_t lah[MODE == kLagged ? MT : 1][4], lal[MODE == kLagged ? MT : 1][4];
             if constexpr (MODE == kLagged) {
-#pragma unroll
-                for (int kb = 0; kb < 8; ++kb)
-#pragma unroll
-                    for (int rr = 0; rr < 4; ++rr) {
-                        const float4 x = ld_tile_row(sm.tile, warp, g, key_row(kb, c, rr));
-                        hr[kb][rr][0] = x.x;
-                        hr[kb][rr][1] = x.y;
-                        hr[kb][rr][2] = x.z;
-                        hr[kb][rr][3] = x.w;
-                    }
                 if (me.pa > 0) {
-                    // W of the previous step's rows, staged with the tile (box `warp`,
-                    // row t, 128-byte swizzle), in the accumulator layout of the W
-                    // product: token 8 ntt + 2c + (e & 1), column col0 + 2m + (e >> 1).
-                    float wp[MT][2][4];
+                    float wp[MT][2][4];  // token 8 ntt + 2c + (e & 1), column col0 + 2m + (e >> 1)
                     const unsigned char *wb = sm.wprev + warp * kWpBoxBytes;
 #pragma unroll
                     for (int m = 0; m < MT; ++m)
@@ -970,8 +987,7 @@ __global__ void __launch_bounds__(kThreads, kBlocksPerSM)
                                 wp[m][ntt][eo] = live ? x.x : 0.0f;
                                 wp[m][ntt][2 + eo] = live ? x.y : 0.0f;
                             }
-                    state_update<true, true>(hr, wp, ax.pdcol, ax.pgam, smem_u32(tb.kp), kTokHalfBytes,
-                                             lane, c, opaque(me.u.tile) + col0);
+                    update_weights(wp, ax.pdcol, c, lah, lal);
                 }
             }
             if constexpr (TC) {
@@ -1234,7 +1250,7 @@ __global__ void __launch_bounds__(kThreads, kBlocksPerSM)
                     if (lane < kTinvLanes) ax.Tinv[t][tj] = acc;
                 }
                 float hv[4][CPT];
-                if ((!MULTI || ch == 0) && MODE != kLagged) {
+                if (!MULTI || ch == 0) {
 #pragma unroll
                     for (int rr = 0; rr < 4; ++rr) {
                         const float4 x = ld_tile_row(sm.tile, warp, g, key_row(kb, c, rr));
@@ -1251,6 +1267,13 @@ __global__ void __launch_bounds__(kThreads, kBlocksPerSM)
                     for (int rr = 0; rr < 4; ++rr)
 #pragma unroll
                         for (int e = 0; e < CPT; ++e) hv[rr][e] = hr[kKeep ? kb : 0][rr][e];
+                }
+                if constexpr (MODE == kLagged) {
+                    // These rows of the committed state, written to the slot, then used.
+                    if (me.pa > 0) {
+                        update_rows(hv, kb, lah, lal, ax.pgam, smem_u32(tb.kp), kTokHalfBytes, lane);
+                        store_rows(opaque(me.u.tile) + col0, kb, c, hv);
+                    }
                 }
                 uint32_t b[4][2];
 #pragma unroll
