@@ -17,7 +17,7 @@ from speculative_decode_gated_gb300 import binding, inputs, staging
 pytestmark = pytest.mark.gpu
 
 
-def steps(kind, seed=41, n=3):
+def steps(kind, seed=41, n=3, gate="alpha"):
     """n steps of the same requests (slot ids from the seed's metadata stream)."""
     rng = np.random.default_rng(seed)
     out = []
@@ -34,7 +34,7 @@ def steps(kind, seed=41, n=3):
         if len(acc) > 2:
             acc[2] = 0  # nothing accepted
         out.append(inputs.make_custom(dk=128, dv=128, pool_slots=11, qkv_dtype="bf16", seed=seed,
-                                      layer=i, accepted=acc, name=f"{kind}{i}", **spec))
+                                      layer=i, accepted=acc, name=f"{kind}{i}", gate=gate, **spec))
     return out
 
 
@@ -68,9 +68,11 @@ def run_chain(probs, bad=None):
         prev_d, prev_w, prev_host = d, w, prob
 
 
-@pytest.mark.parametrize("kind", ["uniform", "ragged"])
-def test_chain_matches_the_oracle(kind):
-    for i, prob, prev, code, before, after, ref_after, o, o_ref in run_chain(steps(kind)):
+@pytest.mark.parametrize("kind,gate", [("uniform", "alpha"), ("ragged", "alpha"), ("ragged", "log")])
+def test_chain_matches_the_oracle(kind, gate):
+    """gate = "log": alpha holds g for both steps; the kernel applies expf to the
+    previous step's gates too."""
+    for i, prob, prev, code, before, after, ref_after, o, o_ref in run_chain(steps(kind, gate=gate)):
         assert code == 0
         # outputs of every draft row
         rows = np.concatenate([np.arange(prob.cu_seqlens[r], prob.cu_seqlens[r + 1])
@@ -118,3 +120,43 @@ def test_bad_previous_length_is_flagged_and_skipped():
         rows = np.concatenate([np.arange(prob.cu_seqlens[r], prob.cu_seqlens[r + 1])
                                for r in good]).astype(int)
         assert rel_err(o[rows], o_ref[rows]) <= TOL
+
+
+@pytest.mark.parametrize("name", ["b64_h32_d128_t16_x24", "b128_h32_d128_ragged16"])
+def test_full_size_sampled(name):
+    """The benchmark's workloads at full size, in the launch the benchmark times
+    (the previous step is the same problem, as in bench.py --order lagged):
+    sampled units against the oracle (commit the previous step's prefix, then
+    verify), every committed slot of the sample within the tolerance."""
+    from parity import pick_units
+    prob = inputs.make_problem(name)
+    units = pick_units(prob, 40)
+    # oracle: the state after a_prev rows of the previous step (or the checkpoint), then verify
+    _, s_acc = oracle.run_units(prob, units, want_o=False)
+    s0 = prob.s0.reshape(prob.units, prob.dk, prob.dv)[units].astype(np.float64)
+    acc_u = np.array([prob.accepted[int(u) // prob.heads] for u in units])
+    s_mid = np.where(acc_u[:, None, None] > 0, s_acc, s0)
+    o_ref, _ = oracle.run_units(prob, units, s0=s_mid, want_state=False)
+    d = staging.DeviceProblem(prob, "cuda")
+    w_prev = torch.zeros((prob.n_tok, prob.heads, prob.dv), device="cuda")
+    w = torch.zeros_like(w_prev)
+    # the previous step's W: what its own call (from the same checkpoints) writes
+    binding.gdn_commit_verify(d.c, None, d.o, w_prev)
+    prev = binding.make_prev_step(k=d.k, alpha=d.alpha, w=w_prev, accepted=d.accepted,
+                                  max_T=prob.max_T, cu_seqlens=d.cu_seqlens)
+    d.o.fill_(float("nan"))
+    binding.gdn_commit_verify(d.c, prev, d.o, w)
+    torch.cuda.synchronize()
+    assert binding.gdn_read_device_error(d.c) == 0
+    o = d.o.cpu().numpy()
+    pool = d.pool.cpu().numpy()
+    got = np.zeros_like(o_ref)
+    for n, u in enumerate(units):
+        r, h = divmod(int(u), prob.heads)
+        c0, L = int(prob.cu_seqlens[r]), int(prob.lengths[r])
+        got[n, :L] = o[c0:c0 + L, h]
+        if prob.accepted[r] > 0:
+            assert rel_err(pool[int(prob.slot_ids[r]), h], s_acc[n]) <= TOL, f"unit {u} state"
+    assert rel_err(got, o_ref) <= TOL
+    del d
+    torch.cuda.empty_cache()

@@ -2,7 +2,7 @@
 
 * bf16 o (GDN_FLAG_O_BF16): the output must be, bit for bit, the round to
   nearest even of the float32 output of the same call (oracle parity itself
-  is judged on the float32 path, which the other tests cover).
+  is established on the float32 path, which the other tests cover).
 * log-space gates (GDN_FLAG_LOG_GATE): alpha holds g and the kernels use
   alpha = expf(g); compared with the oracle, which takes alpha = exp(g).
 """
