@@ -6,8 +6,8 @@
  * checkpoint of that state, computes the draft tokens' outputs from the
  * checkpoint and the buffered inputs, and on rejection keeps only the accepted
  * prefix (OCRia write-up "OCRia 推理栈：单卡 B200 提速近 10 倍", section "Make
- * speculative verification cheaper"; the same in "How OCRia achieved a 10x
- * inference speedup on B200 GPUs", section "Wie es funktioniert").  The state
+ * speculative verification cheaper"; the same in "Wie OCRia einen 10-fachen
+ * Inference-Speedup auf B200-GPUs erreichte", section "Wie es funktioniert").  The state
  * update is the gated delta rule, with S the dv x dk state of one unit
  * (request r, head h):
  *
@@ -37,6 +37,16 @@
  *                            no request names are left bit-identical.
  *   gdn_verify_commit_fused  both in one pass: reads each checkpoint once,
  *                            writes o for every token and the state once.
+ *   gdn_commit_verify        the previous step's commit, then this step's
+ *                            verify, in one pass (the order an engine can run
+ *                            them in: a step's accepted lengths are known only
+ *                            after all its layers verified).
+ *   gdn_*_layers             the same calls for the layers of one step, in as
+ *                            few launches as possible.
+ *   gdn_replay_verify/commit a multi-step ReplaySSM buffer: outputs from the
+ *                            checkpoint plus buffered rows, periodic flush.
+ *   gdn_accept_prefix        greedy accepted lengths from token ids, on the
+ *                            device.
  *
  * Device-side argument errors (a slot id outside [0, pool_slots), a_r outside
  * [0, T_r], a ragged length outside [0, max_T]) cannot be seen on the host
