@@ -22,15 +22,18 @@
 // shuffle or shared-memory transpose.
 //
 // Pipeline of one block (the block walks units blockIdx.x, + gridDim.x, ...):
-//   * thread 0 issues, for the next unit that has work, four 3-D TMA copies of
-//     its 64 KiB tile (boxes of 32 value columns x 128 key rows) into the
-//     block's single tile stage, and 16-token boxes of its k, q and v rows into
-//     the other of two token buffers, all with the 128-byte swizzle, as soon
-//     as the current unit has read the tile (right after the first product);
-//   * at the same time it asks TMA to pull the unit after that into L2, so the
-//     shared-memory loads issued one unit later hit in L2;
-//   * metadata is loaded two units ahead and the gates one unit ahead, so no
-//     thread ever waits on a load it has just issued.
+//   * one thread of warp 1 issues, for the next unit that has work, four 3-D
+//     TMA copies of its 64 KiB tile (boxes of 32 value columns x 128 key rows)
+//     into the block's single tile stage as soon as the current unit has read
+//     the tile (right after the first product); one thread of warp 3 issues
+//     the 16-token boxes of its k, q and v rows into the other of two token
+//     buffers when the current unit starts; all with the 128-byte swizzle;
+//   * one thread of warp 2 asks TMA to pull the unit after that into L2, so
+//     the shared-memory loads issued one unit later hit in L2 (a TMA issue can
+//     hold its warp while the copy engine is busy, hence three issuing warps);
+//   * metadata is loaded three units ahead (mid-unit, not behind the stores)
+//     and the gates one unit ahead, so no thread waits on a load it has just
+//     issued.
 // Waits on the TMA mbarriers are bounded (about 2 s by %globaltimer); on expiry
 // the block reports GDN_DEVERR_TIMEOUT and stops after its copies have landed.
 //
@@ -460,7 +463,7 @@ __device__ __forceinline__ void finalize_replay(const Args &p, UnitPlan &pl, int
     if (bad && tid == 0 && p.dev_err) atomicOr(p.dev_err, GDN_DEVERR_REPLAY);
 }
 
-// Thread 0: the token boxes (k, v and, unless committing, q) of chunk `ch` of
+// One thread: the token boxes (k, v and, unless committing, q) of chunk `ch` of
 // one unit: token rows row0 + 16 ch + [0, 16).
 template <int MODE>
 __device__ __forceinline__ void issue_tokens(const Maps &maps, const UnitPlan &pl, int ch,
@@ -482,7 +485,7 @@ __device__ __forceinline__ void issue_tokens(const Maps &maps, const UnitPlan &p
     }
 }
 
-// Thread 0: the four tile boxes of one unit.
+// One thread: the four tile boxes of one unit.
 // Commit-then-verify units with a prefix to commit also bring the previous
 // step's W rows of the request (4 boxes of 32 columns x 16 rows) on the same
 // barrier.
@@ -501,7 +504,7 @@ __device__ __forceinline__ void issue_tile(const Maps &maps, const UnitPlan &pl,
             tma_load_3d(smem_u32(wprev) + b * kWpBoxBytes, &maps.wp, 32 * b, pl.h, pl.prow0, tile_bar);
 }
 
-// Thread 0: pull the tile and token rows of a later unit into L2 (no shared
+// One thread: pull the tile and token rows of a later unit into L2 (no shared
 // memory, no barrier), so its shared-memory loads, issued later, hit in L2.
 template <int MODE>
 __device__ __forceinline__ void prefetch_unit(const Maps &maps, const UnitPlan &pl) {
@@ -1306,7 +1309,7 @@ __global__ void __launch_bounds__(kThreads, kBlocksPerSM)
             }
 
             // Tinv is complete.  After the first chunk the tile is in registers:
-            // the stage is free and thread 0 sends the next unit's tile.
+            // the stage is free and warp 1 sends the next unit's tile.
             __syncthreads();
             if (!MULTI || ch == 0) {
                 ++processed;
