@@ -439,6 +439,11 @@ def run_ours(args, rank, world, local_rank):
                           "all verifies then all commits"),
                 "l2": "inputs larger than L2 (each step touches ~%.1f GB)" % (bytes_call * L / 1e9),
                 "algo": {1: "recurrent", 2: "chunk", 3: "chunk_tc"}.get(algo_used, str(algo_used)),
+                "arith": ("fp32 state and outputs; the state-sized products on tensor cores "
+                          "in bf16 on hi/lo splits of the fp32 operands (about 16 mantissa "
+                          "bits), fp32 accumulation; solves and gates in fp32"
+                          if algo_used in (binding.GDN_ALGO_CHUNK, binding.GDN_ALGO_CHUNK_TC)
+                          else "fp32 on CUDA cores"),
                 "accepted": ("greedy prefix match of token ids on the device, every step"
                              if args.with_accept else "given (device array)"),
             },
