@@ -15,7 +15,7 @@ from speculative_decode_gated_gb300 import binding, inputs, staging
 
 pytestmark = pytest.mark.gpu
 
-AUTO, REC = binding.GDN_ALGO_AUTO, binding.GDN_ALGO_RECURRENT
+AUTO, REC, TC = binding.GDN_ALGO_AUTO, binding.GDN_ALGO_RECURRENT, binding.GDN_ALGO_CHUNK_TC
 
 CASES = {
     # chunked kernel, uniform drafts, one launch
@@ -76,11 +76,20 @@ def check_layer_state(prob, before, after, units, s_ref):
         assert err <= TOL, f"layer state unit {u}: {err:.3e}"
 
 
-@pytest.mark.parametrize("name", list(CASES))
-@pytest.mark.parametrize("mode", ["verify", "commit", "fused"])
-def test_layers_parity_and_equal_to_single_calls(name, mode):
+def _layer_params():
+    for name in CASES:
+        for mode in ("verify", "commit", "fused"):
+            yield pytest.param(name, mode, None, id=f"{name}-{mode}")
+    # the tcgen05 kernel: layer batches run as one launch per layer
+    for mode in ("verify", "commit", "fused"):
+        yield pytest.param("ragged_b5_h2_d128_x4", mode, TC, id=f"ragged_b5_h2_d128_x4-{mode}-tc")
+
+
+@pytest.mark.parametrize("name,mode,algo", list(_layer_params()))
+def test_layers_parity_and_equal_to_single_calls(name, mode, algo):
     probs, refs = case(name)
-    algo = REC if probs[0].qkv_dtype == "fp32" else AUTO
+    if algo is None:
+        algo = REC if probs[0].qkv_dtype == "fp32" else AUTO
     pool, dps, arr = stage(probs, algo)
     pool_single = pool.clone()
     for d in dps:
