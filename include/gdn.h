@@ -272,7 +272,7 @@ GDN_API gdn_status gdn_replay_commit(const gdn_problem *p, const gdn_replay *rb,
  * what makes step 1 a single rank-a update: no products of the checkpoint.
  *
  *   p     this step: everything gdn_verify takes.  bf16 q/k/v, dk = dv = 128,
- *         max_T <= 16 (GDN_ERR_UNSUPPORTED otherwise); AUTO or GDN_ALGO_CHUNK.
+ *         1 <= max_T <= 16 (GDN_ERR_UNSUPPORTED otherwise); AUTO or GDN_ALGO_CHUNK.
  *   prev  the previous step of the same requests (same batch, heads, slot ids),
  *         or NULL for the first step (nothing is committed).
  *   o     as gdn_verify.

@@ -210,3 +210,22 @@ def test_device_side_argument_errors(kind, algo):
     units = np.array([r * prob.heads + hh for r in good for hh in range(prob.heads)])
     o_ref, _ = oracle_units(prob, units)
     assert rel_err(gather_outputs(prob, units, o, o_ref), o_ref) <= TOL
+
+
+@pytest.mark.parametrize("algo", [AUTO, REC, TC], ids=["auto", "rec", "tc"])
+def test_extreme_gates(algo):
+    """Gates at their limits in one batch: alpha in {0, 1e-30, 1e-6, 1} (the decay
+    products of the chunk form underflow to zero or stay exactly 1) and beta in
+    {0, 1}; the outputs and committed states still match the oracle."""
+    prob = inputs.make_custom(batch=4, heads=2, dk=128, dv=128, lengths=[16, 9, 16, 5],
+                              qkv_dtype="bf16", pool_slots=6, accept="uniform", seed=61,
+                              name="extreme_gates")
+    rng = np.random.default_rng(62)
+    prob.alpha = rng.choice(np.array([0.0, 1e-30, 1e-6, 1.0], np.float32),
+                            size=prob.alpha.shape).astype(np.float32)
+    prob.beta = rng.choice(np.array([0.0, 1.0], np.float32), size=prob.beta.shape).astype(np.float32)
+    units = np.arange(prob.units)
+    o_ref, s_ref = oracle_units(prob, units)
+    d = staging.DeviceProblem(prob, "cuda", algo=algo)
+    check_verify(d, units, o_ref)
+    check_state_update(d, units, s_ref, d.commit)
