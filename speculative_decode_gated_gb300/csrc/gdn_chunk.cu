@@ -872,10 +872,12 @@ __global__ void __launch_bounds__(kThreads, kBlocksPerSM)
             }
             // Gates of the next step, loaded straight into the registers just
             // freed (consumed one step later, so this load is never waited on here).
+            // A single-chunk unit loads the next unit's gates after its tile wait
+            // instead, away from the stores the previous unit just issued.
             if (more) {
                 ga = gate_load(L.a[me.layer].alpha, p, me, ch + 1, tid);
                 gb = gate_load(L.a[me.layer].beta, p, me, ch + 1, tid);
-            } else {
+            } else if (MULTI && ch > 0) {
                 ga = gate_load(L.a[cur.layer].alpha, p, cur, 0, tid);
                 gb = gate_load(L.a[cur.layer].beta, p, cur, 0, tid);
                 gpa = prev_gate_load<MODE>(L.a[cur.layer], cur, tid);
@@ -963,6 +965,11 @@ __global__ void __launch_bounds__(kThreads, kBlocksPerSM)
                     break;
                 }
                 raw = load_unit_meta<MODE, RAGGED, NL>(p, unit + 3 * G, W, U);
+                if (!more) {  // a single-chunk unit: the next unit's gates
+                    ga = gate_load(L.a[cur.layer].alpha, p, cur, 0, tid);
+                    gb = gate_load(L.a[cur.layer].beta, p, cur, 0, tid);
+                    gpa = prev_gate_load<MODE>(L.a[cur.layer], cur, tid);
+                }
             }
 
             // 4b. Commit-then-verify: the weights of the previous step's accepted
