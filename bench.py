@@ -469,8 +469,28 @@ def run_e2e(args, dps, stream, dev, fused):
     streams with the kernels of other layers."""
     import torch
 
-    host_in = [[t.cpu().pin_memory() for t in (d.q, d.k, d.v, d.alpha, d.beta, d.accepted)]
-               for d in dps]
+    # Each layer's inputs live in one device buffer (q, k, v, alpha, beta and the
+    # accepted lengths as 16-byte-aligned views of it) filled from one pinned host
+    # buffer: one host-to-device copy per layer and step.
+    names = ("q", "k", "v", "alpha", "beta", "accepted")
+    host_in, dev_in = [], []
+    for d in dps:
+        parts = [getattr(d, n) for n in names]
+        nbytes = [t.numel() * t.element_size() for t in parts]
+        offs, total = [], 0
+        for nb in nbytes:
+            offs.append(total)
+            total += (nb + 15) // 16 * 16
+        dbuf = torch.empty(total, dtype=torch.uint8, device=dev)
+        hbuf = torch.empty(total, dtype=torch.uint8).pin_memory()
+        for n, t, off, nb in zip(names, parts, offs, nbytes):
+            view = dbuf[off:off + nb].view(t.dtype).view(t.shape)
+            view.copy_(t)
+            hbuf[off:off + nb].copy_(t.cpu().contiguous().view(torch.uint8).view(-1))
+            setattr(d, n, view)
+        d.c = d._make_c()  # the C problem now points into the packed buffer
+        host_in.append(hbuf)
+        dev_in.append(dbuf)
     host_o = [torch.empty(d.o.shape, dtype=d.o.dtype).pin_memory() for d in dps]
     h2d = torch.cuda.Stream(dev)
     d2h = torch.cuda.Stream(dev)
@@ -479,7 +499,7 @@ def run_e2e(args, dps, stream, dev, fused):
     ev_used = [torch.cuda.Event() for _ in range(L)]
     ev_o = [torch.cuda.Event() for _ in range(L)]
     ev_read = [torch.cuda.Event() for _ in range(L)]
-    bi = sum(sum(t.numel() * t.element_size() for t in hs) for hs in host_in)
+    bi = sum(h.numel() for h in host_in)
     bo = sum(t.numel() * t.element_size() for t in host_o)
     kinds = ["fused"] if fused else ["verify", "commit"]
     calls = [{m: d.launcher(m, stream) for m in kinds} for d in dps]
@@ -488,8 +508,7 @@ def run_e2e(args, dps, stream, dev, fused):
         for l, d in enumerate(dps):
             with torch.cuda.stream(h2d):
                 h2d.wait_event(ev_used[l])
-                for dst, src in zip((d.q, d.k, d.v, d.alpha, d.beta, d.accepted), host_in[l]):
-                    dst.copy_(src, non_blocking=True)
+                dev_in[l].copy_(host_in[l], non_blocking=True)
                 ev_in[l].record(h2d)
             stream.wait_event(ev_in[l])
             stream.wait_event(ev_read[l])
