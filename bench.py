@@ -414,6 +414,12 @@ def run_ours(args, rank, world, local_rank):
         cpu = {"value": us, "unit": UNIT, "cores": threads, "kind": "oracle",
                "sample": f"{n} of {p0.units} units of layer 0, verify pass + commit pass, "
                          f"{dt:.1f} s wall, scaled to a full layer-call"}
+        if args.cpu_units_1t > 0:
+            dt1, us1, n1 = cpu_oracle_time(p0, args.cpu_units_1t, 1)
+            cpu["single_thread"] = {
+                "value": us1, "unit": UNIT, "cores": 1,
+                "sample": f"{n1} of {p0.units} units of layer 0, {dt1:.1f} s wall, "
+                          f"scaled to a full layer-call"}
 
     if rank == 0:
         gbs = bytes_call / (us_call * 1e-6) / 1e9
@@ -553,6 +559,8 @@ def main():
     ap.add_argument("--layers", type=int, default=0,
                     help="run only the first N layers (small cases for profiling; 0 = all)")
     ap.add_argument("--cpu-units", type=int, default=256)
+    ap.add_argument("--cpu-units-1t", type=int, default=32,
+                    help="units of the single-threaded oracle sample (0 skips it)")
     ap.add_argument("--ref-units", type=int, default=64)
     ap.add_argument("--e2e-steps", type=int, default=20)
     ap.add_argument("--no-e2e", action="store_true")
