@@ -47,6 +47,7 @@
  *                            checkpoint plus buffered rows, periodic flush.
  *   gdn_accept_prefix        greedy accepted lengths from token ids, on the
  *                            device.
+ *   gdn_selftest_wait_timeout  runs the bounded wait to its expiry (diagnostic).
  *
  * Device-side argument errors (a slot id outside [0, pool_slots), a_r outside
  * [0, T_r], a ragged length outside [0, max_T]) cannot be seen on the host
@@ -298,6 +299,17 @@ GDN_API gdn_status gdn_commit_verify(const gdn_problem *p, const gdn_prev_step *
 
 GDN_API gdn_status gdn_read_device_error(const gdn_problem *p, cudaStream_t stream,
                                          int32_t *host_code);
+
+/* Self-check of the bounded waits (diagnostic; not part of a decode step).
+ * The chunked kernel waits on shared-memory barriers for its copies and
+ * products, and gives up after about two seconds with GDN_DEVERR_TIMEOUT
+ * rather than hang.  This call runs that same wait in one block, on a barrier
+ * that nothing completes: after about two seconds the block ORs
+ * GDN_DEVERR_TIMEOUT into *dev_err and exits, and the CUDA context stays
+ * usable.  Asynchronous on `stream` (one SM is busy meanwhile).
+ * dev_err: device int32, caller-owned, 4-byte aligned, not NULL (else
+ * GDN_ERR_NULL_PTR / GDN_ERR_ALIGN before any CUDA call). */
+GDN_API gdn_status gdn_selftest_wait_timeout(int32_t *dev_err, cudaStream_t stream);
 
 /* The algo that AUTO resolves to for this problem (host only, no CUDA call),
  * or -1 when the shape fails validation. */

@@ -16,7 +16,7 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 LIB_DIR = os.path.join(PKG, "_lib")
 LIB = os.path.join(LIB_DIR, "libgdn.so")
-SOURCES = ["gdn_api.cu", "gdn_recurrent.cu", "gdn_chunk.cu", "gdn_accept.cu"]
+SOURCES = ["gdn_api.cu", "gdn_recurrent.cu", "gdn_chunk.cu", "gdn_accept.cu", "gdn_selftest.cu"]
 
 NVCC_FLAGS = [
     "-gencode", "arch=compute_103a,code=sm_103a",

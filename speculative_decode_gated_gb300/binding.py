@@ -31,7 +31,7 @@ EXPORTED = (
     "gdn_verify", "gdn_commit", "gdn_verify_commit_fused",
     "gdn_verify_layers", "gdn_commit_layers", "gdn_verify_commit_fused_layers",
     "gdn_accept_prefix", "gdn_replay_verify", "gdn_replay_commit", "gdn_commit_verify",
-    "gdn_read_device_error",
+    "gdn_read_device_error", "gdn_selftest_wait_timeout",
     "gdn_select_algo", "gdn_status_string", "gdn_last_error_string", "gdn_version",
 )
 
@@ -105,12 +105,14 @@ def lib() -> ctypes.CDLL:
         h.gdn_replay_commit.argtypes = [P, R, S, S]
         h.gdn_commit_verify.argtypes = [P, ctypes.POINTER(gdn_prev_step), S, S, S]
         h.gdn_read_device_error.argtypes = [P, S, ctypes.POINTER(ctypes.c_int32)]
+        h.gdn_selftest_wait_timeout.argtypes = [S, S]
         h.gdn_select_algo.argtypes = [P]
         h.gdn_status_string.argtypes = [ctypes.c_int]
         for name in ("gdn_verify", "gdn_commit", "gdn_verify_commit_fused",
                      "gdn_verify_layers", "gdn_commit_layers", "gdn_verify_commit_fused_layers",
                      "gdn_accept_prefix", "gdn_replay_verify", "gdn_replay_commit",
-                     "gdn_commit_verify", "gdn_read_device_error", "gdn_select_algo"):
+                     "gdn_commit_verify", "gdn_read_device_error", "gdn_selftest_wait_timeout",
+                     "gdn_select_algo"):
             getattr(h, name).restype = ctypes.c_int
         for name in ("gdn_status_string", "gdn_last_error_string", "gdn_version"):
             getattr(h, name).restype = ctypes.c_char_p
@@ -281,6 +283,14 @@ def gdn_accept_prefix(draft_ids: torch.Tensor, target_ids: torch.Tensor, accepte
                                  _ptr(draft_ids), _ptr(target_ids), _ptr(accepted), _ptr(dev_err),
                                  _stream(stream))
     _raise(st, "gdn_accept_prefix")
+
+
+def gdn_selftest_wait_timeout(dev_err: torch.Tensor, stream=None) -> None:
+    """Runs the kernels' bounded wait on a barrier nothing completes: about two
+    seconds later GDN_DEVERR_TIMEOUT is ORed into dev_err (int32, one element)."""
+    _check(dev_err, "dev_err", (torch.int32,), dev_err.device)
+    st = lib().gdn_selftest_wait_timeout(_ptr(dev_err), _stream(stream))
+    _raise(st, "gdn_selftest_wait_timeout")
 
 
 class Replay:

@@ -434,6 +434,17 @@ gdn_status gdn_accept_prefix(int32_t batch, int32_t max_T, const int32_t *cu_seq
     return GDN_OK;
 }
 
+gdn_status gdn_selftest_wait_timeout(int32_t *dev_err, cudaStream_t stream) {
+    if (!dev_err) return GDN_ERR_NULL_PTR;
+    if (!aligned4(dev_err)) return GDN_ERR_ALIGN;
+    const cudaError_t e = gdn::launch_wait_selftest(dev_err, stream);
+    if (e != cudaSuccess) {
+        set_cuda_error(e, "kernel launch");
+        return GDN_ERR_CUDA;
+    }
+    return GDN_OK;
+}
+
 gdn_status gdn_read_device_error(const gdn_problem *p, cudaStream_t stream, int32_t *host_code) {
     if (!p || !host_code) return GDN_ERR_NULL_PTR;
     *host_code = 0;

@@ -59,6 +59,7 @@
 
 #include "gdn_device.cuh"
 #include "gdn_launch.h"
+#include "gdn_wait.cuh"
 
 namespace gdn {
 namespace {
@@ -70,7 +71,6 @@ constexpr uint32_t kBoxBytes = 32 * D * 4;        // tile box: 32 value columns 
 constexpr uint32_t kTileBytes = 4 * kBoxBytes;    // 64 KiB
 constexpr uint32_t kTokHalfBytes = CT * 64 * 2;   // token box: 64 of 128 bf16 x 16 tokens
 constexpr uint32_t kTokBytes = 2 * kTokHalfBytes; // one [16][128] bf16 tile
-constexpr unsigned long long kWaitNs = 2000000000ull;
 
 // Token tiles of one step, 1024-byte aligned, each a swizzled [16][128] bf16
 // tile in two halves of 64 columns (one TMA box each).  The q and k halves of
@@ -122,46 +122,9 @@ __device__ __forceinline__ uint32_t smem_u32(const void *p) {
     return (uint32_t)__cvta_generic_to_shared(p);
 }
 
-__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
-    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;\n" ::"r"(bar), "r"(count) : "memory");
-}
-
 __device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes) {
     asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;\n" ::"r"(bar), "r"(bytes)
                  : "memory");
-}
-
-__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
-    uint32_t ok;
-    asm volatile(
-        "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
-        " selp.u32 %0, 1, 0, p;\n}\n"
-        : "=r"(ok)
-        : "r"(bar), "r"(parity)
-        : "memory");
-    return ok != 0;
-}
-
-__device__ __forceinline__ unsigned long long globaltimer() {
-    unsigned long long t;
-    asm volatile("mov.u64 %0, %globaltimer;" : "=l"(t));
-    return t;
-}
-
-// Waits for the phase of `bar` with parity `parity` to complete; false after ~2 s.
-__device__ __noinline__ bool wait_parity(uint32_t bar, uint32_t parity) {
-    unsigned long long t0 = 0;
-    for (uint32_t it = 1;; ++it) {
-        if (mbar_try_wait(bar, parity)) return true;
-        if ((it & 63) == 0) {
-            const unsigned long long now = globaltimer();
-            if (t0 == 0) {
-                t0 = now;
-            } else if (now - t0 > kWaitNs) {
-                return false;
-            }
-        }
-    }
 }
 
 __device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap *map, int c0, int c1,

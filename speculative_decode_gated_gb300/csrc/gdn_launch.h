@@ -24,4 +24,8 @@ cudaError_t launch_accept(int B, int max_T, const int32_t *cu_seqlens, long long
                           const int32_t *draft, const int32_t *target, int32_t *accepted,
                           int32_t *dev_err, cudaStream_t stream);
 
+// One block that waits on a barrier nothing completes, until the bounded wait
+// gives up; ORs GDN_DEVERR_TIMEOUT into *dev_err (not NULL).
+cudaError_t launch_wait_selftest(int32_t *dev_err, cudaStream_t stream);
+
 }  // namespace gdn

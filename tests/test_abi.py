@@ -236,6 +236,12 @@ def test_accept_prefix_validation(lib):
     assert call_accept(lib, err=ACC_PTR + 4) == 8              # accepted over the error word
 
 
+def test_selftest_wait_timeout_validation(lib):
+    # Both checks return before any CUDA call (no GPU here).
+    assert lib.gdn_selftest_wait_timeout(None, None) == 1
+    assert lib.gdn_selftest_wait_timeout((1 << 40) + 2, None) == 7
+
+
 
 # ---------------------------------------------------------------- replay buffer
 
