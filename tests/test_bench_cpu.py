@@ -1,0 +1,84 @@
+"""Host-side pieces of the benchmark on CPU: the reference arm's JSON line
+(the oracle timed on the host cores) and the clock-sample parser that decides
+whether a timed region saw a throttle reason."""
+import json
+import os
+import subprocess
+import sys
+import tempfile
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+sys.path.insert(0, ROOT)
+
+import bench  # noqa: E402
+
+CONTRACT_KEYS = ("metric", "value", "unit", "n_gpus", "steps", "warmup", "ms_per_step",
+                 "higher_is_better", "scaling", "vs_baseline", "dtype", "data", "config",
+                 "cpu_baseline", "e2e")
+
+
+def test_reference_arm_prints_one_contract_line():
+    env = dict(os.environ, RANK="0", WORLD_SIZE="1", LOCAL_RANK="0")
+    res = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference",
+                          "--steps", "1", "--warmup", "3", "--ref-units", "4"], env=env,
+                         capture_output=True, text=True, timeout=600)
+    assert res.returncode == 0, res.stderr
+    lines = [l for l in res.stdout.splitlines() if l.strip()]
+    assert len(lines) == 1
+    line = json.loads(lines[0])
+    for key in CONTRACT_KEYS:
+        assert key in line, key
+    assert line["impl"] == "reference"
+    assert line["metric"] == bench.METRIC and line["unit"] == bench.UNIT
+    assert line["higher_is_better"] is False
+    assert line["value"] > 0 and line["steps"] == 1 and line["warmup"] == 3
+    assert line["config"]["workload"] == bench.WORKLOAD
+    cpu = line["cpu_baseline"]
+    assert cpu["kind"] == "oracle" and cpu["cores"] >= 1 and cpu["value"] == line["value"]
+    assert "4 of" in cpu["sample"]
+    assert line["e2e"] == {"value": line["value"], "unit": line["unit"],
+                           "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}
+
+
+class _DoneProc:
+    def terminate(self):
+        pass
+
+    def wait(self, timeout=None):
+        return 0
+
+
+def _parse(rows):
+    s = bench.ClockSampler(0)
+    s.proc = _DoneProc()
+    s.file = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+    s.file.write("\n".join(rows) + "\n")
+    return s.stop()
+
+
+def test_clock_samples_without_throttle():
+    rows = [f"0, {mhz}, 2070, 900.5, 0x0000000000000000, Not Active, Not Active, Not Active, "
+            f"Not Active" for mhz in (2070, 2055, 2070)]
+    got = _parse(rows)
+    assert got["sm_mhz"] == 2070 and got["sm_max_mhz"] == 2070
+    assert got["reasons"] == [] and got["samples"] == 3
+    assert got["power_w_max"] == 900.5
+
+
+def test_clock_samples_report_each_active_reason_once():
+    rows = [
+        "0, 1980, 2070, 1390.0, 0x4, Not Active, Not Active, Not Active, Active",
+        "0, 1500, 2070, 1200.0, 0x48, Not Active, Active, Not Active, Active",
+        "0, 2070, 2070, 800.0, 0x0, Not Active, Not Active, Not Active, Not Active",
+        "garbage line",
+        "0, [N/A], 2070, 800.0, 0x0, Not Active, Not Active, Not Active, Not Active",
+    ]
+    got = _parse(rows)
+    assert got["samples"] == 3
+    assert got["reasons"] == ["hw_thermal_slowdown", "sw_power_cap"]
+    assert got["sm_mhz"] == 1980
+
+
+def test_clock_sampler_without_nvidia_smi_reports_nothing():
+    s = bench.ClockSampler(0)
+    assert s.stop() is None
