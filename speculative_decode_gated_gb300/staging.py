@@ -101,6 +101,9 @@ class DeviceProblem:
             st = fn()
             if st != binding.GDN_OK:
                 raise binding.GdnError(st, f"gdn {mode}")
+        # The raw addresses above stay valid only while their tensors (and the
+        # C problem) do: the callable keeps this object alive.
+        call.keep = (self, self.c)
         return call
 
 
@@ -133,7 +136,7 @@ def layers_launcher(dps, mode: str, stream):
         st = fn()
         if st != binding.GDN_OK:
             raise binding.GdnError(st, f"gdn {mode} layers")
-    call.keep = (arr, o)
+    call.keep = (list(dps), arr, o)  # the owners of the raw addresses above
     return call
 
 
@@ -205,6 +208,7 @@ def replay_launcher(d: DeviceProblem, r: DeviceReplay, mode: str, stream):
         st = fn()
         if st != binding.GDN_OK:
             raise binding.GdnError(st, f"gdn replay {mode}")
+    call.keep = (d, d.c, r, r.c)  # the owners of the raw addresses above
     return call
 
 
@@ -225,4 +229,5 @@ def commit_verify_launcher(d: DeviceProblem, prevs, ws, stream):
         st = lib.gdn_commit_verify(ref, pref, o, w, s)
         if st != binding.GDN_OK:
             raise binding.GdnError(st, "gdn_commit_verify")
+    call.keep = (d, d.c, prevs, ws)  # the owners of the raw addresses above
     return call
