@@ -17,7 +17,10 @@ step = for every layer: gdn_verify then gdn_commit.  Every step touches about
 --impl reference times the float64 CPU oracle on a bounded sample of the same
 workload (the slow reference this path is checked against).  Under torchrun
 (N > 1) every rank runs its own replica of the workload (weak scaling; no data
-is exchanged); the step time is the maximum over ranks.
+is exchanged); the step time is the maximum over ranks, and `value` is the
+whole job's microseconds per layer-call: that time over the layer-calls of all
+ranks (so it falls as N grows).  The HBM fractions are then taken against N
+GPUs' peak; the roofline entry stays the dominant kernel on one GPU.
 """
 from __future__ import annotations
 
@@ -223,6 +226,13 @@ def max_over_ranks(value: float, world: int, device=None) -> float:
     return float(t.item())
 
 
+def job_us_per_layer_call(ms_total: float, steps: int, layers: int, world: int) -> float:
+    """The whole job's microseconds per layer-call: the slowest rank's time for
+    `steps` steps, over the layer-calls of all `world` ranks (each rank runs
+    `layers` layer-calls per step on its own replica)."""
+    return ms_total * 1e3 / (steps * layers * world)
+
+
 # ----------------------------------------------------------------- arms
 
 def run_reference(args, rank):
@@ -392,7 +402,7 @@ def run_ours(args, rank, world, local_rank):
     clk = clocks.stop()
     ms_total = max_over_ranks(t_start.elapsed_time(t_end), world, dev)
     ms_step = ms_total / args.steps
-    us_call = ms_step * 1e3 / L
+    us_call = job_us_per_layer_call(ms_total, args.steps, L, world)
 
     avg_ms = {m: statistics.fmean(a.elapsed_time(b) for a, b in events[m]) for m in kinds}
     dominant = max(kinds, key=lambda m: avg_ms[m] * n_per_step[m])
@@ -404,7 +414,7 @@ def run_ours(args, rank, world, local_rank):
             .get(algo_used, "gdn_recurrent") + "_" + MODE_NAME[dominant])
     traffic = profile_traffic(ktag, name)
 
-    e2e = (run_e2e(args, dps, stream, dev, fused)
+    e2e = (run_e2e(args, dps, stream, dev, fused, world)
            if not (args.no_e2e or batched or args.replay or args.order == "lagged") else None)
 
     cpu = None
@@ -422,7 +432,7 @@ def run_ours(args, rank, world, local_rank):
                           f"scaled to a full layer-call"}
 
     if rank == 0:
-        gbs = bytes_call / (us_call * 1e-6) / 1e9
+        gbs = bytes_call / (us_call * 1e-6) / 1e9  # the whole job's GB/s
         line = {
             "metric": METRIC, "value": us_call, "unit": UNIT, "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step,
@@ -454,8 +464,8 @@ def run_ours(args, rank, world, local_rank):
                              if args.with_accept else "given (device array)"),
             },
             "achieved_gbs": gbs,
-            "frac_of_8tbs": gbs / NOMINAL_HBM_GBS,
-            "frac_of_measured_hbm": gbs / peak,
+            "frac_of_8tbs": gbs / (NOMINAL_HBM_GBS * world),
+            "frac_of_measured_hbm": gbs / (peak * world),
             "alg_bytes_per_layer_call": bytes_call,
             "kernel_us": {MODE_NAME[m]: avg_ms[m] * 1e3 for m in kinds},
             "roofline": {"bound": "hbm", "kernel": ktag, "achieved": achieved, "peak": peak,
@@ -469,10 +479,11 @@ def run_ours(args, rank, world, local_rank):
         print(json.dumps(line), flush=True)
 
 
-def run_e2e(args, dps, stream, dev, fused):
+def run_e2e(args, dps, stream, dev, fused, world=1):
     """Same metric end to end: every step copies each layer's q/k/v/gates/accepted
     from pinned host memory and reads every layer's o back, overlapped on copy
-    streams with the kernels of other layers."""
+    streams with the kernels of other layers.  With N ranks, the slowest rank's
+    time over all ranks' layer-calls, and the copied bytes of all ranks."""
     import torch
 
     # Each layer's inputs live in one device buffer (q, k, v, alpha, beta and the
@@ -538,9 +549,10 @@ def run_e2e(args, dps, stream, dev, fused):
     for _ in range(args.e2e_steps):
         one_step()
     torch.cuda.synchronize()
-    dt = time.perf_counter() - t0
-    return {"value": dt / args.e2e_steps * 1e6 / L, "unit": UNIT,
-            "h2d_bytes_per_step": bi, "d2h_bytes_per_step": bo, "steps": args.e2e_steps}
+    dt = max_over_ranks(time.perf_counter() - t0, world, dev)
+    return {"value": job_us_per_layer_call(dt * 1e3, args.e2e_steps, L, world), "unit": UNIT,
+            "h2d_bytes_per_step": bi * world, "d2h_bytes_per_step": bo * world,
+            "steps": args.e2e_steps}
 
 
 def main():

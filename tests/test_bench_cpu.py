@@ -7,6 +7,8 @@ import subprocess
 import sys
 import tempfile
 
+import pytest
+
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 sys.path.insert(0, ROOT)
 
@@ -38,6 +40,15 @@ def test_reference_arm_prints_one_contract_line():
     assert "4 of" in cpu["sample"]
     assert line["e2e"] == {"value": line["value"], "unit": line["unit"],
                            "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}
+
+
+def test_job_value_is_the_whole_jobs_time_per_layer_call():
+    # one rank: 300 steps of 24 layer-calls in 620 ms
+    assert bench.job_us_per_layer_call(620.0, 300, 24, 1) == pytest.approx(620e3 / 7200)
+    # weak scaling: each of 4 ranks does the same work in the same time, so the
+    # job does four times the layer-calls per microsecond
+    one = bench.job_us_per_layer_call(620.0, 300, 24, 1)
+    assert bench.job_us_per_layer_call(620.0, 300, 24, 4) == pytest.approx(one / 4)
 
 
 class _DoneProc:
