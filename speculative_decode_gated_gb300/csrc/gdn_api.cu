@@ -79,7 +79,8 @@ bool shape_ok(const gdn_problem *p) {
 }
 
 // Which kernel AUTO picks.  The chunked tensor-core kernel covers bf16 q/k/v at
-// dk = dv = 128 with up to 16 tokens per request; the recurrent kernel the rest.
+// dk = dv = 128 and any draft length (16-token chunks chained through the state);
+// the recurrent kernel the rest.
 int resolve_algo(const gdn_problem *p) {
     // The chunked kernel also needs at least one token row (ragged input may have none).
     const bool chunk_ok = gdn::chunk_supported(p->qkv_dtype == GDN_BF16, p->dk, p->dv, p->max_T) &&
