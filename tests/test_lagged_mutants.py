@@ -25,7 +25,13 @@ MUTANTS = {
 
 
 def run_pins():
-    checks = [pins.test_chain_equals_one_run_over_the_accepted_rows,
+    def chain_short():
+        pins.test_chain_equals_one_run_over_the_accepted_rows(pins.SHORT)
+
+    def chain_long():
+        pins.test_chain_equals_one_run_over_the_accepted_rows(pins.LONG)
+
+    checks = [chain_short, chain_long,
               pins.test_first_step_commits_nothing, pins.test_nothing_accepted_is_a_plain_verify]
     failed = []
     for check in checks:

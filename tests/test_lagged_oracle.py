@@ -56,9 +56,14 @@ class Concat:
         self.s0 = s0
 
 
-def chain(seed=3):
-    lens = [[5, 1, 4], [3, 6, 2], [4, 4, 6]]
-    accs = [[2, 0, 4], [3, 1, 0], [0, 4, 6]]
+SHORT = ([[5, 1, 4], [3, 6, 2], [4, 4, 6]], [[2, 0, 4], [3, 1, 0], [0, 4, 6]])
+# drafts longer than one 16-row chunk: commit points inside a chunk, on a
+# chunk boundary (16, 32) and at the full length
+LONG = ([[40, 17, 33], [16, 35, 20], [32, 9, 48]], [[37, 0, 16], [16, 35, 3], [32, 9, 0]])
+
+
+def chain(seed=3, lens_accs=SHORT):
+    lens, accs = lens_accs
     steps = [step(seed, i, l, a) for i, (l, a) in enumerate(zip(lens, accs))]
     rng = np.random.default_rng(11)
     p0 = steps[0]
@@ -66,8 +71,9 @@ def chain(seed=3):
     return steps, pool
 
 
-def test_chain_equals_one_run_over_the_accepted_rows():
-    steps, pool0 = chain()
+@pytest.mark.parametrize("lens_accs", [SHORT, LONG], ids=["short", "multichunk"])
+def test_chain_equals_one_run_over_the_accepted_rows(lens_accs):
+    steps, pool0 = chain(lens_accs=lens_accs)
     p0 = steps[0]
     s0 = oracle.gather_s0(pool0, p0.slot_ids, p0.heads).reshape(p0.batch, p0.heads, p0.dk, p0.dv)
     pool, prev = pool0, None
