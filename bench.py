@@ -236,30 +236,165 @@ def job_us_per_layer_call(ms_total: float, steps: int, layers: int, world: int) 
 # ----------------------------------------------------------------- arms
 
 def run_reference(args, rank):
+    """The oracle on the host cores.  A step is one bounded sample: verify and
+    commit passes over `--ref-units` units of layer 0.  `ms_per_step` is the wall
+    time of that sample as it ran; `value` scales it to a whole layer-call
+    (units of a layer-call / units of the sample)."""
     if rank != 0:
         return
     prob = inputs.make_problem(args.workload, layer=0)
     threads = os.cpu_count() or 1
     for _ in range(args.warmup):
         cpu_oracle_time(prob, args.ref_units, threads)
-    times = []
+    times, walls = [], []
+    n = 0
     for _ in range(args.steps):
-        _, us, n = cpu_oracle_time(prob, args.ref_units, threads)
+        dt, us, n = cpu_oracle_time(prob, args.ref_units, threads)
         times.append(us)
+        walls.append(dt)
     value = statistics.median(times)
-    sample = (f"{args.ref_units} of {prob.units} units of layer 0 per step "
-              f"(verify pass + commit pass), scaled to a full layer-call")
+    scale = prob.units / n
+    sample = (f"{n} of {prob.units} units of layer 0 per step (verify pass + commit pass), "
+              f"{statistics.median(walls):.2f} s wall per step, scaled by {scale:g} "
+              f"to a full layer-call")
     line = {
         "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT,
         "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
-        "ms_per_step": value / 1e3, "higher_is_better": False, "scaling": "weak",
-        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": args.workload, "order": "verify then commit per layer"},
+        "ms_per_step": statistics.fmean(walls) * 1e3, "higher_is_better": False,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": args.workload, "order": "verify then commit per layer",
+                   "step": f"{n} sampled units (ms_per_step is their wall time)",
+                   "value_scale": scale},
         "cpu_baseline": {"value": value, "unit": UNIT, "cores": threads, "kind": "oracle",
                          "sample": sample},
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
+
+
+# ----------------------------------------------------------------- timing
+
+def time_calls(calls, kinds, stream, steps, warmup, world, dev, check=()):
+    """Warm up, then two timed regions of `steps` steps each (a step issues every
+    call of `calls` once, in order, on `stream`):
+      1. one event pair around all steps, launches back to back as in use
+         (the headline figure);
+      2. an event pair around every launch, for the per-kernel durations.
+    Returns the slowest rank's region-1 milliseconds, the mean milliseconds of
+    each call kind in region 2 and the calls of each kind per step."""
+    import torch
+    import torch.distributed as dist
+
+    from speculative_decode_gated_gb300 import binding
+
+    def barrier():
+        if world > 1:
+            dist.barrier()
+
+    def step(events=None):
+        if events is None:
+            for _, call in calls:
+                call()
+            return
+        for m, call in calls:
+            a, b = events[m][events["i"][m]]
+            a.record(stream)
+            call()
+            b.record(stream)
+            events["i"][m] += 1
+
+    for _ in range(warmup):
+        step()
+    torch.cuda.synchronize()
+    for d in check:
+        if binding.gdn_read_device_error(d.c) != 0:
+            raise RuntimeError("device-side argument error during warm-up")
+    n_per_step = {m: sum(1 for mm, _ in calls if mm == m) for m in kinds}
+    events = {m: [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                  for _ in range(n_per_step[m] * steps)] for m in kinds}
+    events["i"] = {m: 0 for m in kinds}
+    barrier()
+    torch.cuda.synchronize()
+    t_start = torch.cuda.Event(enable_timing=True)
+    t_end = torch.cuda.Event(enable_timing=True)
+    t_start.record(stream)
+    for _ in range(steps):
+        step()
+    t_end.record(stream)
+    torch.cuda.synchronize()
+    barrier()
+    for _ in range(steps):
+        step(events)
+    torch.cuda.synchronize()
+    barrier()
+    ms_total = max_over_ranks(t_start.elapsed_time(t_end), world, dev)
+    avg_ms = {m: statistics.fmean(a.elapsed_time(b) for a, b in events[m]) for m in kinds}
+    return ms_total, avg_ms, n_per_step
+
+
+# The other target workloads, timed in the same run as the headline: name,
+# call order, independent instances cycled through (each with its own pool and
+# inputs), and why.
+PER_CONFIG = [
+    ("b32_h32_d128_t16", "engine", 8,
+     "8 instances (own pools and tokens); all verifies, then all commits, so that no "
+     "commit re-reads in L2 a checkpoint its verify just read (one instance's "
+     "checkpoints, 64 MiB, would fit in the 129 MB L2)"),
+    ("b128_h32_d128_ragged16", "fused", 2,
+     "2 instances alternating, fused verify+commit per call (541 MB per call)"),
+]
+
+
+def run_per_config(args, dev, stream, world):
+    """The b32 (verify+commit) and b128 ragged (fused) workloads, each timed like
+    the headline: one event pair around back-to-back steps, and bracketed launches
+    for the dominant kernel's roofline fraction."""
+    import torch
+
+    from speculative_decode_gated_gb300 import binding, staging
+
+    peak, peak_kind = measured_peaks()
+    out = {}
+    for name, order, n_inst, why in PER_CONFIG:
+        probs = [inputs.make_problem(name, layer=l) for l in range(n_inst)]
+        p0 = probs[0]
+        pool = staging.new_pool(p0.pool_slots, p0.heads, p0.dk, p0.dv, dev, fill="zero",
+                                layers=n_inst)
+        dps = [staging.DeviceProblem(pr, dev, pool=pool[l], algo=args.algo)
+               for l, pr in enumerate(probs)]
+        if order == "fused":
+            kinds = ["f"]
+            calls = [("f", d.launcher("fused", stream)) for d in dps]
+        else:
+            kinds = ["v", "c"]
+            calls = ([("v", d.launcher("verify", stream)) for d in dps]
+                     + [("c", d.launcher("commit", stream)) for d in dps])
+        bytes_of = {m: [alg_bytes(pr, MODE_NAME[m]) for pr in probs] for m in kinds}
+        ms_total, avg_ms, n_per_step = time_calls(calls, kinds, stream, args.per_config_steps,
+                                                  args.warmup, world, dev, check=dps)
+        us_call = job_us_per_layer_call(ms_total, args.per_config_steps, n_inst, world)
+        bytes_call = sum(sum(bytes_of[m]) for m in kinds) / n_inst
+        gbs = bytes_call / (us_call * 1e-6) / 1e9
+        dominant = max(kinds, key=lambda m: avg_ms[m] * n_per_step[m])
+        per_launch = sum(bytes_of[dominant]) / len(bytes_of[dominant])
+        achieved = per_launch / (avg_ms[dominant] * 1e-3) / 1e9
+        out[name] = {
+            "order": why,
+            "us_per_layer_call": us_call,
+            "alg_bytes_per_layer_call": bytes_call,
+            "achieved_gbs": gbs,
+            "frac_of_measured_hbm": gbs / (peak * world),
+            "frac_of_8tbs": gbs / (NOMINAL_HBM_GBS * world),
+            "meets_70pct_of_8tbs": gbs >= 0.7 * NOMINAL_HBM_GBS * world,
+            "kernel_us": {MODE_NAME[m]: avg_ms[m] * 1e3 for m in kinds},
+            "dominant": {"kernel": MODE_NAME[dominant], "achieved_gbs": achieved,
+                         "frac": achieved / peak, "peak_source": peak_kind},
+            "steps": args.per_config_steps,
+        }
+        del calls, dps, pool
+        torch.cuda.synchronize()
+        torch.cuda.empty_cache()
+    return out
 
 
 def run_ours(args, rank, world, local_rank):
@@ -351,60 +486,15 @@ def run_ours(args, rank, world, local_rank):
         bytes_of["a"] = [2 * 4 * p0.n_tok + 4 * p0.batch + (4 * (p0.batch + 1) if p0.ragged else 0)]
     bytes_call = sum(sum(bytes_of[m]) for m in kinds) / L
 
-    def step(events=None):
-        if events is None:
-            for _, call in calls:
-                call()
-            return
-        for m, call in calls:
-            a, b = events[m][events["i"][m]]
-            a.record(stream)
-            call()
-            b.record(stream)
-            events["i"][m] += 1
-
-    for _ in range(args.warmup):
-        step()
-    torch.cuda.synchronize()
-    for d in dps:
-        if binding.gdn_read_device_error(d.c) != 0:
-            raise RuntimeError("device-side argument error during warm-up")
-
-    def barrier():
-        if world > 1:
-            dist.barrier()
-
-    n_per_step = {m: sum(1 for mm, _ in calls if mm == m) for m in kinds}
-    events = {m: [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-                  for _ in range(n_per_step[m] * args.steps)] for m in kinds}
-    events["i"] = {m: 0 for m in kinds}
     clocks = ClockSampler(local_rank)
     clocks.start()
     time.sleep(0.3)
-    # Timed region 1 (the headline): K steps, events only at its two ends, so
-    # consecutive launches overlap as they would in use.
-    barrier()
-    torch.cuda.synchronize()
-    t_start = torch.cuda.Event(enable_timing=True)
-    t_end = torch.cuda.Event(enable_timing=True)
-    t_start.record(stream)
-    for _ in range(args.steps):
-        step()
-    t_end.record(stream)
-    torch.cuda.synchronize()
-    barrier()
-    # Timed region 2: the same K steps with an event pair around every launch,
-    # for the per-kernel durations of the roofline.
-    for _ in range(args.steps):
-        step(events)
-    torch.cuda.synchronize()
-    barrier()
+    ms_total, avg_ms, n_per_step = time_calls(calls, kinds, stream, args.steps, args.warmup,
+                                              world, dev, check=dps)
     clk = clocks.stop()
-    ms_total = max_over_ranks(t_start.elapsed_time(t_end), world, dev)
     ms_step = ms_total / args.steps
     us_call = job_us_per_layer_call(ms_total, args.steps, L, world)
 
-    avg_ms = {m: statistics.fmean(a.elapsed_time(b) for a, b in events[m]) for m in kinds}
     dominant = max(kinds, key=lambda m: avg_ms[m] * n_per_step[m])
     per_launch_bytes = {m: sum(bytes_of[m]) / len(bytes_of[m]) for m in kinds}
     peak, peak_kind = measured_peaks()
@@ -416,6 +506,10 @@ def run_ours(args, rank, world, local_rank):
 
     e2e = (run_e2e(args, dps, stream, dev, fused, world)
            if not (args.no_e2e or batched or args.replay or args.order == "lagged") else None)
+    per_config = None
+    if not (args.no_per_config or args.replay or args.draft or args.layers or batched
+            or args.order != "interleaved" or args.workload != WORKLOAD):
+        per_config = run_per_config(args, dev, stream, world)
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline and not args.replay:
@@ -474,6 +568,7 @@ def run_ours(args, rank, world, local_rank):
             "gpu_launches": args.steps * len(calls),  # in timed region 1
             "clocks": clk,
             "e2e": e2e,
+            "per_config": per_config,
             "cpu_baseline": cpu,
         }
         print(json.dumps(line), flush=True)
@@ -550,9 +645,32 @@ def run_e2e(args, dps, stream, dev, fused, world=1):
         one_step()
     torch.cuda.synchronize()
     dt = max_over_ranks(time.perf_counter() - t0, world, dev)
+
+    # The host link's floor for the same bytes: the same copies, both directions
+    # at once on the two copy streams, with no kernel running.
+    def copies_only():
+        for l, d in enumerate(dps):
+            with torch.cuda.stream(h2d):
+                dev_in[l].copy_(host_in[l], non_blocking=True)
+            with torch.cuda.stream(d2h):
+                host_o[l].copy_(d.o, non_blocking=True)
+
+    copies_only()
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    for _ in range(args.e2e_steps):
+        copies_only()
+    torch.cuda.synchronize()
+    dt_copy = max_over_ranks(time.perf_counter() - t0, world, dev)
+    floor = job_us_per_layer_call(dt_copy * 1e3, args.e2e_steps, L, world)
     return {"value": job_us_per_layer_call(dt * 1e3, args.e2e_steps, L, world), "unit": UNIT,
             "h2d_bytes_per_step": bi * world, "d2h_bytes_per_step": bo * world,
-            "steps": args.e2e_steps}
+            "steps": args.e2e_steps,
+            "copy_floor": {"value": floor, "unit": UNIT,
+                           "link_gbs": (bi + bo) / (dt_copy / args.e2e_steps) / 1e9,
+                           "how": "the same host<->device copies alone, both directions at "
+                                  "once, no kernels: the host link bounds the end-to-end "
+                                  "figure from below"}}
 
 
 def main():
@@ -586,6 +704,9 @@ def main():
     ap.add_argument("--batch-layers", action="store_true",
                     help="all layers' commits (or fused calls) in one layer-batch launch")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-per-config", action="store_true",
+                    help="skip the b32 and b128 ragged workloads timed after the headline")
+    ap.add_argument("--per-config-steps", type=int, default=200)
     args = ap.parse_args()
     if args.mode is None:
         args.mode = "fused" if "ragged" in args.workload else "separate"

@@ -78,7 +78,8 @@ extern "C" {
 typedef enum gdn_status {
     GDN_OK = 0,
     GDN_ERR_NULL_PTR = 1,     /* a required pointer is NULL */
-    GDN_ERR_BAD_DIM = 2,      /* batch/heads/max_T/pool_slots/n_tok out of range, or unknown flags */
+    GDN_ERR_BAD_DIM = 2,      /* batch/heads/max_T/pool_slots/n_tok out of range (token rows,
+                                 batch*max_T or n_tok, above 2^31 - 1), or unknown flags */
     GDN_ERR_BAD_DTYPE = 3,    /* qkv_dtype is not a gdn_dtype */
     GDN_ERR_UNSUPPORTED = 4,  /* dk/dv (or a forced algo) not supported */
     GDN_ERR_DEVICE_ARG = 5,   /* reported by gdn_read_device_error only */
@@ -113,7 +114,12 @@ typedef enum gdn_algo {
 #define GDN_DEVERR_SLOT     1   /* slot_ids[r] outside [0, pool_slots) */
 #define GDN_DEVERR_ACCEPTED 2   /* accepted[r] outside [0, T_r]        */
 #define GDN_DEVERR_SEQLEN   4   /* cu[r+1] - cu[r] outside [0, max_T], or rows outside [0, n_tok) */
-#define GDN_DEVERR_TIMEOUT  8   /* an internal pipeline wait gave up (about 2 s); results incomplete */
+#define GDN_DEVERR_TIMEOUT  8   /* an internal pipeline wait gave up (about 2 s); results incomplete.
+                                   The block that gave up also bounds its wait for its own
+                                   copies in flight; if that wait gives up too, copies (or, on
+                                   the tcgen05 kernel, products) may still land after the kernel
+                                   ends.  Treat every later result on the stream as suspect until
+                                   the CUDA context has been rebuilt. */
 #define GDN_DEVERR_REPLAY  16   /* replay buffer: len_in[slot] < 0, or buffered plus new rows > capacity */
 
 /* Variant bits of gdn_problem.flags (the same in every problem of a layer batch). */
@@ -135,7 +141,9 @@ typedef struct gdn_problem {
     int32_t algo;                /* gdn_algo */
     int32_t flags;               /* GDN_FLAG_* bits; all other bits must be 0 */
     const int32_t *cu_seqlens;   /* device [batch+1] token-row offsets, or NULL (uniform) */
-    const void *q;               /* device [N_tok][heads][dk], 16-byte aligned */
+    const void *q;               /* device [N_tok][heads][dk], 16-byte aligned; may be NULL for
+                                    the commit calls (gdn_commit, gdn_commit_layers,
+                                    gdn_replay_commit), which read no q */
     const void *k;               /* device [N_tok][heads][dk], 16-byte aligned */
     const void *v;               /* device [N_tok][heads][dv], 16-byte aligned */
     const float *alpha;          /* device [N_tok][heads]: alpha, or g = log(alpha) with GDN_FLAG_LOG_GATE */
@@ -256,8 +264,6 @@ GDN_API gdn_status gdn_replay_verify(const gdn_problem *p, const gdn_replay *rb,
 GDN_API gdn_status gdn_replay_commit(const gdn_problem *p, const gdn_replay *rb,
                                      const int32_t *accepted, cudaStream_t stream);
 
-/* Waits for `stream`, copies *p->dev_err to *host_code (0 when dev_err is NULL).
- * Returns GDN_ERR_DEVICE_ARG when the word is non-zero, GDN_OK when it is zero. */
 /* Commit the previous step, then verify the next one, in one pass over each
  * checkpoint (OCRia write-up, section "Make speculative verification
  * cheaper": rollback keeps the accepted prefix; in an engine the accepted
@@ -297,6 +303,8 @@ typedef struct gdn_prev_step {
 GDN_API gdn_status gdn_commit_verify(const gdn_problem *p, const gdn_prev_step *prev, void *o,
                                      float *w, cudaStream_t stream);
 
+/* Waits for `stream`, copies *p->dev_err to *host_code (0 when dev_err is NULL).
+ * Returns GDN_ERR_DEVICE_ARG when the word is non-zero, GDN_OK when it is zero. */
 GDN_API gdn_status gdn_read_device_error(const gdn_problem *p, cudaStream_t stream,
                                          int32_t *host_code);
 

@@ -24,9 +24,10 @@ struct Range {
     uintptr_t lo, hi;  // [lo, hi)
 };
 
+// An absent array (NULL) covers no bytes.
 Range range(const void *ptr, int64_t bytes) {
     const uintptr_t lo = reinterpret_cast<uintptr_t>(ptr);
-    return Range{lo, lo + (uintptr_t)(bytes > 0 ? bytes : 0)};
+    return Range{lo, ptr ? lo + (uintptr_t)(bytes > 0 ? bytes : 0) : lo};
 }
 
 bool overlap(Range a, Range b) {
@@ -106,8 +107,11 @@ gdn_status validate(const gdn_problem *p, bool with_o, const void *o, bool with_
     if (*empty) return GDN_OK;
     if (p->pool_slots < p->batch) return GDN_ERR_BAD_DIM;
     if (p->cu_seqlens && p->n_tok < 0) return GDN_ERR_BAD_DIM;
+    // Token rows are indexed with 32-bit ints on the device.
+    if (token_rows(p) > 0x7fffffffLL || kv_rows > 0x7fffffffLL) return GDN_ERR_BAD_DIM;
     if (!p->pool || !p->slot_ids) return GDN_ERR_NULL_PTR;
-    if (p->max_T > 0 && (!p->q || !p->k || !p->v || !p->alpha || !p->beta))
+    // q is read only by calls that produce outputs (a commit may pass NULL).
+    if (p->max_T > 0 && ((with_o && !p->q) || !p->k || !p->v || !p->alpha || !p->beta))
         return GDN_ERR_NULL_PTR;
     if (with_o && !o) return GDN_ERR_NULL_PTR;
     if (with_acc && !accepted) return GDN_ERR_NULL_PTR;

@@ -1543,7 +1543,8 @@ cudaError_t encode_layer(const Args &p, Maps *maps) {
         return cudaErrorInvalidValue;
     if (!encode_tokens(encode, &maps->k, p.k, p.H, p.kv_rows) ||
         !encode_tokens(encode, &maps->v, p.v, p.H, p.kv_rows) ||
-        !encode_tokens(encode, &maps->q, p.q, p.H, p.n_tok))
+        // A commit reads no q and may pass none: k stands in for the unused map.
+        !encode_tokens(encode, &maps->q, p.q ? p.q : p.k, p.H, p.q ? p.n_tok : p.kv_rows))
         return cudaErrorInvalidValue;
     if (p.p_k && !encode_tokens(encode, &maps->kp, p.p_k, p.H, p.p_ntok))  // the previous step's k
         return cudaErrorInvalidValue;

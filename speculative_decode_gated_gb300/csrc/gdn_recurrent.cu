@@ -71,21 +71,25 @@ __global__ void __launch_bounds__(kThreads) rec_kernel(const Args p) {
     for (int t0 = 0; t0 < T_run; t0 += kChunk) {
         const int n = min(kChunk, T_run - t0);
         __syncthreads();  // previous chunk fully consumed
-        // Stage q, k (n x DK), v (n x ncols), alpha, beta as float.
+        // Stage q (not for commit: it has no outputs), k (n x DK), v (n x ncols),
+        // alpha, beta as float.
         constexpr int VEC = BF16 ? 8 : 4;
         for (int e = tid * VEC; e < n * DK; e += nthr * VEC) {
             const int tt = e / DK, c = e - tt * DK;
             const size_t off = ((size_t)(u.row0 + t0 + tt) * p.H + h) * DK + c;
             if (BF16) {
-                const uint4 wq = *reinterpret_cast<const uint4 *>(
-                    reinterpret_cast<const __nv_bfloat16 *>(p.q) + off);
+                if (MODE != kCommit) {
+                    const uint4 wq = *reinterpret_cast<const uint4 *>(
+                        reinterpret_cast<const __nv_bfloat16 *>(p.q) + off);
+                    bf16x8_to_f32(wq, &sq[tt][c]);
+                }
                 const uint4 wk = *reinterpret_cast<const uint4 *>(
                     reinterpret_cast<const __nv_bfloat16 *>(p.k) + off);
-                bf16x8_to_f32(wq, &sq[tt][c]);
                 bf16x8_to_f32(wk, &sk[tt][c]);
             } else {
-                *reinterpret_cast<float4 *>(&sq[tt][c]) =
-                    *reinterpret_cast<const float4 *>(reinterpret_cast<const float *>(p.q) + off);
+                if (MODE != kCommit)
+                    *reinterpret_cast<float4 *>(&sq[tt][c]) =
+                        *reinterpret_cast<const float4 *>(reinterpret_cast<const float *>(p.q) + off);
                 *reinterpret_cast<float4 *>(&sk[tt][c]) =
                     *reinterpret_cast<const float4 *>(reinterpret_cast<const float *>(p.k) + off);
             }
@@ -109,8 +113,8 @@ __global__ void __launch_bounds__(kThreads) rec_kernel(const Args p) {
             sb[tid] = p.beta[x];
         }
         __syncthreads();
-        // k_t . q_t, one warp per token.
-        for (int tt = warp; tt < n; tt += nwarps) {
+        // k_t . q_t, one warp per token (outputs only).
+        for (int tt = warp; MODE != kCommit && tt < n; tt += nwarps) {
             float acc = 0.0f;
 #pragma unroll
             for (int i = lane; i < DK; i += 32) acc = fmaf(sk[tt][i], sq[tt][i], acc);
@@ -128,12 +132,12 @@ __global__ void __launch_bounds__(kThreads) rec_kernel(const Args p) {
 #pragma unroll
             for (int i = 0; i < R; i += 4) {
                 const float4 k4 = *reinterpret_cast<const float4 *>(&sk[tt][i0 + i]);
-                const float4 q4 = *reinterpret_cast<const float4 *>(&sq[tt][i0 + i]);
                 uu[0] = fmaf(k4.x, g[i + 0], uu[0]);
                 uu[1] = fmaf(k4.y, g[i + 1], uu[1]);
                 uu[2] = fmaf(k4.z, g[i + 2], uu[2]);
                 uu[3] = fmaf(k4.w, g[i + 3], uu[3]);
                 if (MODE != kCommit) {
+                    const float4 q4 = *reinterpret_cast<const float4 *>(&sq[tt][i0 + i]);
                     pp[0] = fmaf(q4.x, g[i + 0], pp[0]);
                     pp[1] = fmaf(q4.y, g[i + 1], pp[1]);
                     pp[2] = fmaf(q4.z, g[i + 2], pp[2]);

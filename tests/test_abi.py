@@ -100,13 +100,24 @@ def call(lib, fn, c, o=O_PTR, acc=ACC_PTR):
     (dict(dk=48), 4), (dict(dk=512), 4), (dict(dv=48), 4), (dict(dv=160), 4), (dict(algo=9), 4),
     (dict(algo=2, qkv_dtype=0), 4), (dict(algo=2, dk=64, dv=64), 4),
     (dict(algo=3, qkv_dtype=0), 4), (dict(algo=3, dk=64, dv=64), 4), (dict(algo=4), 4),
-    (dict(pool=None), 1), (dict(slot_ids=None), 1), (dict(q=None), 1), (dict(beta=None), 1),
+    (dict(pool=None), 1), (dict(slot_ids=None), 1), (dict(k=None), 1), (dict(beta=None), 1),
+    # token rows are 32-bit indices on the device
+    (dict(batch=1 << 21, max_T=1024, pool_slots=1 << 22), 2),
+    (dict(cu_seqlens=(1 << 40) + 11 * (1 << 32), n_tok=1 << 31), 2),
     (dict(q=(1 << 40) + 8), 7), (dict(pool=(1 << 40) + 5 * (1 << 32) + 4), 7),
     (dict(alpha=(1 << 40) + 3 * (1 << 32) + 2), 7),
     (dict(pool=1 << 40), 8),  # pool over q
 ])
 def test_host_validation_rejects(lib, fn, over, status):
     assert call(lib, fn, fake_problem(**over)) == status
+
+
+def test_q_is_required_only_with_outputs(lib):
+    # verify and fused read q; a commit reads none.  The misaligned pool stops the
+    # commit before any launch, after the pointer checks have passed.
+    assert call(lib, "verify", fake_problem(q=None)) == 1
+    assert call(lib, "fused", fake_problem(q=None)) == 1
+    assert call(lib, "commit", fake_problem(q=None, pool=(1 << 40) + 5 * (1 << 32) + 4)) == 7
 
 
 def test_output_checks(lib):

@@ -6,6 +6,7 @@ import os
 import subprocess
 import sys
 import tempfile
+import time
 
 import pytest
 
@@ -21,6 +22,7 @@ CONTRACT_KEYS = ("metric", "value", "unit", "n_gpus", "steps", "warmup", "ms_per
 
 def test_reference_arm_prints_one_contract_line():
     env = dict(os.environ, RANK="0", WORLD_SIZE="1", LOCAL_RANK="0")
+    t0 = time.perf_counter()
     res = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference",
                           "--steps", "1", "--warmup", "3", "--ref-units", "4"], env=env,
                          capture_output=True, text=True, timeout=600)
@@ -40,6 +42,12 @@ def test_reference_arm_prints_one_contract_line():
     assert "4 of" in cpu["sample"]
     assert line["e2e"] == {"value": line["value"], "unit": line["unit"],
                            "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}
+    # ms_per_step is the wall time of the sample that ran (it fits in the process's
+    # own run time); value is that sample scaled to a whole layer-call
+    wall_ms = (time.perf_counter() - t0) * 1e3
+    assert 0 < line["ms_per_step"] * line["steps"] < wall_ms
+    assert line["config"]["value_scale"] == pytest.approx(2048 / 4)
+    assert line["value"] > line["ms_per_step"] * 1e3
 
 
 def test_job_value_is_the_whole_jobs_time_per_layer_call():

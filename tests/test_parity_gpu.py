@@ -1,10 +1,10 @@
 """GPU parity: the CUDA path (through the C ABI) against the float64 oracle.
 
-Small problems are compared on every unit; the full-size workloads on a sample
-of units (always including the first and last unit, requests with a_r = 0 and
-a_r = T_r and the shortest ragged request), in the same launch configuration
-the benchmark times.  Bookkeeping (which pool slots change) is compared bitwise
-over the whole pool in every case.
+Every unit is compared, small problems and the full-size workloads alike (the
+b32 and b128 ragged workloads, and the first and last layer of the 24-layer
+one), in the same launch configuration the benchmark times.  Bookkeeping
+(which pool slots change) is compared bitwise over the whole pool in every
+case.
 """
 import ctypes
 
@@ -124,25 +124,31 @@ def test_small_parity(name, algo, mode):
 FULL = ["b32_h32_d128_t16", "b64_h32_d128_t16_x24", "b128_h32_d128_ragged16"]
 
 
-@pytest.mark.parametrize("name", FULL)
-@pytest.mark.parametrize("mode", ["separate", "fused"])
-@pytest.mark.parametrize("algo", [AUTO, TC], ids=["auto", "tc"])
-def test_full_size_sampled(name, mode, algo):
-    layers = [0, 23] if name.endswith("x24") else [0]
-    for layer in layers:
-        prob = inputs.make_problem(name, layer=layer)
-        units = pick_units(prob, 40)
-        o_ref, s_ref = oracle_units(prob, units)
-        d = staging.DeviceProblem(prob, "cuda", algo=algo)
-        if mode == "separate":
-            check_verify(d, units, o_ref)
-            check_state_update(d, units, s_ref, d.commit)
-        else:
-            d.o.fill_(float("nan"))
-            check_state_update(d, units, s_ref, d.fused)
-            assert rel_err(gather_outputs(prob, units, d.o.cpu().numpy(), o_ref), o_ref) <= TOL
-        del d
-        torch.cuda.empty_cache()
+FULL_LAYERS = [(n, l) for n in FULL for l in ([0, 23] if n.endswith("x24") else [0])]
+
+
+@pytest.mark.parametrize("name,layer", FULL_LAYERS, ids=[f"{n}-layer{l}" for n, l in FULL_LAYERS])
+def test_full_size_every_unit(name, layer):
+    """All units of the workload (of the named layer), against one oracle run:
+    verify then commit, and fused, on the default kernel and on the tcgen05 one.
+    Per-unit or per-round faults of the persistent kernel (its last, partly
+    filled round of units) would show here."""
+    prob = inputs.make_problem(name, layer=layer)
+    units = np.arange(prob.units)
+    o_ref, s_ref = oracle_units(prob, units)
+    for algo in (AUTO, TC):
+        for mode in ("separate", "fused"):
+            d = staging.DeviceProblem(prob, "cuda", algo=algo)
+            if mode == "separate":
+                check_verify(d, units, o_ref)
+                check_state_update(d, units, s_ref, d.commit)
+            else:
+                d.o.fill_(float("nan"))
+                check_state_update(d, units, s_ref, d.fused)
+                err = rel_err(gather_outputs(prob, units, d.o.cpu().numpy(), o_ref), o_ref)
+                assert err <= TOL, f"fused o: max rel err {err:.3e}"
+            del d
+            torch.cuda.empty_cache()
 
 
 @pytest.mark.parametrize("golden", ["hand_2x2_t2.txt", "hand_dk3_dv2_t2.txt"])
