@@ -22,12 +22,14 @@
 // shuffle or shared-memory transpose.
 //
 // Pipeline of one block (the block walks units blockIdx.x, + gridDim.x, ...):
-//   * one thread of warp 1 issues, for the next unit that has work, four 3-D
-//     TMA copies of its 64 KiB tile (boxes of 32 value columns x 128 key rows)
-//     into the block's single tile stage as soon as the current unit has read
-//     the tile (right after the first product); one thread of warp 3 issues
-//     the 16-token boxes of its k, q and v rows into the other of two token
-//     buffers when the current unit starts; all with the 128-byte swizzle;
+//   * the 64 KiB tile stage is eight half-boxes (32 value columns x 64 key
+//     rows), one mbarrier each: warp w reads only its own 32 columns, so it
+//     waits only for its two half-boxes, and as soon as it has read the upper
+//     (lower) half of its columns in the first product, its lane 0 issues the
+//     same half-box of the next unit that has work into the freed space; one
+//     thread of warp 3 issues the 16-token boxes of its k, q and v rows into
+//     the other of two token buffers when the current unit starts; all with
+//     the 128-byte swizzle;
 //   * one thread of warp 2 asks TMA to pull the unit after that into L2, so
 //     the shared-memory loads issued one unit later hit in L2 (a TMA issue can
 //     hold its warp while the copy engine is busy, hence three issuing warps);
@@ -67,7 +69,8 @@ namespace {
 constexpr int CT = 16;   // token block
 constexpr int D = 128;   // dk = dv
 constexpr int kBlocksPerSM = 2;
-constexpr uint32_t kBoxBytes = 32 * D * 4;        // tile box: 32 value columns x 128 key rows
+constexpr uint32_t kBoxBytes = 32 * D * 4;        // one warp's columns: 32 value columns x 128 key rows
+constexpr uint32_t kHalfBytes = kBoxBytes / 2;    // one TMA box: 32 value columns x 64 key rows
 constexpr uint32_t kTileBytes = 4 * kBoxBytes;    // 64 KiB
 constexpr uint32_t kTokHalfBytes = CT * 64 * 2;   // token box: 64 of 128 bf16 x 16 tokens
 constexpr uint32_t kTokBytes = 2 * kTokHalfBytes; // one [16][128] bf16 tile
@@ -99,7 +102,8 @@ struct Aux {
     float palpha[CT];       // alpha of its rows t < a_prev (1 beyond)
     float pdcol[CT];        // prod_{s<r<a_prev} alpha_r for s < a_prev, else 0
     float pgam;             // prod_{r<a_prev} alpha_r
-    unsigned long long tile_full, tok_full[2];
+    unsigned long long tile_full[4][2];  // [warp][key-row half]: that warp's columns of those rows
+    unsigned long long tok_full[2];
     unsigned long long mma_full;  // tcgen05 products completed
     uint32_t tmem_base;           // TMEM address of this block's columns
     int abort_flag;
@@ -120,6 +124,12 @@ static_assert(kBlocksPerSM * (kSmemBytes + 1024) <= 233472, "two blocks per SM")
 
 __device__ __forceinline__ uint32_t smem_u32(const void *p) {
     return (uint32_t)__cvta_generic_to_shared(p);
+}
+
+// Orders this thread's earlier generic-proxy shared-memory accesses before
+// later async-proxy (TMA) accesses of the same memory.
+__device__ __forceinline__ void fence_proxy_async_smem() {
+    asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory");
 }
 
 __device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes) {
@@ -448,23 +458,31 @@ __device__ __forceinline__ void issue_tokens(const Maps &maps, const UnitPlan &p
     }
 }
 
-// One thread: the four tile boxes of one unit.
-// Commit-then-verify units with a prefix to commit also bring the previous
-// step's W rows of the request (4 boxes of 32 columns x 16 rows) on the same
-// barrier.
+// One thread: half-box `hf` (key rows 64 hf .. 64 hf + 63) of warp w's columns
+// 32 w .. 32 w + 31 of one unit's tile, on barrier tile_full[w][hf].
+// Commit-then-verify units with a prefix to commit also bring, with the upper
+// half, warp w's columns of the previous step's W rows of the request (one box
+// of 32 columns x 16 rows).
 template <int MODE>
-__device__ __forceinline__ void issue_tile(const Maps &maps, const UnitPlan &pl,
-                                           unsigned char *tile, uint32_t tile_bar,
-                                           unsigned char *wprev) {
-    const bool wp = MODE == kLagged && pl.pa > 0;
-    mbar_arrive_expect_tx(tile_bar, kTileBytes + (wp ? 4 * kWpBoxBytes : 0u));
+__device__ __forceinline__ void issue_tile_half(const Maps &maps, const UnitPlan &pl, int w, int hf,
+                                                unsigned char *tile, uint32_t bar,
+                                                unsigned char *wprev) {
+    const bool wp = MODE == kLagged && pl.pa > 0 && hf == 0;
+    mbar_arrive_expect_tx(bar, kHalfBytes + (wp ? kWpBoxBytes : 0u));
+    tma_load_3d(smem_u32(tile) + w * kBoxBytes + hf * kHalfBytes, &maps.pool, 32 * w, 64 * hf,
+                pl.tile, bar);
+    if (wp) tma_load_3d(smem_u32(wprev) + w * kWpBoxBytes, &maps.wp, 32 * w, pl.h, pl.prow0, bar);
+}
+
+// One thread: all eight half-boxes of one unit (nothing of the stage is in use).
+template <int MODE>
+__device__ __forceinline__ void issue_tile(const Maps &maps, const UnitPlan &pl, unsigned char *tile,
+                                           Aux &ax, unsigned char *wprev) {
 #pragma unroll
-    for (int b = 0; b < 4; ++b)
-        tma_load_3d(smem_u32(tile) + b * kBoxBytes, &maps.pool, 32 * b, 0, pl.tile, tile_bar);
-    if (wp)
+    for (int w = 0; w < 4; ++w)
 #pragma unroll
-        for (int b = 0; b < 4; ++b)
-            tma_load_3d(smem_u32(wprev) + b * kWpBoxBytes, &maps.wp, 32 * b, pl.h, pl.prow0, tile_bar);
+        for (int hf = 0; hf < 2; ++hf)
+            issue_tile_half<MODE>(maps, pl, w, hf, tile, smem_u32(&ax.tile_full[w][hf]), wprev);
 }
 
 // One thread: pull the tile and token rows of a later unit into L2 (no shared
@@ -478,7 +496,7 @@ __device__ __forceinline__ void prefetch_unit(const Maps &maps, const UnitPlan &
         if (MODE != kCommit) tma_prefetch_3d(&maps.q, 64 * hb, pl.h, pl.qrow0 > 0 ? pl.qrow0 : 0);
     }
 #pragma unroll
-    for (int b = 0; b < 4; ++b) tma_prefetch_3d(&maps.pool, 32 * b, 0, pl.tile);
+    for (int b = 0; b < 8; ++b) tma_prefetch_3d(&maps.pool, 32 * (b & 3), 64 * (b >> 2), pl.tile);
 }
 
 // Read through L2 only (no L1 line is left behind), for the hints below.
@@ -523,7 +541,8 @@ __device__ __forceinline__ void early_prefetch(const Launch<NL> &L, int w0, int 
             if (MODE != kCommit) tma_prefetch_3d(&maps.q, 64 * hb, h[j], (int)row);
         }
 #pragma unroll
-        for (int b = 0; b < 4; ++b) tma_prefetch_3d(&maps.pool, 32 * b, 0, (int)(sl * p.H + h[j]));
+        for (int b = 0; b < 8; ++b)
+            tma_prefetch_3d(&maps.pool, 32 * (b & 3), 64 * (b >> 2), (int)(sl * p.H + h[j]));
     }
 }
 
@@ -689,7 +708,6 @@ __global__ void __launch_bounds__(kThreads, kBlocksPerSM)
     const int W = NL == 1 ? U : U * L.n;  // units of the launch
     const int G = gridDim.x;
     const size_t row_stride = (size_t)p.H * D;
-    const uint32_t tile_bar = smem_u32(&ax.tile_full);
     const int col0 = warp * CW + CPT * g;  // this thread's first value column
 
     // Programmatic dependent launch: the next kernel on the stream may be
@@ -698,7 +716,11 @@ __global__ void __launch_bounds__(kThreads, kBlocksPerSM)
     // previous kernel on the stream has completed.  Stream order is kept.
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     if (tid == 0) {
-        mbar_init(tile_bar, 1);
+#pragma unroll
+        for (int w = 0; w < 4; ++w) {
+            mbar_init(smem_u32(&ax.tile_full[w][0]), 1);
+            mbar_init(smem_u32(&ax.tile_full[w][1]), 1);
+        }
         mbar_init(smem_u32(&ax.tok_full[0]), 1);
         mbar_init(smem_u32(&ax.tok_full[1]), 1);
         mbar_init(smem_u32(&ax.mma_full), 1);
@@ -723,19 +745,19 @@ __global__ void __launch_bounds__(kThreads, kBlocksPerSM)
 
     // Plans: `cur` is the unit being computed, `nxt` the next one (its loads are
     // issued during `cur`), `raw` the metadata of the one after.
+    // The metadata of the first three units is loaded at once (the loads are
+    // independent), then the first unit's copies go out before anything else.
     int unit = blockIdx.x;  // launch unit
     UnitPlan cur, nxt;
-    RawMeta raw;
     cur.skip = true;
     nxt.skip = true;
+    const RawMeta m0 = load_unit_meta<MODE, RAGGED, NL>(p, unit, W, U);
+    const RawMeta m1 = load_unit_meta<MODE, RAGGED, NL>(p, unit + G, W, U);
+    RawMeta raw = load_unit_meta<MODE, RAGGED, NL>(p, unit + 2 * G, W, U);
     if (unit < W) {
-        cur = plan_unit<MODE, NL, REPLAY>(L, unit, U, load_unit_meta<MODE, RAGGED, NL>(p, unit, W, U));
+        cur = plan_unit<MODE, NL, REPLAY>(L, unit, U, m0);
         if (REPLAY) finalize_replay<MODE>(L.a[cur.layer], cur, tid);
     }
-    if (unit + G < W)
-        nxt = plan_unit<MODE, NL, REPLAY>(L, unit + G, U,
-                                          load_unit_meta<MODE, RAGGED, NL>(p, unit + G, W, U));
-    raw = load_unit_meta<MODE, RAGGED, NL>(p, unit + 2 * G, W, U);
 
     // A step is one 16-token chunk of one unit.  Step k (in the order this block
     // computes them) uses token buffer k & 1; its token boxes go out when step
@@ -748,8 +770,9 @@ __global__ void __launch_bounds__(kThreads, kBlocksPerSM)
     int steps = 0;       // steps computed
     if (tid == 0 && !cur.skip) {
         issue_tokens<MODE>(L.maps[cur.layer], cur, 0, sm.tok[0], smem_u32(&ax.tok_full[0]));
-        issue_tile<MODE>(L.maps[cur.layer], cur, sm.tile, tile_bar, sm.wprev);
+        issue_tile<MODE>(L.maps[cur.layer], cur, sm.tile, ax, sm.wprev);
     }
+    if (unit + G < W) nxt = plan_unit<MODE, NL, REPLAY>(L, unit + G, U, m1);
     if (tid == 0 && !nxt.skip) prefetch_unit<MODE>(L.maps[nxt.layer], nxt);
     if (!cur.skip) {
         ++issued;
@@ -790,7 +813,7 @@ __global__ void __launch_bounds__(kThreads, kBlocksPerSM)
                 if (tid == kTokIssuer)
                     issue_tokens<MODE>(L.maps[cur.layer], cur, 0, sm.tok[tok_issued & 1],
                                        smem_u32(&ax.tok_full[tok_issued & 1]));
-                if (tid == kTileIssuer) issue_tile<MODE>(L.maps[cur.layer], cur, sm.tile, tile_bar, sm.wprev);
+                if (tid == kTileIssuer) issue_tile<MODE>(L.maps[cur.layer], cur, sm.tile, ax, sm.wprev);
                 ++issued;
                 ++tok_issued;
             }
@@ -812,6 +835,7 @@ __global__ void __launch_bounds__(kThreads, kBlocksPerSM)
             const TokBuf &tb = sm.tok[steps & 1];
 
             // 1. Gates into shared memory; token block arrival.
+            fence_proxy_async_smem();  // reads of the token buffer refilled below come first
             __syncthreads();  // the previous step is done with the small matrices
             // The next step's token block goes into the other buffer now.
             if (tok_issued == steps + 1 && (more || !cur.skip)) {
@@ -917,15 +941,27 @@ __global__ void __launch_bounds__(kThreads, kBlocksPerSM)
             }
             __syncthreads();
 
-            // 4. The checkpoint tile of this unit (first chunk only).  The metadata
-            //    of the unit three ahead is loaded here, mid-unit: at the top of the
-            //    loop these loads would queue behind the previous unit's stores.
+            // 4. The checkpoint tile of this unit (first chunk only): the tcgen05
+            //    path waits here for its warp's two half-boxes; the mma.sync path
+            //    waits for each half where the first product reads it.  The
+            //    metadata of the unit three ahead is loaded here, mid-unit: at the
+            //    top of the loop these loads would queue behind the previous
+            //    unit's stores.
+            bool tile_ok = true;
+            const uint32_t hbar0 = smem_u32(&ax.tile_full[warp][0]);
+            const uint32_t hbar1 = smem_u32(&ax.tile_full[warp][1]);
             if (!MULTI || ch == 0) {
-                if (!wait_parity(tile_bar, processed & 1)) ax.abort_flag = 1;
-                __syncthreads();
-                if (ax.abort_flag) {
-                    aborted = true;
-                    break;
+                if constexpr (TC) {
+                    if (!wait_parity(hbar0, processed & 1) || !wait_parity(hbar1, processed & 1))
+                        ax.abort_flag = 1;
+                    __syncthreads();
+                    if (ax.abort_flag) {
+                        aborted = true;
+                        break;
+                    }
+                } else if (MODE == kLagged) {
+                    // the previous step's W rows come with the upper half-box
+                    tile_ok = mbar_try_wait(hbar0, processed & 1) || wait_parity(hbar0, processed & 1);
                 }
                 raw = load_unit_meta<MODE, RAGGED, NL>(p, unit + 3 * G, W, U);
                 if (!more) {  // a single-chunk unit: the next unit's gates
@@ -1001,12 +1037,13 @@ __global__ void __launch_bounds__(kThreads, kBlocksPerSM)
                     tmem_wait_st();
                 }
                 tc_fence_before();
+                fence_proxy_async_smem();  // the reads of the stage come before its refill
                 __syncthreads();
                 // The tile is in TMEM (and registers): the stage is free for the next unit.
                 if (!MULTI || ch == 0) {
                     ++processed;
                     if (!cur.skip) {
-                        if (tid == kTileIssuer) issue_tile<MODE>(L.maps[cur.layer], cur, sm.tile, tile_bar, sm.wprev);
+                        if (tid == kTileIssuer) issue_tile<MODE>(L.maps[cur.layer], cur, sm.tile, ax, sm.wprev);
                         ++issued;
                     }
                     if (tid == kPrefIssuer && !nxt.skip) prefetch_unit<MODE>(L.maps[nxt.layer], nxt);
@@ -1224,6 +1261,13 @@ __global__ void __launch_bounds__(kThreads, kBlocksPerSM)
                 }
                 float hv[4][CPT];
                 if (!MULTI || ch == 0) {
+                    // This warp's half-box of these rows: wait for it (first rows of
+                    // each half); after its last rows, hand it to the next unit.
+                    if ((kb & 3) == 0 && (MODE != kLagged || kb == 4)) {
+                        const uint32_t hb = kb == 0 ? hbar0 : hbar1;
+                        tile_ok = (mbar_try_wait(hb, processed & 1) || wait_parity(hb, processed & 1)) &&
+                                  tile_ok;
+                    }
 #pragma unroll
                     for (int rr = 0; rr < 4; ++rr) {
                         const float4 x = ld_tile_row(sm.tile, warp, g, key_row(kb, c, rr));
@@ -1245,7 +1289,7 @@ __global__ void __launch_bounds__(kThreads, kBlocksPerSM)
                     // These rows of the committed state, written to the slot, then used.
                     if (me.pa > 0) {
                         update_rows(hv, kb, lah, lal, ax.pgam, smem_u32(tb.kp), kTokHalfBytes, lane);
-                        store_rows(opaque(me.u.tile) + col0, kb, c, hv);
+                        if (tile_ok) store_rows(opaque(me.u.tile) + col0, kb, c, hv);
                     }
                 }
                 uint32_t b[4][2];
@@ -1276,17 +1320,28 @@ __global__ void __launch_bounds__(kThreads, kBlocksPerSM)
                             al[3], b[nt][0], b[nt][1]);
                     }
                 }
+                // The last rows of a half-box are consumed (the products above used
+                // them): hand this warp's half-box to the next unit.  The proxy fence
+                // orders each lane's shared-memory reads of it before the copy that
+                // overwrites it.
+                if ((!MULTI || ch == 0) && (kb & 3) == 3 && !cur.skip) {
+                    fence_proxy_async_smem();
+                    __syncwarp();
+                    if (lane == 0 && tile_ok)
+                        issue_tile_half<MODE>(L.maps[cur.layer], cur, warp, kb >> 2, sm.tile,
+                                              kb == 3 ? hbar0 : hbar1, sm.wprev);
+                }
             }
 
-            // Tinv is complete.  After the first chunk the tile is in registers:
-            // the stage is free and warp 1 sends the next unit's tile.
-            __syncthreads();
+            // Tinv is complete.  After the first chunk the tile is in registers,
+            // and every warp has sent its half-boxes of the next unit's tile.
+            if (__syncthreads_or(!tile_ok)) {
+                aborted = true;
+                break;
+            }
             if (!MULTI || ch == 0) {
                 ++processed;
-                if (!cur.skip) {
-                    if (tid == kTileIssuer) issue_tile<MODE>(L.maps[cur.layer], cur, sm.tile, tile_bar, sm.wprev);
-                    ++issued;
-                }
+                if (!cur.skip) ++issued;
                 if (tid == kPrefIssuer && !nxt.skip) prefetch_unit<MODE>(L.maps[nxt.layer], nxt);
             }
 
@@ -1428,7 +1483,9 @@ __global__ void __launch_bounds__(kThreads, kBlocksPerSM)
     // Copies still in flight must land before the block exits.
     if (tid == 0) {
         bool ok = true;
-        if (issued > processed) ok = wait_parity(tile_bar, processed & 1) && ok;
+        if (issued > processed)
+            for (int b = 0; b < 8; ++b)
+                ok = wait_parity(smem_u32(&ax.tile_full[b & 3][b >> 2]), processed & 1) && ok;
         for (int k = steps; k < tok_issued; ++k)
             ok = wait_parity(smem_u32(&ax.tok_full[k & 1]), (k >> 1) & 1) && ok;
         if (!ok) aborted = true;
@@ -1535,7 +1592,7 @@ cudaError_t encode_layer(const Args &p, Maps *maps) {
     // The pool as a 3-D tensor: value column (contiguous), key row, slot * H + head.
     const cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)D, (cuuint64_t)tiles};
     const cuuint64_t strides[2] = {(cuuint64_t)D * 4, (cuuint64_t)D * D * 4};
-    const cuuint32_t box[3] = {32, (cuuint32_t)D, 1};
+    const cuuint32_t box[3] = {32, (cuuint32_t)D / 2, 1};
     const cuuint32_t elem[3] = {1, 1, 1};
     if (encode(&maps->pool, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, p.pool, dims, strides, box, elem,
                CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
