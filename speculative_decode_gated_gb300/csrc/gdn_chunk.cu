@@ -30,9 +30,10 @@
 //     thread of warp 3 issues the 16-token boxes of its k, q and v rows into
 //     the other of two token buffers when the current unit starts; all with
 //     the 128-byte swizzle;
-//   * one thread of warp 2 asks TMA to pull the unit after that into L2, so
-//     the shared-memory loads issued one unit later hit in L2 (a TMA issue can
-//     hold its warp while the copy engine is busy, hence three issuing warps);
+//   * before the wait on the previous kernel, thread 0 asks TMA to pull the
+//     block's first unit into L2 (the only L2 prefetch: prefetches of later
+//     units share the copy engine's queue with the loads that are needed
+//     first, and measured slower);
 //   * metadata is loaded three units ahead (mid-unit, not behind the stores)
 //     and the gates one unit ahead, so no thread waits on a load it has just
 //     issued.
@@ -474,29 +475,26 @@ __device__ __forceinline__ void issue_tile_half(const Maps &maps, const UnitPlan
     if (wp) tma_load_3d(smem_u32(wprev) + w * kWpBoxBytes, &maps.wp, 32 * w, pl.h, pl.prow0, bar);
 }
 
-// One thread: all eight half-boxes of one unit (nothing of the stage is in use).
+// One thread: all eight half-boxes of one unit (no part of the stage is in use).
+template <int MODE>
+__device__ __forceinline__ void issue_tile(const Maps &maps, const UnitPlan &pl, unsigned char *tile,
+                                           Aux &ax, unsigned char *wprev);
+
+// Lane 0 of warp w: both half-boxes of warp w's columns of one unit (that
+// warp's part of the stage is not in use).
+template <int MODE>
+__device__ __forceinline__ void issue_warp_tile(const Maps &maps, const UnitPlan &pl, int w,
+                                                unsigned char *tile, Aux &ax, unsigned char *wprev) {
+#pragma unroll
+    for (int hf = 0; hf < 2; ++hf)
+        issue_tile_half<MODE>(maps, pl, w, hf, tile, smem_u32(&ax.tile_full[w][hf]), wprev);
+}
+
 template <int MODE>
 __device__ __forceinline__ void issue_tile(const Maps &maps, const UnitPlan &pl, unsigned char *tile,
                                            Aux &ax, unsigned char *wprev) {
 #pragma unroll
-    for (int w = 0; w < 4; ++w)
-#pragma unroll
-        for (int hf = 0; hf < 2; ++hf)
-            issue_tile_half<MODE>(maps, pl, w, hf, tile, smem_u32(&ax.tile_full[w][hf]), wprev);
-}
-
-// One thread: pull the tile and token rows of a later unit into L2 (no shared
-// memory, no barrier), so its shared-memory loads, issued later, hit in L2.
-template <int MODE>
-__device__ __forceinline__ void prefetch_unit(const Maps &maps, const UnitPlan &pl) {
-#pragma unroll
-    for (int hb = 0; hb < 2; ++hb) {
-        tma_prefetch_3d(&maps.k, 64 * hb, pl.h, pl.u.row0);
-        tma_prefetch_3d(&maps.v, 64 * hb, pl.h, pl.u.row0);
-        if (MODE != kCommit) tma_prefetch_3d(&maps.q, 64 * hb, pl.h, pl.qrow0 > 0 ? pl.qrow0 : 0);
-    }
-#pragma unroll
-    for (int b = 0; b < 8; ++b) tma_prefetch_3d(&maps.pool, 32 * (b & 3), 64 * (b >> 2), pl.tile);
+    for (int w = 0; w < 4; ++w) issue_warp_tile<MODE>(maps, pl, w, tile, ax, wprev);
 }
 
 // Read through L2 only (no L1 line is left behind), for the hints below.
@@ -507,43 +505,36 @@ __device__ __forceinline__ int ld_l2(const int32_t *ptr) {
 }
 
 // Thread 0, before the wait on the previous kernel of the stream: ask for the
-// tiles and token rows of this block's first two units in L2.  Prefetches
-// change no memory, so issuing them early is safe even when the previous
-// kernel is still writing what they touch (the real loads come after the wait
-// and read the current data from L2).  The metadata read here may be stale for
-// the same reason; it only picks addresses, clamped into the arrays, and is
-// read again after the wait.
+// tile and token rows of this block's first unit in L2.  Prefetches change no
+// memory, so issuing them early is safe even when the previous kernel is still
+// writing what they touch (the real loads come after the wait and read the
+// current data from L2).  The metadata read here may be stale for the same
+// reason; it only picks addresses, clamped into the arrays, and is read again
+// after the wait.
 template <int MODE, bool RAGGED, int NL, bool REPLAY>
-__device__ __forceinline__ void early_prefetch(const Launch<NL> &L, int w0, int G, int W, int U) {
+__device__ __forceinline__ void early_prefetch(const Launch<NL> &L, int w, int W, int U) {
+    if (w >= W) return;
     const Args &p = L.a[0];
-    int h[2], row0[2], slot[2], layer[2];
-#pragma unroll
-    for (int j = 0; j < 2; ++j) {
-        const int w = w0 + j * G < W ? w0 + j * G : W - 1;
-        layer[j] = NL == 1 ? 0 : w / U;
-        const int unit = w - layer[j] * U;
-        const int r = unit / p.H;
-        h[j] = unit - r * p.H;
-        row0[j] = RAGGED ? ld_l2(p.cu_seqlens + r) : r * p.max_T;
-        slot[j] = ld_l2(p.slot_ids + r);
-    }
-#pragma unroll
-    for (int j = 0; j < 2; ++j) {
-        if (w0 + j * G >= W) break;
-        const Maps &maps = L.maps[layer[j]];
-        const long long row = row0[j] < 0 ? 0 : (row0[j] >= p.n_tok ? p.n_tok - 1 : row0[j]);
-        const long long sl = slot[j] < 0 ? 0 : (slot[j] >= p.pool_slots ? p.pool_slots - 1 : slot[j]);
+    const int layer = NL == 1 ? 0 : w / U;
+    const int unit = w - layer * U;
+    const int r = unit / p.H;
+    const int h = unit - r * p.H;
+    const int row0 = RAGGED ? ld_l2(p.cu_seqlens + r) : r * p.max_T;
+    const int slot = ld_l2(p.slot_ids + r);
+    const Maps &maps = L.maps[layer];
+    const long long row = row0 < 0 ? 0 : (row0 >= p.n_tok ? p.n_tok - 1 : row0);
+    const long long sl = slot < 0 ? 0 : (slot >= p.pool_slots ? p.pool_slots - 1 : slot);
+    if (!REPLAY) {  // replay: the buffered length is not known yet, so the tile only
 #pragma unroll
         for (int hb = 0; hb < 2; ++hb) {
-            if (REPLAY) break;  // the buffered length is not known yet: the tile only
-            tma_prefetch_3d(&maps.k, 64 * hb, h[j], (int)row);
-            tma_prefetch_3d(&maps.v, 64 * hb, h[j], (int)row);
-            if (MODE != kCommit) tma_prefetch_3d(&maps.q, 64 * hb, h[j], (int)row);
+            tma_prefetch_3d(&maps.k, 64 * hb, h, (int)row);
+            tma_prefetch_3d(&maps.v, 64 * hb, h, (int)row);
+            if (MODE != kCommit) tma_prefetch_3d(&maps.q, 64 * hb, h, (int)row);
         }
-#pragma unroll
-        for (int b = 0; b < 8; ++b)
-            tma_prefetch_3d(&maps.pool, 32 * (b & 3), 64 * (b >> 2), (int)(sl * p.H + h[j]));
     }
+#pragma unroll
+    for (int b = 0; b < 8; ++b)
+        tma_prefetch_3d(&maps.pool, 32 * (b & 3), 64 * (b >> 2), (int)(sl * p.H + h));
 }
 
 // Gate of token 16 ch + min(tid, left - 1) of a unit, left = the unit's tokens
@@ -581,10 +572,10 @@ constexpr int CW = D / NW;       // 32 columns per warp
 constexpr int MT = CW / 16;      // 2 m-tiles
 constexpr int CPT = 2 * MT;      // 4 columns per lane
 constexpr int kTinvLanes = CT / NW;  // Tinv columns per warp
-// Threads that issue the copies (each issue may stall its warp for a while when
-// the copy engine is busy, so the work is spread over warps 1-3; warp 0
-// issues the tensor-core products).
-constexpr int kTokIssuer = 96, kTileIssuer = 32, kPrefIssuer = 64;
+// The thread that issues the token boxes (a copy issue may stall its warp for a
+// while when the copy engine is busy; warp 0 issues the tcgen05 products).  The
+// tile half-boxes are issued by lane 0 of the warp that reads them.
+constexpr int kTokIssuer = 96;
 
 // Columns CPT g + [0, CPT) of warp w's slice, key row `row`, from the swizzled tile.
 __device__ __forceinline__ float4 ld_tile_row(const unsigned char *tile, int warp, int g, int row) {
@@ -740,7 +731,7 @@ __global__ void __launch_bounds__(kThreads, kBlocksPerSM)
     const uint32_t mma_bar = smem_u32(&ax.mma_full);
     int mma_phase = 0;
     const int j = 32 * warp + lane;  // tcgen05 path: this thread's value column
-    if (tid == 0) early_prefetch<MODE, RAGGED, NL, REPLAY>(L, blockIdx.x, G, W, U);
+    if (tid == 0) early_prefetch<MODE, RAGGED, NL, REPLAY>(L, blockIdx.x, W, U);
     asm volatile("griddepcontrol.wait;" ::: "memory");
 
     // Plans: `cur` is the unit being computed, `nxt` the next one (its loads are
@@ -751,12 +742,26 @@ __global__ void __launch_bounds__(kThreads, kBlocksPerSM)
     UnitPlan cur, nxt;
     cur.skip = true;
     nxt.skip = true;
-    const RawMeta m0 = load_unit_meta<MODE, RAGGED, NL>(p, unit, W, U);
-    const RawMeta m1 = load_unit_meta<MODE, RAGGED, NL>(p, unit + G, W, U);
-    RawMeta raw = load_unit_meta<MODE, RAGGED, NL>(p, unit + 2 * G, W, U);
-    if (unit < W) {
-        cur = plan_unit<MODE, NL, REPLAY>(L, unit, U, m0);
-        if (REPLAY) finalize_replay<MODE>(L.a[cur.layer], cur, tid);
+    // (Kernels for units of several chunks plan the units one after the other:
+    // their state registers leave no room for three units' metadata at once.)
+    RawMeta m1, raw;
+    if (MULTI) {
+        if (unit < W) {
+            cur = plan_unit<MODE, NL, REPLAY>(L, unit, U, load_unit_meta<MODE, RAGGED, NL>(p, unit, W, U));
+            if (REPLAY) finalize_replay<MODE>(L.a[cur.layer], cur, tid);
+        }
+        if (unit + G < W)
+            nxt = plan_unit<MODE, NL, REPLAY>(L, unit + G, U,
+                                              load_unit_meta<MODE, RAGGED, NL>(p, unit + G, W, U));
+        raw = load_unit_meta<MODE, RAGGED, NL>(p, unit + 2 * G, W, U);
+    } else {
+        const RawMeta m0 = load_unit_meta<MODE, RAGGED, NL>(p, unit, W, U);
+        m1 = load_unit_meta<MODE, RAGGED, NL>(p, unit + G, W, U);
+        raw = load_unit_meta<MODE, RAGGED, NL>(p, unit + 2 * G, W, U);
+        if (unit < W) {
+            cur = plan_unit<MODE, NL, REPLAY>(L, unit, U, m0);
+            if (REPLAY) finalize_replay<MODE>(L.a[cur.layer], cur, tid);
+        }
     }
 
     // A step is one 16-token chunk of one unit.  Step k (in the order this block
@@ -768,12 +773,20 @@ __global__ void __launch_bounds__(kThreads, kBlocksPerSM)
     int processed = 0;   // units whose tile was consumed
     int tok_issued = 0;  // steps whose token load was issued
     int steps = 0;       // steps computed
-    if (tid == 0 && !cur.skip) {
-        issue_tokens<MODE>(L.maps[cur.layer], cur, 0, sm.tok[0], smem_u32(&ax.tok_full[0]));
-        issue_tile<MODE>(L.maps[cur.layer], cur, sm.tile, ax, sm.wprev);
+    if (!cur.skip) {
+        // the first unit's token boxes (warp 3) and each warp's own half-boxes
+        // (kernels for units of several chunks keep it on one thread: their state
+        // registers leave no room for the spread issue)
+        if (tid == kTokIssuer)
+            issue_tokens<MODE>(L.maps[cur.layer], cur, 0, sm.tok[0], smem_u32(&ax.tok_full[0]));
+        if (MULTI ? tid == 0 : lane == 0) {
+            if (MULTI)
+                issue_tile<MODE>(L.maps[cur.layer], cur, sm.tile, ax, sm.wprev);
+            else
+                issue_warp_tile<MODE>(L.maps[cur.layer], cur, warp, sm.tile, ax, sm.wprev);
+        }
     }
-    if (unit + G < W) nxt = plan_unit<MODE, NL, REPLAY>(L, unit + G, U, m1);
-    if (tid == 0 && !nxt.skip) prefetch_unit<MODE>(L.maps[nxt.layer], nxt);
+    if (!MULTI && unit + G < W) nxt = plan_unit<MODE, NL, REPLAY>(L, unit + G, U, m1);
     if (!cur.skip) {
         ++issued;
         ++tok_issued;
@@ -813,11 +826,15 @@ __global__ void __launch_bounds__(kThreads, kBlocksPerSM)
                 if (tid == kTokIssuer)
                     issue_tokens<MODE>(L.maps[cur.layer], cur, 0, sm.tok[tok_issued & 1],
                                        smem_u32(&ax.tok_full[tok_issued & 1]));
-                if (tid == kTileIssuer) issue_tile<MODE>(L.maps[cur.layer], cur, sm.tile, ax, sm.wprev);
+                if (MULTI ? tid == 0 : lane == 0) {
+                    if (MULTI)
+                        issue_tile<MODE>(L.maps[cur.layer], cur, sm.tile, ax, sm.wprev);
+                    else
+                        issue_warp_tile<MODE>(L.maps[cur.layer], cur, warp, sm.tile, ax, sm.wprev);
+                }
                 ++issued;
                 ++tok_issued;
             }
-            if (tid == kPrefIssuer && !nxt.skip) prefetch_unit<MODE>(L.maps[nxt.layer], nxt);
             continue;
         }
         // Commit-then-verify: the previous step's gate (thread t < 16: row t) and the
@@ -942,8 +959,9 @@ __global__ void __launch_bounds__(kThreads, kBlocksPerSM)
             __syncthreads();
 
             // 4. The checkpoint tile of this unit (first chunk only): the tcgen05
-            //    path waits here for its warp's two half-boxes; the mma.sync path
-            //    waits for each half where the first product reads it.  The
+            //    path and units of several chunks wait here for the warp's two
+            //    half-boxes; single-chunk units wait for each half where the first
+            //    product reads it.  The
             //    metadata of the unit three ahead is loaded here, mid-unit: at the
             //    top of the loop these loads would queue behind the previous
             //    unit's stores.
@@ -951,9 +969,9 @@ __global__ void __launch_bounds__(kThreads, kBlocksPerSM)
             const uint32_t hbar0 = smem_u32(&ax.tile_full[warp][0]);
             const uint32_t hbar1 = smem_u32(&ax.tile_full[warp][1]);
             if (!MULTI || ch == 0) {
-                if constexpr (TC) {
-                    if (!wait_parity(hbar0, processed & 1) || !wait_parity(hbar1, processed & 1))
-                        ax.abort_flag = 1;
+                if constexpr (TC || MULTI) {
+                    // (units of several chunks read the whole tile into registers)
+                    if (!wait_parity2(hbar0, hbar1, processed & 1)) ax.abort_flag = 1;
                     __syncthreads();
                     if (ax.abort_flag) {
                         aborted = true;
@@ -1043,10 +1061,9 @@ __global__ void __launch_bounds__(kThreads, kBlocksPerSM)
                 if (!MULTI || ch == 0) {
                     ++processed;
                     if (!cur.skip) {
-                        if (tid == kTileIssuer) issue_tile<MODE>(L.maps[cur.layer], cur, sm.tile, ax, sm.wprev);
+                        if (tid == 0) issue_tile<MODE>(L.maps[cur.layer], cur, sm.tile, ax, sm.wprev);
                         ++issued;
                     }
-                    if (tid == kPrefIssuer && !nxt.skip) prefetch_unit<MODE>(L.maps[nxt.layer], nxt);
                 }
                 if (tid == 0) {
                     // [Q; K] (32 token rows: P and Z in one product) or K alone (16 rows).
@@ -1263,7 +1280,7 @@ __global__ void __launch_bounds__(kThreads, kBlocksPerSM)
                 if (!MULTI || ch == 0) {
                     // This warp's half-box of these rows: wait for it (first rows of
                     // each half); after its last rows, hand it to the next unit.
-                    if ((kb & 3) == 0 && (MODE != kLagged || kb == 4)) {
+                    if (!MULTI && (kb & 3) == 0 && (MODE != kLagged || kb == 4)) {
                         const uint32_t hb = kb == 0 ? hbar0 : hbar1;
                         tile_ok = (mbar_try_wait(hb, processed & 1) || wait_parity(hb, processed & 1)) &&
                                   tile_ok;
@@ -1323,8 +1340,9 @@ __global__ void __launch_bounds__(kThreads, kBlocksPerSM)
                 // The last rows of a half-box are consumed (the products above used
                 // them): hand this warp's half-box to the next unit.  The proxy fence
                 // orders each lane's shared-memory reads of it before the copy that
-                // overwrites it.
-                if ((!MULTI || ch == 0) && (kb & 3) == 3 && !cur.skip) {
+                // overwrites it.  (Units of several chunks keep their state in
+                // registers through the loop; they send the next tile after it.)
+                if (!MULTI && (kb & 3) == 3 && !cur.skip) {
                     fence_proxy_async_smem();
                     __syncwarp();
                     if (lane == 0 && tile_ok)
@@ -1334,15 +1352,20 @@ __global__ void __launch_bounds__(kThreads, kBlocksPerSM)
             }
 
             // Tinv is complete.  After the first chunk the tile is in registers,
-            // and every warp has sent its half-boxes of the next unit's tile.
-            if (__syncthreads_or(!tile_ok)) {
+            // and every warp has sent (or, for units of several chunks, now sends)
+            // its half-boxes of the next unit's tile.
+            if (MULTI) {
+                if (ch == 0) fence_proxy_async_smem();
+                __syncthreads();
+            } else if (__syncthreads_or(!tile_ok)) {
                 aborted = true;
                 break;
             }
             if (!MULTI || ch == 0) {
                 ++processed;
+                if (MULTI && !cur.skip && tid == 0)
+                    issue_tile<MODE>(L.maps[cur.layer], cur, sm.tile, ax, sm.wprev);
                 if (!cur.skip) ++issued;
-                if (tid == kPrefIssuer && !nxt.skip) prefetch_unit<MODE>(L.maps[nxt.layer], nxt);
             }
 
             // Token indices of this thread in the fragments: n-tile half ntt, element e:

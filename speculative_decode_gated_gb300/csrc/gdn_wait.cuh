@@ -48,4 +48,9 @@ __device__ __noinline__ inline bool wait_parity(uint32_t bar, uint32_t parity) {
     }
 }
 
+// Waits for the phases of two barriers with the same parity; false after ~2 s.
+__device__ __noinline__ inline bool wait_parity2(uint32_t bar0, uint32_t bar1, uint32_t parity) {
+    return wait_parity(bar0, parity) && wait_parity(bar1, parity);
+}
+
 }  // namespace gdn
