@@ -332,6 +332,32 @@ def time_calls(calls, kinds, stream, steps, warmup, world, dev, check=()):
     return ms_total, avg_ms, n_per_step
 
 
+def time_back_to_back(calls, kinds, stream, steps, world, dev):
+    """Mean milliseconds per launch of each call kind when the step's launches
+    of that kind run back to back (all verifies of the step, then all its
+    commits, as an engine issues a step's verifies), with an event pair
+    around each kind's run of launches only."""
+    import torch
+    import torch.distributed as dist
+
+    by_kind = {m: [call for mm, call in calls if mm == m] for m in kinds}
+    ev = {m: [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+              for _ in range(steps)] for m in kinds}
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    for i in range(steps):
+        for m in kinds:
+            a, b = ev[m][i]
+            a.record(stream)
+            for call in by_kind[m]:
+                call()
+            b.record(stream)
+    torch.cuda.synchronize()
+    return {m: statistics.fmean(a.elapsed_time(b) for a, b in ev[m]) / len(by_kind[m])
+            for m in kinds}
+
+
 # The other target workloads, timed in the same run as the headline: name,
 # call order, independent instances cycled through (each with its own pool and
 # inputs), and why.
@@ -491,6 +517,9 @@ def run_ours(args, rank, world, local_rank):
     time.sleep(0.3)
     ms_total, avg_ms, n_per_step = time_calls(calls, kinds, stream, args.steps, args.warmup,
                                               world, dev, check=dps)
+    b2b = None
+    if len(kinds) > 1 and not args.replay:
+        b2b = time_back_to_back(calls, kinds, stream, args.steps, world, dev)
     clk = clocks.stop()
     ms_step = ms_total / args.steps
     us_call = job_us_per_layer_call(ms_total, args.steps, L, world)
@@ -562,6 +591,11 @@ def run_ours(args, rank, world, local_rank):
             "frac_of_measured_hbm": gbs / (peak * world),
             "alg_bytes_per_layer_call": bytes_call,
             "kernel_us": {MODE_NAME[m]: avg_ms[m] * 1e3 for m in kinds},
+            "kernel_us_back_to_back": None if b2b is None else dict(
+                {MODE_NAME[m]: b2b[m] * 1e3 for m in kinds},
+                how="mean per launch when the step's launches of one kind run back to back "
+                    "(events around each kind's run only); kernel_us brackets every launch "
+                    "with events, which breaks the dependent-launch overlap"),
             "roofline": {"bound": "hbm", "kernel": ktag, "achieved": achieved, "peak": peak,
                          "peak_source": peak_kind, "unit": "GB/s", "frac": achieved / peak,
                          "traffic": traffic, "alg_bytes_per_launch": per_launch_bytes[dominant]},

@@ -1,8 +1,7 @@
 // Chunked (WY) form of the gated delta rule for one block of up to 16 draft
 // tokens, with the two state-sized products on tensor cores, as a persistent
-// kernel with two resident blocks per SM, each of which prefetches its next
-// unit's checkpoint tile and token block with TMA while it computes the
-// current unit.
+// kernel with two resident blocks per SM, each of which loads its next unit's
+// checkpoint tile and token block with TMA while it computes the current unit.
 //
 // With the tile H_0 (dk x dv, H = S^T), tokens t = 0..T-1 and
 //   D[t][s] = prod_{s<r<=t} alpha_r        (D[t][t] = 1),   gamma_t = D[t][0] * alpha_0,
@@ -25,8 +24,9 @@
 //   * the 64 KiB tile stage is eight half-boxes (32 value columns x 64 key
 //     rows), one mbarrier each: warp w reads only its own 32 columns, so it
 //     waits only for its two half-boxes, and as soon as it has read the upper
-//     (lower) half of its columns in the first product, its lane 0 issues the
-//     same half-box of the next unit that has work into the freed space; one
+//     (lower) half of its columns in the first product (and the products have
+//     consumed the loaded values), its lane 0 issues the same half-box of the
+//     next unit that has work into the freed space, behind a proxy fence; one
 //     thread of warp 3 issues the 16-token boxes of its k, q and v rows into
 //     the other of two token buffers when the current unit starts; all with
 //     the 128-byte swizzle;
@@ -767,8 +767,9 @@ __global__ void __launch_bounds__(kThreads, kBlocksPerSM)
     // A step is one 16-token chunk of one unit.  Step k (in the order this block
     // computes them) uses token buffer k & 1; its token boxes go out when step
     // k-1 starts (that buffer was last used by step k-2).  A unit's tile goes
-    // out when the previous unit has read its own tile (right after that unit's
-    // first product); later chunks start from the state held in registers.
+    // out half-box by half-box as the previous unit's first product consumes
+    // its own (units of several chunks: after that product); later chunks
+    // start from the state held in registers.
     int issued = 0;      // units whose tile load was issued
     int processed = 0;   // units whose tile was consumed
     int tok_issued = 0;  // steps whose token load was issued
