@@ -85,8 +85,6 @@ struct TokBuf {
     unsigned char qk[2][2][kTokHalfBytes];  // [column half][0: q, 1: k]
     unsigned char v[kTokBytes];             // halves kTokHalfBytes apart
     unsigned char kp[kTokBytes];            // commit-then-verify: the previous step's k rows
-    __device__ unsigned char *q() { return qk[0][0]; }
-    __device__ unsigned char *k() { return qk[0][1]; }
     __device__ const unsigned char *q() const { return qk[0][0]; }
     __device__ const unsigned char *k() const { return qk[0][1]; }
 };
@@ -300,10 +298,6 @@ __device__ __forceinline__ void umma_commit(uint32_t bar) {
                  : "memory");
 }
 
-// fp32 pair -> bf16x2 words hi and lo (element 0 in the low half).
-__device__ __forceinline__ void split_pair(float x0, float x1, uint32_t &hi, uint32_t &lo) {
-    split2(x0, x1, hi, lo);
-}
 
 // ------------------------------------------------------------ per-unit plan
 
