@@ -956,10 +956,9 @@ __global__ void __launch_bounds__(kThreads, kBlocksPerSM)
             // 4. The checkpoint tile of this unit (first chunk only): the tcgen05
             //    path and units of several chunks wait here for the warp's two
             //    half-boxes; single-chunk units wait for each half where the first
-            //    product reads it.  The
-            //    metadata of the unit three ahead is loaded here, mid-unit: at the
-            //    top of the loop these loads would queue behind the previous
-            //    unit's stores.
+            //    product reads it.  The metadata of the unit three ahead is loaded
+            //    here, mid-unit: at the top of the loop these loads would queue
+            //    behind the previous unit's stores.
             bool tile_ok = true;
             const uint32_t hbar0 = smem_u32(&ax.tile_full[warp][0]);
             const uint32_t hbar1 = smem_u32(&ax.tile_full[warp][1]);
@@ -1273,8 +1272,9 @@ __global__ void __launch_bounds__(kThreads, kBlocksPerSM)
                 }
                 float hv[4][CPT];
                 if (!MULTI || ch == 0) {
-                    // This warp's half-box of these rows: wait for it (first rows of
-                    // each half); after its last rows, hand it to the next unit.
+                    // This warp's half-box of these rows: wait for it at the first
+                    // rows of each half (it goes to the next unit after the products
+                    // of the half's last rows, below).
                     if (!MULTI && (kb & 3) == 0 && (MODE != kLagged || kb == 4)) {
                         const uint32_t hb = kb == 0 ? hbar0 : hbar1;
                         tile_ok = (mbar_try_wait(hb, processed & 1) || wait_parity(hb, processed & 1)) &&
