@@ -10,7 +10,10 @@ Workload (default): batch 64, 32 heads, dk = dv = 128, 16 draft tokens per
 request, 24 independent layers called back to back, each request's state in a
 24 x 512-slot fp32 pool (24 GiB), accepted lengths ~ Binomial(16, 0.75).  One
 step = for every layer: gdn_verify then gdn_commit.  Every step touches about
-11 GB, far more than the 129 MB L2, so no flush is needed between steps.
+11 GB, far more than the 129 MB L2, so no flush is needed between steps.  The
+timed steps replay the step's calls captured once in a CUDA graph, as an
+engine runs its decode step (--no-graph: launched one by one); the one-by-one
+figure is measured and reported beside it either way.
 
   python bench.py [--steps K] [--warmup W] [--gpus N] [--impl ours|reference]
 
@@ -274,14 +277,39 @@ def run_reference(args, rank):
 
 # ----------------------------------------------------------------- timing
 
-def time_calls(calls, kinds, stream, steps, warmup, world, dev, check=()):
-    """Warm up, then two timed regions of `steps` steps each (a step issues every
+def graph_of(calls, stream, reps=1):
+    """`reps` steps' calls captured in one CUDA graph (the library's per-device
+    set-up has run in the warm-up); returns a callable that replays it on
+    `stream`."""
+    import torch
+
+    g = torch.cuda.CUDAGraph()
+    torch.cuda.synchronize()
+    with torch.cuda.graph(g, stream=stream):
+        for _ in range(reps):
+            for _, call in calls:
+                call()
+    torch.cuda.synchronize()
+
+    def replay():
+        g.replay()
+    replay.keep = g
+    return replay
+
+
+def time_calls(calls, kinds, stream, steps, warmup, world, dev, check=(), graph=True):
+    """Warm up, then timed regions of `steps` steps each (a step issues every
     call of `calls` once, in order, on `stream`):
-      1. one event pair around all steps, launches back to back as in use
-         (the headline figure);
+      1. one event pair around all steps, launches back to back as in use (the
+         headline figure): with `graph`, the steps are replays of a CUDA graph
+         captured once, as an engine runs its decode step (a graph holds
+         enough steps for at least 24 launches, so the gap between two
+         replays is spread over them);
+      1b. with `graph`, the same with the calls launched one by one;
       2. an event pair around every launch, for the per-kernel durations.
     Returns the slowest rank's region-1 milliseconds, the mean milliseconds of
-    each call kind in region 2 and the calls of each kind per step."""
+    each call kind in region 2, the calls of each kind per step, and the
+    region-1b milliseconds (None without `graph`)."""
     import torch
     import torch.distributed as dist
 
@@ -309,6 +337,14 @@ def time_calls(calls, kinds, stream, steps, warmup, world, dev, check=()):
     for d in check:
         if binding.gdn_read_device_error(d.c) != 0:
             raise RuntimeError("device-side argument error during warm-up")
+    region1, reps = step, 1
+    if graph:
+        reps = -(-24 // len(calls))  # steps per replay
+        with torch.cuda.stream(stream):
+            region1 = graph_of(calls, stream, reps)
+            region1()
+        torch.cuda.synchronize()
+    runs = -(-steps // reps)  # region-1 iterations; steps_run = runs * reps
     n_per_step = {m: sum(1 for mm, _ in calls if mm == m) for m in kinds}
     events = {m: [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
                   for _ in range(n_per_step[m] * steps)] for m in kinds}
@@ -318,18 +354,28 @@ def time_calls(calls, kinds, stream, steps, warmup, world, dev, check=()):
     t_start = torch.cuda.Event(enable_timing=True)
     t_end = torch.cuda.Event(enable_timing=True)
     t_start.record(stream)
-    for _ in range(steps):
-        step()
+    for _ in range(runs):
+        region1()
     t_end.record(stream)
     torch.cuda.synchronize()
     barrier()
+    # the time of `steps` steps at the measured rate (runs * reps steps ran)
+    ms_total = max_over_ranks(t_start.elapsed_time(t_end), world, dev) * steps / (runs * reps)
+    ms_direct = None
+    if graph:
+        t_start.record(stream)
+        for _ in range(steps):
+            step()
+        t_end.record(stream)
+        torch.cuda.synchronize()
+        barrier()
+        ms_direct = max_over_ranks(t_start.elapsed_time(t_end), world, dev)
     for _ in range(steps):
         step(events)
     torch.cuda.synchronize()
     barrier()
-    ms_total = max_over_ranks(t_start.elapsed_time(t_end), world, dev)
     avg_ms = {m: statistics.fmean(a.elapsed_time(b) for a, b in events[m]) for m in kinds}
-    return ms_total, avg_ms, n_per_step
+    return ms_total, avg_ms, n_per_step, ms_direct
 
 
 def time_back_to_back(calls, kinds, stream, steps, world, dev):
@@ -396,9 +442,12 @@ def run_per_config(args, dev, stream, world):
             calls = ([("v", d.launcher("verify", stream)) for d in dps]
                      + [("c", d.launcher("commit", stream)) for d in dps])
         bytes_of = {m: [alg_bytes(pr, MODE_NAME[m]) for pr in probs] for m in kinds}
-        ms_total, avg_ms, n_per_step = time_calls(calls, kinds, stream, args.per_config_steps,
-                                                  args.warmup, world, dev, check=dps)
+        ms_total, avg_ms, n_per_step, ms_direct = time_calls(
+            calls, kinds, stream, args.per_config_steps, args.warmup, world, dev, check=dps,
+            graph=not args.no_graph)
         us_call = job_us_per_layer_call(ms_total, args.per_config_steps, n_inst, world)
+        us_direct = (None if ms_direct is None else
+                     job_us_per_layer_call(ms_direct, args.per_config_steps, n_inst, world))
         bytes_call = sum(sum(bytes_of[m]) for m in kinds) / n_inst
         gbs = bytes_call / (us_call * 1e-6) / 1e9
         dominant = max(kinds, key=lambda m: avg_ms[m] * n_per_step[m])
@@ -407,6 +456,7 @@ def run_per_config(args, dev, stream, world):
         out[name] = {
             "order": why,
             "us_per_layer_call": us_call,
+            "us_per_layer_call_launched_one_by_one": us_direct,
             "alg_bytes_per_layer_call": bytes_call,
             "achieved_gbs": gbs,
             "frac_of_measured_hbm": gbs / (peak * world),
@@ -451,6 +501,8 @@ def run_ours(args, rank, world, local_rank):
     if batched and not (multi and (fused or args.order == "engine")):
         raise SystemExit("--batch-layers needs a multi-layer workload and --mode fused or "
                          "--order engine")
+    if not args.no_graph:  # capture needs a stream other than the default one
+        torch.cuda.set_stream(torch.cuda.Stream(dev))
     stream = torch.cuda.current_stream(dev)
     per_layer = {m: [alg_bytes(pr, MODE_NAME[m]) for pr in layers] for m in ("v", "c", "f", "cv")}
     # bytes_of[kind]: algorithmic bytes of each launch of that kind in one step
@@ -515,14 +567,16 @@ def run_ours(args, rank, world, local_rank):
     clocks = ClockSampler(local_rank)
     clocks.start()
     time.sleep(0.3)
-    ms_total, avg_ms, n_per_step = time_calls(calls, kinds, stream, args.steps, args.warmup,
-                                              world, dev, check=dps)
+    ms_total, avg_ms, n_per_step, ms_direct = time_calls(
+        calls, kinds, stream, args.steps, args.warmup, world, dev, check=dps,
+        graph=not args.no_graph)
     b2b = None
     if len(kinds) > 1 and not args.replay:
         b2b = time_back_to_back(calls, kinds, stream, args.steps, world, dev)
     clk = clocks.stop()
     ms_step = ms_total / args.steps
     us_call = job_us_per_layer_call(ms_total, args.steps, L, world)
+    us_direct = None if ms_direct is None else job_us_per_layer_call(ms_direct, args.steps, L, world)
 
     dominant = max(kinds, key=lambda m: avg_ms[m] * n_per_step[m])
     per_launch_bytes = {m: sum(bytes_of[m]) / len(bytes_of[m]) for m in kinds}
@@ -577,6 +631,9 @@ def run_ours(args, rank, world, local_rank):
                           if args.order == "lagged" else
                           "all verifies then all commits"),
                 "l2": "inputs larger than L2 (each step touches ~%.1f GB)" % (bytes_call * L / 1e9),
+                "issue": ("each timed step replays the step's calls captured once in a CUDA graph "
+                          "(value_launched_one_by_one: the same calls launched one by one)"
+                          if us_direct is not None else "the calls launched one by one"),
                 "algo": {1: "recurrent", 2: "chunk", 3: "chunk_tc"}.get(algo_used, str(algo_used)),
                 "arith": ("fp32 state and outputs; the state-sized products on tensor cores "
                           "in bf16 on hi/lo splits of the fp32 operands (about 16 mantissa "
@@ -586,6 +643,7 @@ def run_ours(args, rank, world, local_rank):
                 "accepted": ("greedy prefix match of token ids on the device, every step"
                              if args.with_accept else "given (device array)"),
             },
+            "value_launched_one_by_one": us_direct,
             "achieved_gbs": gbs,
             "frac_of_8tbs": gbs / (NOMINAL_HBM_GBS * world),
             "frac_of_measured_hbm": gbs / (peak * world),
@@ -738,6 +796,10 @@ def main():
     ap.add_argument("--batch-layers", action="store_true",
                     help="all layers' commits (or fused calls) in one layer-batch launch")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-graph", action="store_true",
+                    help="time the headline loop with the calls launched one by one (default: "
+                         "replays of one step captured in a CUDA graph; the one-by-one figure "
+                         "is reported beside it)")
     ap.add_argument("--no-per-config", action="store_true",
                     help="skip the b32 and b128 ragged workloads timed after the headline")
     ap.add_argument("--per-config-steps", type=int, default=200)
