@@ -56,7 +56,7 @@ MODE_NAME = {"v": "verify", "c": "commit", "f": "fused", "cv": "commit_verify",
 
 # ----------------------------------------------------------------- accounting
 
-def alg_bytes(prob, mode: str) -> int:
+def alg_bytes(prob, mode: str, o_bytes: int = 4) -> int:
     """Minimum bytes the method moves for one call, per unit (request, head):
     verify  = state read + T (q, k, v, alpha, beta) + T o
     commit  = [a > 0] (state read + state write) + a (k, v, alpha, beta)
@@ -66,7 +66,7 @@ def alg_bytes(prob, mode: str) -> int:
     tile = prob.dk * prob.dv * 4
     q_k = prob.dk * esz
     v_ = prob.dv * esz
-    o_ = prob.dv * 4
+    o_ = prob.dv * o_bytes
     lens = prob.lengths.astype(np.int64)
     acc = prob.accepted.astype(np.int64)
     H = prob.heads
@@ -486,13 +486,16 @@ def run_ours(args, rank, world, local_rank):
     n_layers = inputs.WORKLOADS[name].get("layers", 1)
     if args.layers:
         n_layers = min(n_layers, args.layers)
-    layers = [inputs.make_problem(name, layer=l, draft=args.draft) for l in range(n_layers)]
+    layers = [inputs.make_problem(name, layer=l, draft=args.draft,
+                                  gate="log" if args.log_gate else "alpha")
+              for l in range(n_layers)]
     L = len(layers)
     p0 = layers[0]
     multi = "layers" in inputs.WORKLOADS[name]
     pool = staging.new_pool(p0.pool_slots, p0.heads, p0.dk, p0.dv, dev, fill="zero",
                             layers=L if multi else None)
-    dps = [staging.DeviceProblem(pr, dev, pool=(pool[l] if multi else pool), algo=args.algo)
+    dps = [staging.DeviceProblem(pr, dev, pool=(pool[l] if multi else pool), algo=args.algo,
+                                 o_bf16=args.o_bf16)
            for l, pr in enumerate(layers)]
     if multi:
         staging.share_request_arrays(dps)  # one step's requests, as an engine holds them
@@ -504,7 +507,9 @@ def run_ours(args, rank, world, local_rank):
     if not args.no_graph:  # capture needs a stream other than the default one
         torch.cuda.set_stream(torch.cuda.Stream(dev))
     stream = torch.cuda.current_stream(dev)
-    per_layer = {m: [alg_bytes(pr, MODE_NAME[m]) for pr in layers] for m in ("v", "c", "f", "cv")}
+    o_bytes = 2 if args.o_bf16 else 4
+    per_layer = {m: [alg_bytes(pr, MODE_NAME[m], o_bytes) for pr in layers]
+                 for m in ("v", "c", "f", "cv")}
     # bytes_of[kind]: algorithmic bytes of each launch of that kind in one step
     bytes_of = dict(per_layer, C=[sum(per_layer["c"])], F=[sum(per_layer["f"])])
     replay_bufs = None
@@ -591,7 +596,8 @@ def run_ours(args, rank, world, local_rank):
            if not (args.no_e2e or batched or args.replay or args.order == "lagged") else None)
     per_config = None
     if not (args.no_per_config or args.replay or args.draft or args.layers or batched
-            or args.order != "interleaved" or args.workload != WORKLOAD):
+            or args.order != "interleaved" or args.workload != WORKLOAD
+            or args.o_bf16 or args.log_gate):
         per_config = run_per_config(args, dev, stream, world)
 
     cpu = None
@@ -642,6 +648,9 @@ def run_ours(args, rank, world, local_rank):
                           else "fp32 on CUDA cores"),
                 "accepted": ("greedy prefix match of token ids on the device, every step"
                              if args.with_accept else "given (device array)"),
+                "variant": ", ".join(v for v, on in (("bf16 o", args.o_bf16),
+                                                     ("log-space gates", args.log_gate)) if on)
+                           or "none",
             },
             "value_launched_one_by_one": us_direct,
             "achieved_gbs": gbs,
@@ -796,6 +805,8 @@ def main():
     ap.add_argument("--batch-layers", action="store_true",
                     help="all layers' commits (or fused calls) in one layer-batch launch")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--o-bf16", action="store_true", help="the bf16-output variant")
+    ap.add_argument("--log-gate", action="store_true", help="the log-space gate variant")
     ap.add_argument("--no-graph", action="store_true",
                     help="time the headline loop with the calls launched one by one (default: "
                          "replays of one step captured in a CUDA graph; the one-by-one figure "

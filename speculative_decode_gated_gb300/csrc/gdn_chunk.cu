@@ -1690,7 +1690,20 @@ cudaError_t launch_layers(const Args *layers, int n, int mode, cudaStream_t stre
                                   : launch_mode<kFused, false, NL, true, false, true, true>(L, stream);
             }
         }
-        if (layers[0].flags != 0) {  // variants: one multi-chunk instantiation for any length
+        if (layers[0].flags != 0) {  // variants: single-chunk and multi-chunk instantiations
+            if (layers[0].max_T <= CT) {
+                switch (mode) {
+                    case kVerify:
+                        return ragged ? launch_mode<kVerify, true, NL, false, false, true>(L, stream)
+                                      : launch_mode<kVerify, false, NL, false, false, true>(L, stream);
+                    case kCommit:
+                        return ragged ? launch_mode<kCommit, true, NL, false, false, true>(L, stream)
+                                      : launch_mode<kCommit, false, NL, false, false, true>(L, stream);
+                    default:
+                        return ragged ? launch_mode<kFused, true, NL, false, false, true>(L, stream)
+                                      : launch_mode<kFused, false, NL, false, false, true>(L, stream);
+                }
+            }
             switch (mode) {
                 case kVerify:
                     return ragged ? launch_mode<kVerify, true, NL, true, false, true>(L, stream)

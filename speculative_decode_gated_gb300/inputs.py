@@ -209,16 +209,18 @@ def _recipe_kwargs(name: str) -> dict:
     return spec
 
 
-def make_problem(name: str, layer: int = 0, draft: Optional[int] = None) -> Problem:
+def make_problem(name: str, layer: int = 0, draft: Optional[int] = None,
+                 gate: str = "alpha") -> Problem:
     """The named workload (one layer of it for the multi-layer one).  `draft`
     replaces the draft length of a uniform workload (accepted lengths keep
-    their distribution, over the new length)."""
+    their distribution, over the new length); gate="log" draws the same decay
+    in log space (the log-gate variant)."""
     kw = _recipe_kwargs(name)
     if draft is not None:
         if "T" not in kw:
             raise ValueError(f"{name} has ragged drafts")
         kw["T"] = int(draft)
-    return make_custom(name=name, layer=layer, **kw)
+    return make_custom(name=name, layer=layer, gate=gate, **kw)
 
 
 def make_layers(name: str) -> List[Problem]:
