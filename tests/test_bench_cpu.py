@@ -101,3 +101,26 @@ def test_clock_samples_report_each_active_reason_once():
 def test_clock_sampler_without_nvidia_smi_reports_nothing():
     s = bench.ClockSampler(0)
     assert s.stop() is None
+
+
+def test_algorithmic_bytes_follow_the_per_unit_formulas():
+    """The roofline's byte count: per unit (request, head), with dk = dv = 128,
+    bf16 q/k/v and fp32 gates, state and o,
+      verify = 65536 + T (768 + 8) + T 512
+      commit = [a > 0] 2 * 65536 + a (512 + 8)
+      fused  = 65536 + [a > 0] 65536 + T (768 + 8 + 512)
+    plus per-request metadata; bf16 o halves the o term."""
+    from speculative_decode_gated_gb300 import inputs
+    prob = inputs.make_custom(batch=3, heads=2, dk=128, dv=128, lengths=[16, 5, 9],
+                              qkv_dtype="bf16", pool_slots=4, accepted=[0, 5, 3], seed=1,
+                              name="bytes")
+    T, a, H, B = prob.lengths.astype(int), prob.accepted.astype(int), 2, 3
+    ragged_meta = 4
+    verify = H * sum(65536 + t * (768 + 8) + t * 512 for t in T) + B * (4 + ragged_meta)
+    commit = H * sum((x > 0) * 2 * 65536 + x * (512 + 8) for x in a) + B * (4 + 4 + ragged_meta)
+    fused = H * sum(65536 + (x > 0) * 65536 + t * (768 + 8 + 512) for t, x in zip(T, a)) \
+        + B * (4 + 4 + ragged_meta)
+    assert bench.alg_bytes(prob, "verify") == verify
+    assert bench.alg_bytes(prob, "commit") == commit
+    assert bench.alg_bytes(prob, "fused") == fused
+    assert bench.alg_bytes(prob, "verify", o_bytes=2) == verify - H * sum(T) * 128 * 2
