@@ -285,7 +285,9 @@ def graph_of(calls, stream, reps=1):
 
     g = torch.cuda.CUDAGraph()
     torch.cuda.synchronize()
-    with torch.cuda.graph(g, stream=stream):
+    # thread-local capture: other threads of the process (NCCL's watchdog under
+    # torchrun) may keep querying their own events meanwhile
+    with torch.cuda.graph(g, stream=stream, capture_error_mode="thread_local"):
         for _ in range(reps):
             for _, call in calls:
                 call()
