@@ -147,7 +147,7 @@ def _check(t: Optional[torch.Tensor], name: str, dtypes, device) -> None:
         raise ValueError(f"{name} is on {t.device}, expected {device}")
 
 
-def make_problem(*, q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, alpha: torch.Tensor,
+def make_problem(*, q: Optional[torch.Tensor], k: torch.Tensor, v: torch.Tensor, alpha: torch.Tensor,
                  beta: torch.Tensor, pool: torch.Tensor, slot_ids: torch.Tensor,
                  max_T: int, cu_seqlens: Optional[torch.Tensor] = None,
                  dev_err: Optional[torch.Tensor] = None, algo: int = GDN_ALGO_AUTO,
@@ -157,13 +157,15 @@ def make_problem(*, q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, alpha: to
     q, k: [N_tok, H, dk]; v: [N_tok, H, dv] (bf16 or fp32, same dtype);
     alpha, beta: [N_tok, H] fp32; pool: [slots, H, dk, dv] fp32; slot_ids: [B] int32;
     cu_seqlens: [B+1] int32 or None (uniform length max_T); dev_err: [1] int32 or None.
-    flags: GDN_FLAG_* bits (bf16 o, log-space alpha).
+    flags: GDN_FLAG_* bits (bf16 o, log-space alpha).  q may be None for a problem
+    that only commits (the commit calls read no q).
     """
     dev = pool.device
-    if q.dtype not in (torch.bfloat16, torch.float32) or k.dtype != q.dtype or v.dtype != q.dtype:
+    if k.dtype not in (torch.bfloat16, torch.float32) or v.dtype != k.dtype or \
+            (q is not None and q.dtype != k.dtype):
         raise TypeError("q, k, v must all be bf16 or all fp32")
     for t, n in ((q, "q"), (k, "k"), (v, "v")):
-        _check(t, n, (q.dtype,), dev)
+        _check(t, n, (k.dtype,), dev)
     _check(alpha, "alpha", (torch.float32,), dev)
     _check(beta, "beta", (torch.float32,), dev)
     _check(pool, "pool", (torch.float32,), dev)
@@ -177,7 +179,7 @@ def make_problem(*, q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, alpha: to
     c.batch = slot_ids.numel()
     c.heads, c.dk, c.dv = H, dk, dv
     c.max_T = int(max_T)
-    c.qkv_dtype = GDN_BF16 if q.dtype == torch.bfloat16 else GDN_FP32
+    c.qkv_dtype = GDN_BF16 if k.dtype == torch.bfloat16 else GDN_FP32
     c.algo = int(algo)
     c.flags = int(flags)
     c.cu_seqlens = _ptr(cu_seqlens)
@@ -187,7 +189,7 @@ def make_problem(*, q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, alpha: to
     c.pool_slots = slots
     c.slot_ids = _ptr(slot_ids)
     c.dev_err = _ptr(dev_err)
-    c.n_tok = q.shape[0]
+    c.n_tok = k.shape[0]
     return Problem(c, (q, k, v, alpha, beta, pool, slot_ids, cu_seqlens, dev_err))
 
 

@@ -235,3 +235,24 @@ def test_extreme_gates(algo):
     d = staging.DeviceProblem(prob, "cuda", algo=algo)
     check_verify(d, units, o_ref)
     check_state_update(d, units, s_ref, d.commit)
+
+
+@pytest.mark.parametrize("algo", [AUTO, REC], ids=["auto", "rec"])
+def test_commit_without_q(algo):
+    """The commit calls read no q: a problem given none (q = NULL) commits the
+    same bits as one given q."""
+    prob = inputs.make_custom(batch=5, heads=3, dk=128, dv=128, lengths=[16, 3, 0, 9, 12],
+                              qkv_dtype="bf16", pool_slots=8, accept="uniform", seed=91,
+                              name="commit_no_q")
+    with_q = staging.DeviceProblem(prob, "cuda", algo=algo)
+    no_q = staging.DeviceProblem(prob, "cuda", algo=algo)
+    c = binding.make_problem(q=None, k=no_q.k, v=no_q.v, alpha=no_q.alpha, beta=no_q.beta,
+                             pool=no_q.pool, slot_ids=no_q.slot_ids, max_T=prob.max_T,
+                             cu_seqlens=no_q.cu_seqlens, dev_err=no_q.dev_err, algo=algo)
+    with_q.commit()
+    binding.gdn_commit(c, no_q.accepted)
+    torch.cuda.synchronize()
+    assert binding.gdn_read_device_error(c) == 0
+    assert torch.equal(with_q.pool.view(torch.int32), no_q.pool.view(torch.int32))
+    with pytest.raises(binding.GdnError):  # verify needs q
+        binding.gdn_verify(c, no_q.o)
