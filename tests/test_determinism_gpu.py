@@ -57,3 +57,30 @@ def test_full_size_launches_are_bitwise_repeatable(name, mode):
             if prob.accepted[r] > 0:
                 worst = max(worst, rel_err(got[prob.slot_ids[r], h], s_ref[u]))
         assert worst <= TOL
+
+
+@pytest.mark.parametrize("name", ["b64_h32_d128_t16_x24", "b128_h32_d128_ragged16"])
+def test_commit_then_verify_is_bitwise_repeatable(name):
+    """gdn_commit_verify folds the previous step's prefix into the state inside
+    its first product and stores it there: the same race detector for its
+    tile reads."""
+    prob = inputs.make_problem(name, layer=0)
+    results = []
+    for _ in range(RUNS):
+        d = staging.DeviceProblem(prob, "cuda")
+        w_prev = torch.zeros((prob.n_tok, prob.heads, prob.dv), device="cuda")
+        w = torch.zeros_like(w_prev)
+        binding.gdn_commit_verify(d.c, None, d.o, w_prev)  # the previous step's W
+        prev = binding.make_prev_step(k=d.k, alpha=d.alpha, w=w_prev, accepted=d.accepted,
+                                      max_T=prob.max_T, cu_seqlens=d.cu_seqlens)
+        d.o.fill_(float("nan"))
+        binding.gdn_commit_verify(d.c, prev, d.o, w)
+        torch.cuda.synchronize()
+        assert binding.gdn_read_device_error(d.c) == 0
+        results.append((d.o.clone(), d.pool.clone(), w.clone()))
+        del d
+    o0, p0, w0 = results[0]
+    for o, pool, wv in results[1:]:
+        assert torch.equal(o.view(torch.int32), o0.view(torch.int32)), "o differs between runs"
+        assert torch.equal(pool.view(torch.int32), p0.view(torch.int32)), "states differ"
+        assert torch.equal(wv.view(torch.int32), w0.view(torch.int32)), "W differs between runs"
