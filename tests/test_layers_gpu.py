@@ -147,3 +147,50 @@ def test_layers_mismatch_rejected_before_launch():
     with pytest.raises(binding.GdnError) as e:
         binding.gdn_commit_layers(arr, dps[0].accepted)
     assert e.value.status == binding.GDN_ERR_LAYER_MISMATCH
+
+
+@pytest.mark.parametrize("mode", ["verify", "commit", "fused"])
+def test_full_size_layer_batch(mode):
+    """The 24-layer workload in one layer-batch launch: 24 x 2048 units, about
+    160 rounds of the persistent grid.  Bit for bit equal to the 24 single
+    calls, and the last layer (whose units come last in the launch) against
+    the oracle on every unit."""
+    probs = inputs.make_layers("b64_h32_d128_t16_x24")
+    pool, dps, arr = stage(probs)
+    pool_single = pool.clone()
+    for d in dps:
+        d.o.fill_(float("nan"))
+    acc = dps[0].accepted
+    if mode == "verify":
+        binding.gdn_verify_layers(arr, [d.o for d in dps])
+    elif mode == "commit":
+        binding.gdn_commit_layers(arr, acc)
+    else:
+        binding.gdn_verify_commit_fused_layers(arr, acc, [d.o for d in dps])
+    torch.cuda.synchronize()
+    for d in dps:
+        assert binding.gdn_read_device_error(d.c) == 0
+    outs = [d.o.clone() for d in dps] if mode != "commit" else None
+    batched = pool.clone()
+    # the last layer against the oracle
+    last = probs[-1]
+    units = np.arange(last.units)
+    o_ref, s_ref = oracle_units(last, units)
+    if mode != "commit":
+        err = rel_err(gather_outputs(last, units, outs[-1].cpu().numpy(), o_ref), o_ref)
+        assert err <= TOL, f"last layer o: {err:.3e}"
+    if mode != "verify":
+        check_layer_state(last, pool_single[-1].cpu().numpy(), batched[-1].cpu().numpy(),
+                          units, s_ref)
+    # the single-problem calls on a copy of the pool
+    pool.copy_(pool_single)
+    for d in dps:
+        d.o.fill_(float("nan"))
+        {"verify": d.verify, "commit": d.commit, "fused": d.fused}[mode]()
+    torch.cuda.synchronize()
+    assert torch.equal(pool.view(torch.int32), batched.view(torch.int32))
+    if outs is not None:
+        for l, d in enumerate(dps):
+            assert torch.equal(d.o.view(torch.int32), outs[l].view(torch.int32)), f"layer {l}"
+    del pool, pool_single, batched, dps, arr
+    torch.cuda.empty_cache()
