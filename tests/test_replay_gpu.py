@@ -3,6 +3,7 @@ against the float64 oracle: single steps with buffered lengths from empty to
 full and buffers of many chunks, then a run of steps in which the GPU's own
 buffer lengths and pool carry from one step to the next (each step compared
 with the oracle fed the GPU's state), and bad lengths."""
+import os
 import numpy as np
 import pytest
 import torch
@@ -125,3 +126,39 @@ def test_replay_bad_length_is_flagged_and_skipped():
     c0 = int(prob.cu_seqlens[0])
     assert np.isnan(o[c0:c0 + 16]).all()          # request 0: nothing written
     assert not np.isnan(o[int(prob.cu_seqlens[1]):]).any()
+
+
+@pytest.mark.parametrize("cap", [32, 64])
+def test_replay_full_size(cap):
+    """The 24-layer workload's batch, heads and draft length (2048 units, the
+    benchmark's grid and rounds; a 64-slot pool keeps the oracle's copy small)
+    with C buffered rows per slot: every unit's outputs and every flushed
+    slot against the oracle, untouched slots bit for bit, the new lengths
+    exactly."""
+    prob = inputs.make_custom(name="replay_full", batch=64, heads=32, dk=128, dv=128, T=16,
+                              qkv_dtype="bf16", pool_slots=64, accept="binom", seed=1003)
+    buf = inputs.make_replay(prob, cap, seed=9)
+    d = staging.DeviceProblem(prob, "cuda")
+    r = staging.DeviceReplay(buf, prob.qkv_dtype)
+    pool = d.pool.double().cpu().numpy()
+    want_o = oracle.replay_verify(prob, buf, pool, threads=os.cpu_count() or 1)
+    want_pool, want_len, flushed = oracle.replay_commit(prob, buf, pool,
+                                                        threads=os.cpu_count() or 1)
+    before = d.pool.cpu().numpy()
+    d.o.fill_(float("nan"))
+    binding.gdn_replay_verify(d.c, r.c, d.o)
+    binding.gdn_replay_commit(d.c, r.c, d.accepted)
+    torch.cuda.synchronize()
+    assert binding.gdn_read_device_error(d.c) == 0
+    err = rel_err(d.o.cpu().numpy(), want_o)
+    assert err <= TOL, f"o: {err:.3e}"
+    assert np.array_equal(r.len_out.cpu().numpy(), want_len)
+    after = d.pool.cpu().numpy()
+    flushed_slots = {int(prob.slot_ids[i]) for i in np.flatnonzero(flushed)}
+    assert flushed_slots  # the flush branch is exercised
+    for s in range(prob.pool_slots):
+        if s in flushed_slots:
+            e = rel_err(after[s], want_pool[s])
+            assert e <= TOL, f"slot {s}: {e:.3e}"
+        else:
+            assert np.array_equal(after[s].view(np.int32), before[s].view(np.int32))
