@@ -256,3 +256,44 @@ def test_commit_without_q(algo):
     assert torch.equal(with_q.pool.view(torch.int32), no_q.pool.view(torch.int32))
     with pytest.raises(binding.GdnError):  # verify needs q
         binding.gdn_verify(c, no_q.o)
+
+
+def test_full_size_long_drafts():
+    """32-token drafts on the 24-layer workload's shape (two 16-token chunks per
+    unit, the multi-chunk kernel over 2048 units): every unit against the
+    oracle, verify then commit and fused."""
+    prob = inputs.make_problem("b64_h32_d128_t16_x24", layer=0, draft=32)
+    units = np.arange(prob.units)
+    o_ref, s_ref = oracle_units(prob, units)
+    d = staging.DeviceProblem(prob, "cuda")
+    check_verify(d, units, o_ref)
+    check_state_update(d, units, s_ref, d.commit)
+    f = staging.DeviceProblem(prob, "cuda")
+    f.o.fill_(float("nan"))
+    check_state_update(f, units, s_ref, f.fused)
+    assert rel_err(gather_outputs(prob, units, f.o.cpu().numpy(), o_ref), o_ref) <= TOL
+
+
+@pytest.mark.parametrize("o_bf16,gate", [(False, "log"), (True, "alpha"), (True, "log")],
+                         ids=["log_gate", "bf16_o", "both"])
+def test_full_size_variants(o_bf16, gate):
+    """The precision variants on one layer of the 24-layer workload (their own
+    single-chunk instantiations): every unit against the oracle; bf16 o within
+    the float32 tolerance plus one bfloat16 rounding."""
+    prob = inputs.make_problem("b64_h32_d128_t16_x24", layer=0, gate=gate)
+    units = np.arange(prob.units)
+    o_ref, s_ref = oracle_units(prob, units)
+    tol_o = TOL + 2.0 ** -9 * (1.0 + TOL) if o_bf16 else TOL
+    d = staging.DeviceProblem(prob, "cuda", o_bf16=o_bf16)
+    d.o.fill_(float("nan"))
+    d.verify()
+    torch.cuda.synchronize()
+    assert binding.gdn_read_device_error(d.c) == 0
+    err = rel_err(gather_outputs(prob, units, d.o.float().cpu().numpy(), o_ref), o_ref)
+    assert err <= tol_o, f"verify o: {err:.3e}"
+    check_state_update(d, units, s_ref, d.commit)
+    f = staging.DeviceProblem(prob, "cuda", o_bf16=o_bf16)
+    f.o.fill_(float("nan"))
+    check_state_update(f, units, s_ref, f.fused)
+    err = rel_err(gather_outputs(prob, units, f.o.float().cpu().numpy(), o_ref), o_ref)
+    assert err <= tol_o, f"fused o: {err:.3e}"
