@@ -406,17 +406,36 @@ def time_back_to_back(calls, kinds, stream, steps, world, dev):
             for m in kinds}
 
 
-# The other target workloads, timed in the same run as the headline: name,
-# call order, independent instances cycled through (each with its own pool and
-# inputs), and why.
-PER_CONFIG = [
-    ("b32_h32_d128_t16", "engine", 8,
-     "8 instances (own pools and tokens); all verifies, then all commits, so that no "
-     "commit re-reads in L2 a checkpoint its verify just read (one instance's "
-     "checkpoints, 64 MiB, would fit in the 129 MB L2)"),
-    ("b128_h32_d128_ragged16", "fused", 2,
-     "2 instances alternating, fused verify+commit per call (541 MB per call)"),
-]
+# Single-layer workloads run as independent instances (each with its own pool
+# and inputs) cycled through, all verifies before all commits: one instance's
+# checkpoints fit in the 129 MB L2 on b8 (8 MiB) and b32 (64 MiB), and a commit
+# issued right after its own verify would re-read them there.  In an engine the
+# other layers' work runs between a layer's verify and its commit.
+INSTANCES = {"b8_h16_d128_t8": 24, "b32_h32_d128_t16": 8, "b128_h32_d128_ragged16": 2}
+
+
+def instances_of(name: str, requested: int = 0) -> int:
+    """How many instances a run of the named workload cycles through: 1 for the
+    multi-layer workload (its layers already have their own pools)."""
+    if "layers" in inputs.WORKLOADS[name]:
+        if requested > 1:
+            raise SystemExit(f"{name} has layers of its own; --instances applies to "
+                             "single-layer workloads")
+        return 1
+    return requested if requested > 0 else INSTANCES.get(name, 1)
+
+
+def instance_note(name: str, n: int, fused: bool) -> str:
+    if n == 1:
+        return "1 instance"
+    return (f"{n} instances (own pools and tokens), "
+            + ("fused calls in turn" if fused else
+               "all verifies, then all commits, so that no commit re-reads in L2 a "
+               "checkpoint its verify just read"))
+
+
+# The other target workloads, timed in the same run as the headline.
+PER_CONFIG = [("b32_h32_d128_t16", "engine"), ("b128_h32_d128_ragged16", "fused")]
 
 
 def run_per_config(args, dev, stream, world):
@@ -429,7 +448,9 @@ def run_per_config(args, dev, stream, world):
 
     peak, peak_kind = measured_peaks()
     out = {}
-    for name, order, n_inst, why in PER_CONFIG:
+    for name, order in PER_CONFIG:
+        n_inst = instances_of(name)
+        why = instance_note(name, n_inst, order == "fused")
         probs = [inputs.make_problem(name, layer=l) for l in range(n_inst)]
         p0 = probs[0]
         pool = staging.new_pool(p0.pool_slots, p0.heads, p0.dk, p0.dv, dev, fill="zero",
@@ -485,7 +506,9 @@ def run_ours(args, rank, world, local_rank):
     torch.cuda.set_device(dev)
     binding.lib()  # fails loudly if the CUDA library is missing
     name = args.workload
-    n_layers = inputs.WORKLOADS[name].get("layers", 1)
+    multi = "layers" in inputs.WORKLOADS[name]
+    # layers of the multi-layer workload, or independent instances of a single-layer one
+    n_layers = inputs.WORKLOADS[name]["layers"] if multi else args.instances
     if args.layers:
         n_layers = min(n_layers, args.layers)
     layers = [inputs.make_problem(name, layer=l, draft=args.draft,
@@ -493,10 +516,9 @@ def run_ours(args, rank, world, local_rank):
               for l in range(n_layers)]
     L = len(layers)
     p0 = layers[0]
-    multi = "layers" in inputs.WORKLOADS[name]
     pool = staging.new_pool(p0.pool_slots, p0.heads, p0.dk, p0.dv, dev, fill="zero",
-                            layers=L if multi else None)
-    dps = [staging.DeviceProblem(pr, dev, pool=(pool[l] if multi else pool), algo=args.algo,
+                            layers=L if L > 1 else None)
+    dps = [staging.DeviceProblem(pr, dev, pool=(pool[l] if L > 1 else pool), algo=args.algo,
                                  o_bf16=args.o_bf16)
            for l, pr in enumerate(layers)]
     if multi:
@@ -626,7 +648,10 @@ def run_ours(args, rank, world, local_rank):
             "config": {
                 "workload": name,
                 "description": (f"batch {p0.batch}, heads {p0.heads}, dk {p0.dk}, dv {p0.dv}, "
-                                f"draft {p0.max_T}, {L} layer(s), pool {p0.pool_slots} slots/layer, "
+                                f"draft {p0.max_T}, "
+                                + (f"{L} layer(s)" if multi else
+                                   instance_note(name, L, fused and not args.replay))
+                                + f", pool {p0.pool_slots} slots/layer, "
                                 f"q/k/v {p0.qkv_dtype}, gates/state/o fp32"),
                 "order": (f"ReplaySSM buffer of {args.replay} rows per slot: replay verify then "
                           "replay commit per layer; buffered lengths uniform on [0, C - T] "
@@ -786,7 +811,15 @@ def main():
     ap.add_argument("--workload", default=WORKLOAD, choices=sorted(inputs.WORKLOADS))
     ap.add_argument("--mode", choices=["separate", "fused"], default=None,
                     help="separate verify + commit (default) or the fused call")
-    ap.add_argument("--order", choices=["interleaved", "engine", "lagged"], default="interleaved")
+    ap.add_argument("--order", choices=["interleaved", "engine", "lagged"], default=None,
+                    help="separate calls: verify then commit per layer (interleaved; the "
+                         "default for the multi-layer workload), all verifies then all commits "
+                         "(engine; the default for instances of a single-layer workload), or "
+                         "one commit-then-verify call per layer (lagged)")
+    ap.add_argument("--instances", type=int, default=0,
+                    help="independent instances of a single-layer workload cycled through "
+                         "(0: the workload's default, enough that no commit finds its "
+                         "checkpoints in L2)")
     ap.add_argument("--algo", type=int, default=0,
                     help="0 auto, 1 recurrent, 2 chunk (mma.sync), 3 chunk (tcgen05)")
     ap.add_argument("--layers", type=int, default=0,
@@ -819,6 +852,9 @@ def main():
     args = ap.parse_args()
     if args.mode is None:
         args.mode = "fused" if "ragged" in args.workload else "separate"
+    args.instances = instances_of(args.workload, args.instances)
+    if args.order is None:
+        args.order = "engine" if args.instances > 1 and not args.replay else "interleaved"
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
 

@@ -124,3 +124,27 @@ def test_algorithmic_bytes_follow_the_per_unit_formulas():
     assert bench.alg_bytes(prob, "commit") == commit
     assert bench.alg_bytes(prob, "fused") == fused
     assert bench.alg_bytes(prob, "verify", o_bytes=2) == verify - H * sum(T) * 128 * 2
+
+
+def test_single_layer_workloads_cycle_instances_past_l2():
+    """A single-layer workload runs as independent instances, all verifies
+    before all commits, so that between an instance's verify and its commit
+    the other instances' verifies move more than the 129 MB L2 (its
+    checkpoints are then read from HBM again, as between layers in an
+    engine); the multi-layer workload keeps its own layers."""
+    from speculative_decode_gated_gb300 import inputs
+    l2 = 129e6
+    assert bench.instances_of(bench.WORKLOAD) == 1
+    with pytest.raises(SystemExit):
+        bench.instances_of(bench.WORKLOAD, 2)
+    assert bench.instances_of("b32_h32_d128_t16", 1) == 1
+    for name, _ in bench.PER_CONFIG:
+        assert bench.instances_of(name) == bench.INSTANCES[name]
+    for name, n in bench.INSTANCES.items():
+        assert "layers" not in inputs.WORKLOADS[name]
+        prob = inputs.make_problem(name)
+        checkpoints = prob.units * prob.dk * prob.dv * 4
+        if "ragged" in name:  # fused calls: an instance's next call follows the others' calls
+            assert (n - 1) * bench.alg_bytes(prob, "fused") > l2 or checkpoints > 2 * l2
+        else:
+            assert checkpoints < l2 and (n - 1) * bench.alg_bytes(prob, "verify") > l2
