@@ -512,7 +512,7 @@ def run_ours(args, rank, world, local_rank):
     if args.layers:
         n_layers = min(n_layers, args.layers)
     layers = [inputs.make_problem(name, layer=l, draft=args.draft,
-                                  gate="log" if args.log_gate else "alpha")
+                                  gate="log" if args.log_gate else "alpha", batch=args.batch)
               for l in range(n_layers)]
     L = len(layers)
     p0 = layers[0]
@@ -614,12 +614,16 @@ def run_ours(args, rank, world, local_rank):
     algo_used = binding.gdn_select_algo(dps[0].c)
     ktag = ({binding.GDN_ALGO_CHUNK: "gdn_chunk", binding.GDN_ALGO_CHUNK_TC: "gdn_chunk_tc"}
             .get(algo_used, "gdn_recurrent") + "_" + MODE_NAME[dominant])
-    traffic = profile_traffic(ktag, name)
+    # the committed captures are of the named workloads' own launches (default
+    # instantiation, full layer count); a changed shape or variant has none
+    traffic = (None if (args.batch or args.draft or args.o_bf16 or args.log_gate or args.replay
+                        or (batched and args.layers))
+               else profile_traffic(ktag, name))
 
     e2e = (run_e2e(args, dps, stream, dev, fused, world)
            if not (args.no_e2e or batched or args.replay or args.order == "lagged") else None)
     per_config = None
-    if not (args.no_per_config or args.replay or args.draft or args.layers or batched
+    if not (args.no_per_config or args.replay or args.draft or args.batch or args.layers or batched
             or args.order != "interleaved" or args.workload != WORKLOAD
             or args.o_bf16 or args.log_gate):
         per_config = run_per_config(args, dev, stream, world)
@@ -646,7 +650,7 @@ def run_ours(args, rank, world, local_rank):
             "higher_is_better": False, "scaling": "weak", "vs_baseline": None,
             "dtype": "f32", "data": "synthetic",
             "config": {
-                "workload": name,
+                "workload": name if args.batch is None else f"{name} with batch {p0.batch}",
                 "description": (f"batch {p0.batch}, heads {p0.heads}, dk {p0.dk}, dv {p0.dv}, "
                                 f"draft {p0.max_T}, "
                                 + (f"{L} layer(s)" if multi else
@@ -832,6 +836,9 @@ def main():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--replay", type=int, default=0, metavar="C",
                     help="time the ReplaySSM buffer calls with C buffer rows per slot")
+    ap.add_argument("--batch", type=int, default=None,
+                    help="replace the number of requests of a uniform workload (a sweep of "
+                         "the unit count against the 304 resident blocks)")
     ap.add_argument("--draft", type=int, default=None,
                     help="replace the draft length of a uniform workload (longer drafts run as "
                          "several 16-token chunks)")

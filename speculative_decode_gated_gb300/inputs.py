@@ -210,16 +210,23 @@ def _recipe_kwargs(name: str) -> dict:
 
 
 def make_problem(name: str, layer: int = 0, draft: Optional[int] = None,
-                 gate: str = "alpha") -> Problem:
+                 gate: str = "alpha", batch: Optional[int] = None) -> Problem:
     """The named workload (one layer of it for the multi-layer one).  `draft`
     replaces the draft length of a uniform workload (accepted lengths keep
-    their distribution, over the new length); gate="log" draws the same decay
-    in log space (the log-gate variant)."""
+    their distribution, over the new length); `batch` replaces its number of
+    requests (at most its pool's slots); gate="log" draws the same decay in
+    log space (the log-gate variant)."""
     kw = _recipe_kwargs(name)
     if draft is not None:
         if "T" not in kw:
             raise ValueError(f"{name} has ragged drafts")
         kw["T"] = int(draft)
+    if batch is not None:
+        if "T" not in kw:
+            raise ValueError(f"{name} has ragged drafts")
+        if not 1 <= int(batch) <= kw["pool_slots"]:
+            raise ValueError(f"batch {batch} outside 1..{kw['pool_slots']}")
+        kw["batch"] = int(batch)
     return make_custom(name=name, layer=layer, gate=gate, **kw)
 
 

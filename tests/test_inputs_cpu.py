@@ -96,3 +96,19 @@ def test_token_ids_reproduce_accepted_lengths():
         while a < T and draft[c0 + a] == target[c0 + a]:
             a += 1
         assert a == p.accepted[r]
+
+
+def test_batch_override_keeps_the_recipe():
+    """`batch` replaces only the number of requests of a uniform workload."""
+    from speculative_decode_gated_gb300 import inputs
+    base = inputs.make_problem("b32_h32_d128_t16")
+    p = inputs.make_problem("b32_h32_d128_t16", batch=19)
+    assert p.batch == 19 and p.units == 19 * 32
+    assert (p.heads, p.dk, p.dv, p.max_T, p.pool_slots) == \
+        (base.heads, base.dk, base.dv, base.max_T, base.pool_slots)
+    assert len(set(p.slot_ids.tolist())) == 19
+    for bad in (0, base.pool_slots + 1):
+        with pytest.raises(ValueError):
+            inputs.make_problem("b32_h32_d128_t16", batch=bad)
+    with pytest.raises(ValueError):
+        inputs.make_problem("b128_h32_d128_ragged16", batch=64)
